@@ -1,0 +1,367 @@
+"""MLA decode benchmark: one JSON line per run.
+
+A step is one pass of the whole decode hot path over the DeepSeek-V2-shaped
+workload (batch 64, 128 heads, d_h 128, d_c 512, d_h^R 64, 4096 cached tokens
+per sequence, bf16 cache, one query token): mla_append_cache (this step's 64
+tokens) -> mla_absorb_q -> mla_decode (+ combine) -> mla_unabsorb.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`value` is latent-KV throughput: bytes of latent cache the step's attention
+reads (sum_b L_b * 1152 B) per second of step time, inputs resident in HBM.
+L2 is flushed (a 2x-L2 buffer write) before every timed step, outside the
+step's events. `e2e` is the same metric through the public API with pinned
+HOST inputs copied in and the output copied back inside the timed region.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload. With N > 1 each rank runs an independent replica (the path has no
+exchange step), so `scaling` is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode: latent-KV GB/s & TFLOPS vs B300 roofline; µs per decode step"
+WORKLOAD_ID = 2
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def _workload_sizes(wl):
+    bytes_per_tok = {"bf16": (wl.C + wl.R) * 2, "f32": (wl.C + wl.R) * 4,
+                     "fp8": wl.C + 2 * wl.R + 4 * (wl.C // 128)}[wl.cache]
+    act = 2 if wl.act == "bf16" else 4
+    cache_bytes = sum(wl.seq_lens) * bytes_per_tok
+    qo_bytes = wl.B * wl.n_q * wl.H * ((wl.C + wl.R) + wl.C) * act + wl.B * wl.n_q * wl.H * 4
+    # QK^T over C+R plus P.V over C, per head, per query row, per visible token
+    flops = sum(2 * wl.H * (2 * wl.C + wl.R) * (L - wl.n_q + 1 + j)
+                for L in wl.seq_lens for j in range(wl.n_q))
+    return cache_bytes, qo_bytes, flops
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_oracle_sample(wl, budget_s: float = 12.0, max_heads: int = 128):
+    """Time the fp64 oracle (as it stands) on whole heads of sequence 0, then 1, ...
+    until about budget_s of CPU work. Returns (GB/s equivalent, sample description, threads)."""
+    from oracle import mla_oracle as O
+
+    w_uk, w_uv = wl.weights()
+    q_c, q_r = wl.queries()
+    bytes_per_tok = (wl.C + wl.R) * 2 if wl.cache == "bf16" else wl.C + 2 * wl.R + 4 * (wl.C // 128)
+    done_bytes, heads_done, seqs = 0.0, 0, 0
+    t_total = 0.0
+    for b in range(wl.B):
+        c, r = wl.latents(b)
+        L = wl.seq_lens[b]
+        ce = O.cache_entries(c, r, np.arange(L), wl.cache, wl.rope_base)
+        seqs += 1
+        for h0 in range(0, wl.H, 8):
+            heads = np.arange(h0, min(wl.H, h0 + 8))
+            t0 = time.perf_counter()
+            O.mla_decode_naive(ce["c"], ce["k_r"], q_c[b], q_r[b], w_uk, w_uv, wl.positions(b),
+                               wl.rope_base, heads=heads)
+            t_total += time.perf_counter() - t0
+            heads_done += len(heads)
+            # the share of this sequence's latent-cache work these heads stand for
+            done_bytes += L * bytes_per_tok * len(heads) / wl.H
+            if t_total >= budget_s or heads_done >= max_heads:
+                break
+        if t_total >= budget_s or heads_done >= max_heads:
+            break
+    threads = _blas_threads()
+    sample = (f"fp64 oracle (explicit k^C/v^C decompression per head) on {heads_done} of "
+              f"{wl.H} heads across {seqs} sequence(s) of L={wl.seq_lens[0]}; bytes credited = "
+              f"L * {bytes_per_tok} B * heads/{wl.H} per sequence")
+    return done_bytes / t_total / 1e9, sample, threads, t_total
+
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    import workloads as W
+
+    if rank != 0:
+        return 0
+    wl = W.config(WORKLOAD_ID)
+    rates = []
+    sample = ""
+    threads = 1
+    for i in range(args.warmup + args.steps):
+        v, sample, threads, t = _cpu_oracle_sample(wl, budget_s=args.ref_seconds_per_step)
+        if i >= args.warmup:
+            rates.append(v)
+    value = statistics.median(rates)
+    cache_bytes, _, flops = _workload_sizes(wl)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": cache_bytes / (value * 1e9) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "seq_len": wl.seq_lens[0], "n_heads": wl.H,
+                   "d_latent": wl.C, "d_rope": wl.R, "n_q": wl.n_q, "cache": wl.cache},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local_rank):
+    import torch
+
+    import mla_latent_kv_78_b300 as M
+    import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.config(WORKLOAD_ID)
+    cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act,
+                        kernel=args.kernel)
+    act = torch.bfloat16 if wl.act == "bf16" else torch.float32
+    lat = torch.bfloat16 if wl.latent_storage == "bf16" else torch.float32
+    w_uk, w_uv = wl.weights()
+    step = M.DecodeStep(cfg, torch.from_numpy(wl.block_table()), wl.seq_lens, wl.n_q, wl.num_pages,
+                        torch.from_numpy(w_uk).to(dev).to(act), torch.from_numpy(w_uv).to(dev).to(act),
+                        num_splits=args.splits, device=str(dev))
+    # cache fill: every token before this step's, via the library's append
+    new_c, new_r = [], []
+    for b in range(wl.B):
+        c, r = wl.latents(b)
+        keep = wl.seq_lens[b] - wl.n_q
+        step.prefill(torch.from_numpy(c[:keep]).to(dev).to(lat), torch.from_numpy(r[:keep]).to(dev).to(lat),
+                     torch.full((keep,), b, dtype=torch.int32, device=dev),
+                     torch.arange(keep, dtype=torch.int32, device=dev))
+        new_c.append(c[keep:])
+        new_r.append(r[keep:])
+    q_c, q_r = wl.queries()
+    T = wl.B * wl.n_q
+    inputs_host = {
+        "c": torch.from_numpy(np.concatenate(new_c)).to(lat).pin_memory(),
+        "r": torch.from_numpy(np.concatenate(new_r)).to(lat).pin_memory(),
+        "qc": torch.from_numpy(q_c.reshape(T, wl.H, wl.D)).to(act).pin_memory(),
+        "qr": torch.from_numpy(q_r.reshape(T, wl.H, wl.R)).to(act).pin_memory(),
+    }
+    inputs_dev = {k: v.to(dev) for k, v in inputs_host.items()}
+    out_host = torch.empty(step.o.shape, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    assert step.status() == 0, "device status flagged during cache fill"
+
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    splits_used = M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, wl.max_seq_len, args.splits) > 0
+    launches_per_step = 4 + (1 if splits_used else 0)
+
+    def one_step():
+        step.step(inputs_dev["c"], inputs_dev["r"], inputs_dev["qc"], inputs_dev["qr"])
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        s0, d0, d1, s1 = ev[k]
+        s0.record(stream)
+        step.append(inputs_dev["c"], inputs_dev["r"])
+        step.absorb(inputs_dev["qc"], inputs_dev["qr"])
+        d0.record(stream)
+        step.decode()
+        d1.record(stream)
+        step.unabsorb()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
+    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    assert step.status() == 0, f"device status {step.status()} after timed steps"
+
+    # end to end through the public API, host buffers in and out
+    e2e_ms = []
+    h2d = sum(t.numel() * t.element_size() for t in inputs_host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    for k in range(args.steps + args.warmup):
+        flush.fill_(float(k))
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for key, t in inputs_host.items():
+            inputs_dev[key].copy_(t, non_blocking=True)
+        one_step()
+        out_host.copy_(step.o, non_blocking=True)
+        b_.record(stream)
+        b_.synchronize()
+        if k >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b_))
+
+    cache_bytes, qo_bytes, flops = _workload_sizes(wl)
+    total_ms = sum(step_ms)
+    total_e2e = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, total_e2e = float(t[0]), float(t[1])
+    ms_per_step = total_ms / args.steps
+    value = world * cache_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    e2e_value = world * cache_bytes * args.steps / (total_e2e * 1e-3) / 1e9
+    peaks = _peaks()
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    dec_bytes = cache_bytes + qo_bytes
+    achieved = dec_bytes / (dec_avg_ms * 1e-3) / 1e9
+    kernel_used = M.mla_decode_kernel(cfg, wl.B, wl.n_q)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "seq_len": wl.seq_lens[0], "n_heads": wl.H,
+                   "d_head": wl.D, "d_latent": wl.C, "d_rope": wl.R, "n_q": wl.n_q,
+                   "page_size": wl.P, "cache": wl.cache, "l2": "flushed before every timed step",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "decode_kernel": {1: "simt", 2: "tcgen05"}.get(kernel_used, str(kernel_used)),
+                   "num_splits": args.splits},
+        "us_per_step": ms_per_step * 1e3,
+        "step_tflops": flops / (ms_per_step * 1e-3) / 1e12,
+        "decode": {"us": dec_avg_ms * 1e3, "gbs": achieved,
+                   "tflops": flops / (dec_avg_ms * 1e-3) / 1e12,
+                   "algorithmic_bytes": dec_bytes, "flops": flops},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "mla_decode", "peak_source": peaks["source"],
+                     "tensor_frac": flops / (dec_avg_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": total_e2e / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, sample, threads, t = _cpu_oracle_sample(wl, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": sample, "seconds": t}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor-core decode")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds-per-step", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        return run_ours(args, world, rank, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

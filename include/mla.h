@@ -1,0 +1,186 @@
+/*
+ * mla.h — C ABI of the B300 (sm_103a) DeepSeek-V2 Multi-head Latent Attention
+ * decode library (libmla_b300.so).
+ *
+ * The method. Each token caches only a compressed latent c^{KV} (d_c values)
+ * and one decoupled RoPE key k^R (d_h^R values) shared by all heads
+ * (「一文通透DeepSeek-V2」 §2.2.1 low-rank joint KV compression, §2.2.2 decoupled
+ * RoPE and the (d_c + d_h^R)·l cache). At decode time W^{UK} is absorbed into
+ * the query and W^{UV} into the output, so every head scores against the
+ * shared [c^{KV}; k^R] vector (§2.2.1 last paragraph; 「Deepseek系列从v3到R易
+ * 背面经版」 MLA: MHA becomes MQA) with the scale 1/sqrt(d_h + d_h^R)
+ * (「deepseek(2)——deepseek 關鍵技術」 §1).
+ *
+ * One decode step is four calls, all asynchronous on the caller's stream:
+ *   mla_append_cache  write this step's c^{KV}, RoPE(k^R) into the paged pool
+ *   mla_absorb_q      q_lat = [q^C W^{UK}_i ; RoPE(q^R)] per head
+ *   mla_decode        paged latent attention (+ split-KV log-sum-exp combine)
+ *   mla_unabsorb      o = W^{UV}_i o_lat per head
+ *
+ * Conventions for every call
+ *   - All array pointers are DEVICE pointers, allocated and owned by the
+ *     caller; the library keeps no device allocation and no state between
+ *     calls. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - Arrays are dense, row-major, with the shapes given below; element
+ *     types follow cfg->act_dtype / cfg->cache_dtype.
+ *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code. Arguments are
+ *     checked on the host before anything is launched; on an error nothing
+ *     is launched. Faults only the device can see (a page id outside the
+ *     pool, a sequence shorter than its query count, a bounded wait that
+ *     ran out) are OR-ed as MLA_DEV_* bits into *dev_status (device int32,
+ *     may be NULL), which the caller reads after synchronising. A flagged
+ *     item is skipped, never accessed out of bounds.
+ *   - Sequence b's cached length seq_lens[b] includes this step's n_q new
+ *     tokens; query j of sequence b is at position seq_lens[b] - n_q + j and
+ *     attends to positions 0 .. seq_lens[b] - n_q + j (causal mask,
+ *     「一文通透DeepSeek-V2」 §2.1.1; two-token MTP decode masks the two new
+ *     tokens against each other).
+ *   - Token t of page-table row b at position p lives in page
+ *     block_table[b * max_pages_per_seq + p / page_size], slot p % page_size.
+ */
+#ifndef MLA_B300_H
+#define MLA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG -1   /* null pointer, negative size, inconsistent shape */
+#define MLA_ERR_UNSUPPORTED -2   /* valid but not implemented (e.g. FP8 with fp32 act) */
+#define MLA_ERR_WORKSPACE -3     /* workspace_bytes < mla_decode_workspace_size() */
+#define MLA_ERR_ALIGNMENT -4     /* a pointer misses the 16-byte alignment a kernel needs */
+#define MLA_ERR_CUDA -5          /* a CUDA runtime/driver call failed */
+
+/* ---- device status bits (OR-ed into *dev_status) ----------------------- */
+#define MLA_DEV_INDEX_OUT_OF_RANGE 1  /* page id / sequence id / position outside its table */
+#define MLA_DEV_BAD_SEQLEN 2          /* seq_lens[b] < n_q or > max_seq_len */
+#define MLA_DEV_TIMEOUT 4             /* a bounded barrier wait gave up; outputs invalid */
+
+/* ---- element types ----------------------------------------------------- */
+#define MLA_F32 0
+#define MLA_BF16 1
+#define MLA_FP8_E4M3 2   /* cache only */
+
+/* ---- decode kernel choice ---------------------------------------------- */
+#define MLA_KERNEL_AUTO 0   /* tensor-core kernel when the shape allows, else SIMT */
+#define MLA_KERNEL_SIMT 1   /* generic CUDA-core kernel, any shape */
+#define MLA_KERNEL_TC 2     /* tcgen05/TMEM kernel: n_heads=128, d_latent=512, d_rope=64,
+                               page_size=64, bf16 act, bf16 or FP8 cache, n_q in {1,2} */
+
+typedef struct mla_config {
+  int32_t n_heads;      /* H  = n_h                                               */
+  int32_t d_head;       /* D  = d_h  (per-head q^C / k^C / v^C width)              */
+  int32_t d_latent;     /* C  = d_c  (latent c^{KV} width)                         */
+  int32_t d_rope;       /* R  = d_h^R (decoupled RoPE width, even)                 */
+  int32_t page_size;    /* P  tokens per page of the latent pool                   */
+  int32_t cache_dtype;  /* MLA_F32 | MLA_BF16 | MLA_FP8_E4M3                       */
+  int32_t act_dtype;    /* MLA_F32 | MLA_BF16: q, weights, q_lat, o_lat storage    */
+  int32_t kernel;       /* MLA_KERNEL_*                                           */
+  float softmax_scale;  /* 0 -> 1/sqrt(d_head + d_rope)                            */
+  float rope_base;      /* 0 -> 10000                                             */
+} mla_config;
+
+/*
+ * Bytes of one token's pool entry.
+ *   MLA_F32 / MLA_BF16 cache: [c^{KV} (C) ; RoPE(k^R) (R)] elements of that type.
+ *   MLA_FP8_E4M3 cache: C bytes of E4M3 codes, then 2R bytes of bf16 RoPE(k^R),
+ *   then C/128 fp32 scales, one per 1x128 group (「Deepseek系列从v3到R易背面经版」
+ *   F8量化策略: per-token 1x128 activation groups). 656 bytes at V2 sizes.
+ * Returns 0 for an invalid config.
+ */
+size_t mla_cache_entry_bytes(const mla_config* cfg);
+
+/*
+ * mla_append_cache — cache write (「一文通透DeepSeek-V2」 §2.2.1 c^{KV}_t = W^{DKV} h_t is
+ * cached; §2.2.2 k^R_t = RoPE(W^{KR} h_t) is cached). The projections themselves are
+ * upstream: this call receives c^{KV} and the un-rotated k^R.
+ *
+ *   c_kv        [T][C]   latents (fp32 for an fp32 cache, else bf16)
+ *   k_r         [T][R]   RoPE keys before rotation (same type as c_kv)
+ *   seq_idx     [T]      int32 page-table row of each token, 0 <= seq_idx < batch
+ *   pos         [T]      int32 position of each token in its sequence
+ *   block_table [batch][max_pages_per_seq] int32 page ids
+ *   kv_pool     [num_pages][page_size] entries of mla_cache_entry_bytes()
+ * For each token: k^R is rotated by its position (interleaved pairs, angle
+ * pos * base^(-2k/R), computed in fp64), then [c ; RoPE(k^R)] is written to its
+ * slot; an FP8 cache stores c as E4M3 codes with scale = amax/448 per 128-group
+ * (IEEE fp32 division, round-to-nearest-even, saturating). A token whose row,
+ * position or page id is out of range is skipped and flagged.
+ */
+int mla_append_cache(const mla_config* cfg, const void* c_kv, const void* k_r,
+                     const int32_t* seq_idx, const int32_t* pos, int32_t num_tokens,
+                     const int32_t* block_table, int32_t batch, int32_t max_pages_per_seq,
+                     int32_t num_pages, void* kv_pool, int32_t* dev_status, void* stream);
+
+/*
+ * mla_absorb_q — query-side absorption (「一文通透DeepSeek-V2」 §2.2.1: W^{UK} is absorbed
+ * into the query; 「Deepseek系列从v3到R易背面经版」 MLA: (W^{UQ})^T W^{UK} fused).
+ *
+ *   q_c   [T][H][D]  q^C;   q_r [T][H][R] q^R before rotation;   pos [T] int32
+ *   w_uk  [H][D][C]  head i's rows of W^{UK} in R^{(H D) x C}
+ *   q_lat [T][H][C+R] out:  q_lat[t][i][0:C] = sum_d q_c[t][i][d] w_uk[i][d][:]  (fp32 accum.)
+ *                           q_lat[t][i][C: ] = RoPE_pos[t](q_r[t][i])
+ * All in cfg->act_dtype. Decode orders tokens as t = b * n_q + j.
+ */
+int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const int32_t* pos,
+                 int32_t num_tokens, const void* w_uk, void* q_lat, void* stream);
+
+/*
+ * Workspace bytes mla_decode needs for these sizes (0 when no split is needed).
+ * num_splits as for mla_decode; max_seq_len bounds every seq_lens[b].
+ */
+size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n_q,
+                                 int32_t max_seq_len, int32_t num_splits);
+
+/*
+ * Which decode kernel mla_decode would launch for these sizes:
+ * MLA_KERNEL_SIMT or MLA_KERNEL_TC, or a negative MLA_ERR_* code.
+ */
+int mla_decode_kernel(const mla_config* cfg, int32_t batch, int32_t n_q);
+
+/*
+ * mla_decode — paged latent attention, absorbed form (「deepseek(2)——deepseek 關鍵技術」
+ * §1 o_{t,i} = sum_j softmax_j(q_{t,i}^T k_{j,i} / sqrt(d_h + d_h^R)) v^C_{j,i}, with W^{UK},
+ * W^{UV} moved to the query / output side):
+ *   s_n  = (q_lat[b][j][i] . [c_n ; k^R_n]) * scale   for n <= seq_lens[b] - n_q + j
+ *   o_lat[b][j][i] = sum_n softmax(s)_n c_n,   lse[b][j][i] = ln sum_n e^{s_n}
+ *
+ *   q_lat       [batch][n_q][H][C+R]   act dtype
+ *   kv_pool     as written by mla_append_cache
+ *   block_table [batch][max_pages_per_seq] int32;  seq_lens [batch] int32 (device)
+ *   max_seq_len host-side bound on seq_lens (sizes the split-KV schedule)
+ *   num_splits  0 = automatic; otherwise the SIMT kernel splits each sequence's
+ *               tokens into num_splits ranges and the tensor-core kernel
+ *               spreads the batch's pages over num_splits CTA pairs per query
+ *               row; partial results are merged with log-sum-exp weights.
+ *   workspace   device scratch of >= mla_decode_workspace_size() bytes (may be
+ *               NULL when that size is 0); contents need no initialisation.
+ *   o_lat       [batch][n_q][H][C] act dtype;   lse [batch][n_q][H] fp32 or NULL
+ * The result for a fixed num_splits is deterministic (no floating-point atomics).
+ */
+int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
+               const int32_t* block_table, int32_t max_pages_per_seq, int32_t num_pages,
+               const int32_t* seq_lens, int32_t batch, int32_t n_q, int32_t max_seq_len,
+               int32_t num_splits, void* workspace, size_t workspace_bytes, void* o_lat,
+               float* lse, int32_t* dev_status, void* stream);
+
+/*
+ * mla_unabsorb — output-side absorption (「一文通透DeepSeek-V2」 §2.2.1: W^{UV} is absorbed
+ * into W^O):  o[t][i][r] = sum_k w_uv[i][r][k] * o_lat[t][i][k]   (fp32 accumulation)
+ *   o_lat [T][H][C] act dtype;  w_uv [H][D][C] act dtype;  o [T][H][D] fp32.
+ */
+int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, const void* w_uv,
+                 float* o, void* stream);
+
+/* Human-readable text of a return code (static storage). */
+const char* mla_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_B300_H */

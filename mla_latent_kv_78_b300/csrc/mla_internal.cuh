@@ -1,0 +1,36 @@
+// Launchers shared between the C-ABI front end and the kernel files.
+#pragma once
+
+#include "mla_common.cuh"
+
+namespace mla {
+
+cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, const int32_t* seq_idx,
+                          const int32_t* pos, int T, const int32_t* bt, int batch, int maxp,
+                          int num_pages, void* pool, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_absorb(const Dims& d, const void* q_c, const void* q_r, const int32_t* pos,
+                          int T, const void* w_uk, void* q_lat, cudaStream_t stream);
+
+cudaError_t launch_unabsorb(const Dims& d, const void* o_lat, int T, const void* w_uv, float* o,
+                            cudaStream_t stream);
+
+// Generic CUDA-core decode: grid (H, n_q, B * S). With S > 1 it writes
+// normalised partials to the workspace and a combine kernel merges them.
+size_t simt_workspace_bytes(const Dims& d, int B, int n_q, int S);
+int simt_pick_splits(const Dims& d, int B, int n_q, int max_seq_len, int num_splits, int num_sms);
+cudaError_t launch_decode_simt(const Dims& d, const void* q_lat, const void* pool,
+                               const int32_t* bt, int maxp, int num_pages, const int32_t* seq_lens,
+                               int B, int n_q, int max_seq_len, int S, void* ws, void* o_lat,
+                               float* lse, int32_t* status, cudaStream_t stream);
+
+// Tensor-core decode (tcgen05 + TMEM + TMA), V2 head shapes only.
+bool tc_supported(const Dims& d, int n_q);
+size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,
+                          int num_sms);
+cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool, const int32_t* bt,
+                             int maxp, int num_pages, const int32_t* seq_lens, int B, int n_q,
+                             int max_seq_len, int num_splits, void* ws, size_t ws_bytes,
+                             void* o_lat, float* lse, int32_t* status, cudaStream_t stream);
+
+}  // namespace mla

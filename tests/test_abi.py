@@ -1,0 +1,79 @@
+"""The C-ABI library builds, loads and exports what include/mla.h declares;
+host-side argument checks answer without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_78_b300 as M
+from mla_latent_kv_78_b300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = M.lib()
+    names = _declared()
+    assert "mla_decode" in names and "mla_append_cache" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/mla.h but not exported"
+    # the binding wraps exactly the declared calls
+    assert set(L.EXPORTED) <= set(names)
+
+
+def test_entry_bytes():
+    v2 = dict(H=128, D=128, C=512, R=64, P=64)
+    assert M.mla_cache_entry_bytes(M.make_config(**v2, cache="bf16")) == 1152
+    assert M.mla_cache_entry_bytes(M.make_config(**v2, cache="fp8")) == 656
+    assert M.mla_cache_entry_bytes(M.make_config(4, 32, 64, 16, 16, cache="f32", act="f32")) == 320
+    # invalid: odd RoPE width
+    assert M.mla_cache_entry_bytes(M.make_config(4, 32, 64, 15, 16, cache="f32", act="f32")) == 0
+
+
+def test_host_argument_checks_return_codes():
+    lib = M.lib()
+    cfg = M.make_config(128, 128, 512, 64, 64)
+    bad = M.make_config(128, 128, 512, 63, 64)
+    by = ctypes.byref
+    # invalid config
+    assert lib.mla_decode(by(bad), 1, 1, 1, 1, 1, 1, 1, 1, 1, 0, None, 0, 1, None, None, None) == L.MLA_ERR_INVALID_ARG
+    # null pointers
+    assert lib.mla_decode(by(cfg), None, 1, 1, 1, 1, 1, 1, 1, 1, 0, None, 0, 1, None, None, None) == L.MLA_ERR_INVALID_ARG
+    assert lib.mla_append_cache(by(cfg), None, None, None, None, 4, None, 1, 1, 1, None, None, None) == L.MLA_ERR_INVALID_ARG
+    assert lib.mla_absorb_q(by(cfg), None, None, None, 4, None, None, None) == L.MLA_ERR_INVALID_ARG
+    assert lib.mla_unabsorb(by(cfg), None, 4, None, None, None) == L.MLA_ERR_INVALID_ARG
+    # empty work is a no-op that launches nothing
+    assert lib.mla_append_cache(by(cfg), None, None, None, None, 0, None, 1, 1, 1, None, None, None) == L.MLA_OK
+    assert lib.mla_decode(by(cfg), None, None, None, 1, 1, None, 0, 1, 1, 0, None, 0, None, None, None, None) == L.MLA_OK
+    # max_seq_len beyond the page table's reach
+    assert lib.mla_decode(by(cfg), 16, 16, 16, 2, 4, 16, 1, 1, 129, 0, None, 0, 16, None, None, None) == L.MLA_ERR_INVALID_ARG
+    # n_q larger than max_seq_len
+    assert lib.mla_decode(by(cfg), 16, 16, 16, 2, 4, 16, 1, 3, 2, 0, None, 0, 16, None, None, None) == L.MLA_ERR_INVALID_ARG
+    # FP8 cache needs bf16 activations
+    assert lib.mla_decode_kernel(by(M.make_config(128, 128, 512, 64, 64, cache="fp8", act="f32")), 1, 1) == L.MLA_ERR_UNSUPPORTED
+    assert M.mla_status_string(L.MLA_ERR_WORKSPACE) == "workspace too small"
+
+
+def test_kernel_selection():
+    v2 = M.make_config(128, 128, 512, 64, 64)
+    tiny = M.make_config(4, 32, 64, 16, 16, cache="f32", act="f32")
+    assert M.mla_decode_kernel(tiny, 2, 1) == M.MLA_KERNEL_SIMT
+    forced = M.make_config(128, 128, 512, 64, 64, kernel=M.MLA_KERNEL_SIMT)
+    assert M.mla_decode_kernel(forced, 64, 1) == M.MLA_KERNEL_SIMT
+    k = M.mla_decode_kernel(v2, 64, 1)
+    assert k in (M.MLA_KERNEL_SIMT, M.MLA_KERNEL_TC)
+
+
+def test_workspace_size_grows_with_splits():
+    cfg = M.make_config(128, 128, 512, 64, 64, kernel=M.MLA_KERNEL_SIMT)
+    assert M.mla_decode_workspace_size(cfg, 2, 1, 4096, 1) == 0
+    w2 = M.mla_decode_workspace_size(cfg, 2, 1, 4096, 2)
+    w4 = M.mla_decode_workspace_size(cfg, 2, 1, 4096, 4)
+    assert w2 == 2 * 1 * 128 * 2 * (512 + 1) * 4 and w4 == 2 * w2

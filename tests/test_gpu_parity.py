@@ -1,0 +1,210 @@
+"""GPU parity at sizes the oracle finishes in seconds: every call of the C ABI
+against the fp64 oracle on the same seeded inputs.
+
+Tolerance (both o_lat and o): |gpu - oracle| <= 1e-2 max|oracle| + 1e-3 for bf16 and
+FP8 caches, <= 1e-5 max|oracle| for the fp32 workload. Page placement and FP8
+codes are compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_78_b300 as M
+import workloads as W
+from oracle import mla_oracle as O
+
+from _support import ACT, Case, assert_close, config_of, dev, gpu_rows
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")
+
+# V2 head shapes, sequences that span several 64-token pages with ragged tails
+SMALL_BF16 = W.small_v2(4, [65, 200, 7, 130], n_q=1, cache="bf16", seed=11)
+SMALL_FP8 = W.small_v2(3, [129, 64, 70], n_q=2, cache="fp8", seed=12)
+SMALL_BF16_MTP = W.small_v2(3, [2, 100, 191], n_q=2, cache="bf16", seed=13)
+TINY = W.config(1)
+TINY_PERM = W.config(1).with_(permute_pages=True)
+
+
+def _bits_equal(a: np.ndarray, b: np.ndarray) -> bool:
+    return a.shape == b.shape and np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8], ids=lambda w: w.name + ("-perm" if w.permute_pages else ""))
+def test_append_writes_each_token_to_its_slot(wl):
+    """Every cached token lands in pool[block_table[b][pos // P]][pos % P] and nowhere else
+    (bit-exact); c_KV is copied (or E4M3-coded, bit-exact), k^R is RoPE'd (<= 1 ulp)."""
+    case = Case(wl, prefill=True)
+    case.step.append(case.new_c, case.new_r)
+    torch.cuda.synchronize()
+    assert case.step.status() == 0
+    pool = case.step.pool.cpu().numpy()  # [num_pages, P, entry]
+    touched = np.zeros(pool.shape[:2], dtype=bool)
+    for b in range(wl.B):
+        L = wl.seq_lens[b]
+        c, r = wl.latents(b)
+        ce = O.cache_entries(c, r, np.arange(L), wl.cache, wl.rope_base)
+        pg, sl = O.page_slots(np.full(L, b), np.arange(L), case.bt_np, wl.P)
+        ent = pool[pg, sl]                       # [L, entry]
+        touched[pg, sl] = True
+        if wl.cache == "f32":
+            got_c = ent[:, :4 * wl.C].copy().view(np.float32)
+            got_r = ent[:, 4 * wl.C:].copy().view(np.float32).astype(np.float64)
+            assert _bits_equal(got_c, c.astype(np.float32))
+            np.testing.assert_allclose(got_r, ce["k_r"], rtol=2 ** -23, atol=1e-30)
+        elif wl.cache == "bf16":
+            got_c = ent[:, :2 * wl.C].copy().view(np.uint16)
+            assert np.array_equal(got_c, W.to_bf16_bits(c))
+            got_r = W.bf16_bits_to_f32(ent[:, 2 * wl.C:].copy().view(np.uint16)).astype(np.float64)
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ce["k_r"]), 1e-30))) - 7)
+            assert np.all(np.abs(got_r - ce["k_r"]) <= ulp)
+        else:
+            codes = ent[:, :wl.C]
+            got_r = W.bf16_bits_to_f32(ent[:, wl.C:wl.C + 2 * wl.R].copy().view(np.uint16)).astype(np.float64)
+            scales = ent[:, wl.C + 2 * wl.R:].copy().view(np.float32)
+            assert np.array_equal(codes, ce["codes"]), "E4M3 codes differ"
+            assert _bits_equal(scales, ce["scales"].astype(np.float32)), "group scales differ"
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ce["k_r"]), 1e-30))) - 7)
+            assert np.all(np.abs(got_r - ce["k_r"]) <= ulp)
+    # slots no token maps to stay untouched (the pool starts zeroed)
+    assert not pool[~touched].any()
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_FP8], ids=lambda w: w.name)
+def test_absorb_q(wl):
+    case = Case(wl, prefill=False)
+    case.step.absorb(case.q_c, case.q_r)
+    torch.cuda.synchronize()
+    pos = np.concatenate([wl.positions(b) for b in range(wl.B)])
+    ref = O.absorb_q(case.q_c_np.reshape(-1, wl.H, wl.D), case.q_r_np.reshape(-1, wl.H, wl.R), pos,
+                     case.w_uk_np, wl.rope_base)
+    got = case.step.q_lat.float().cpu().numpy()
+    assert_close(wl, got[..., :wl.C], ref[..., :wl.C], "q_lat latent part")
+    assert_close(wl, got[..., wl.C:], ref[..., wl.C:], "q_lat RoPE part")
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [TINY, SMALL_BF16], ids=lambda w: w.name)
+def test_unabsorb(wl):
+    case = Case(wl, prefill=False)
+    g = np.random.default_rng(5)
+    o_lat = W.round_to_storage(g.standard_normal((wl.B * wl.n_q, wl.H, wl.C)).astype(np.float32) * 0.1, wl.act)
+    case.step.o_lat.copy_(dev(o_lat, ACT[wl.act]))
+    case.step.unabsorb()
+    torch.cuda.synchronize()
+    ref = O.unabsorb(o_lat, case.w_uv_np)
+    assert_close(wl, case.step.o.cpu().numpy(), ref, "o")
+
+
+def _decode_only(wl, kernel, num_splits=0):
+    case = Case(wl, kernel=kernel, num_splits=num_splits)
+    case.step.append(case.new_c, case.new_r)
+    q_lat = wl.latent_queries()
+    case.step.decode(dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act]))
+    torch.cuda.synchronize()
+    assert case.step.status() == 0
+    tau = O.softmax_scale(wl.D, wl.R)
+    for b in range(wl.B):
+        ce = case.cache_of(b)
+        ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_o, f"o_lat[b={b}]")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"lse[b={b}]")
+    return case
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP],
+                         ids=lambda w: w.name + ("-perm" if w.permute_pages else ""))
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_decode_latent_attention(wl, kernel):
+    _decode_only(wl, kernel)
+
+
+@needs_cuda
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_decode_splits_agree(splits):
+    wl = SMALL_BF16
+    base = _decode_only(wl, M.MLA_KERNEL_SIMT, 1)
+    other = _decode_only(wl, M.MLA_KERNEL_SIMT, splits)
+    a = base.step.o_lat.float().cpu().numpy()
+    b = other.step.o_lat.float().cpu().numpy()
+    # split partials are fp32; only the final bf16 rounding may differ (one ulp)
+    assert np.max(np.abs(a - b)) <= 2.0 ** -8 * np.max(np.abs(a))
+    np.testing.assert_allclose(other.step.lse.cpu().numpy(), base.step.lse.cpu().numpy(),
+                               rtol=1e-5, atol=1e-5)
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP],
+                         ids=lambda w: w.name + ("-perm" if w.permute_pages else ""))
+def test_decode_step_end_to_end(wl):
+    """append -> absorb -> decode -> unabsorb against the non-absorbed oracle."""
+    case = Case(wl)
+    case.run_step()
+    assert case.step.status() == 0
+    for b in range(wl.B):
+        o, o_lat, lse = case.oracle(b)
+        assert_close(wl, gpu_rows(case.step.o, wl, b), o, f"o[b={b}]")
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), o_lat, f"o_lat[b={b}]")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), lse, f"lse[b={b}]")
+
+
+@needs_cuda
+def test_decode_is_deterministic():
+    wl = SMALL_BF16
+    case = Case(wl)
+    case.run_step()
+    first = case.step.o_lat.clone()
+    for _ in range(3):
+        case.step.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(first, case.step.o_lat)
+
+
+@needs_cuda
+def test_bad_page_id_is_flagged_and_skipped():
+    """A page id outside the pool sets MLA_DEV_INDEX_OUT_OF_RANGE; the other sequences'
+    results are unaffected and nothing outside the pool is touched."""
+    wl = SMALL_BF16
+    case = Case(wl)
+    case.run_step()
+    good = case.step.o_lat.clone()
+    bt = case.step.block_table.clone()
+    bt[2, 0] = wl.num_pages + 5
+    case.step.block_table.copy_(bt)
+    case.step.dev_status.zero_()
+    case.step.decode()
+    torch.cuda.synchronize()
+    assert case.step.status() & M.MLA_DEV_INDEX_OUT_OF_RANGE
+    for b in (0, 1, 3):
+        assert torch.equal(case.step.o_lat[b], good[b])
+
+
+@needs_cuda
+def test_short_sequence_is_flagged():
+    """seq_lens[b] < n_q cannot hold this step's tokens: MLA_DEV_BAD_SEQLEN."""
+    wl = SMALL_BF16_MTP
+    case = Case(wl)
+    case.run_step()
+    sl = case.step.seq_lens.clone()
+    sl[0] = 1
+    case.step.seq_lens.copy_(sl)
+    case.step.dev_status.zero_()
+    case.step.decode()
+    torch.cuda.synchronize()
+    assert case.step.status() & M.MLA_DEV_BAD_SEQLEN
+
+
+@needs_cuda
+def test_empty_batch_and_empty_token_lists_are_noops():
+    wl = SMALL_BF16
+    cfg = config_of(wl)
+    z = torch.zeros(0, device="cuda")
+    lib = M.lib()
+    assert lib.mla_decode(cfg, None, None, None, 1, 1, None, 0, 1, 1, 0, None, 0, None, None, None, None) == 0
+    assert lib.mla_append_cache(cfg, None, None, None, None, 0, None, 1, 1, 1, None, None, None) == 0
+    assert lib.mla_unabsorb(cfg, None, 0, None, None, None) == 0
+    assert z.numel() == 0
