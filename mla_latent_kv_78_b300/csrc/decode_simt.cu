@@ -200,6 +200,16 @@ static cudaError_t launch_t(const Dims& d, const void* q_lat, const void* pool, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_combine(int C, int S, const float* ws_o, const float* ws_lse, void* o_lat,
+                           int act_dtype, float* lse, size_t rows, cudaStream_t stream) {
+  if (act_dtype == MLA_F32)
+    combine_kernel<float><<<(unsigned)rows, 128, 0, stream>>>(C, S, ws_o, ws_lse, (float*)o_lat, lse);
+  else
+    combine_kernel<__nv_bfloat16><<<(unsigned)rows, 128, 0, stream>>>(C, S, ws_o, ws_lse,
+                                                                      (__nv_bfloat16*)o_lat, lse);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_simt(const Dims& d, const void* q_lat, const void* pool,
                                const int32_t* bt, int maxp, int num_pages, const int32_t* seq_lens,
                                int B, int n_q, int max_seq_len, int S, void* ws, void* o_lat,

@@ -1,16 +1,743 @@
-// Tensor-core MLA decode (tcgen05 / TMEM / TMA) — not yet enabled.
+// Tensor-core MLA decode (tcgen05 / TMEM / TMA) for DeepSeek-V2 head shapes:
+// n_h = 128 heads, d_c = 512, d_h^R = 64, page size 64, bf16 latent cache.
+//
+// What it computes (「deepseek(2)——deepseek 關鍵技術」 §1, absorbed form of
+// 「一文通透DeepSeek-V2」 §2.2.1-2.2.2): for one query row of one sequence,
+//   s[n][h] = q_lat[h] . [c_n ; k^R_n] * scale,   o_lat[h] = sum_n softmax_n(s[:, h]) c_n,
+// with all 128 heads sharing the 576-d latent key of each cached token.
+//
+// Design (B300-first; no design on the pages is followed):
+//  * A CTA pair (cluster of 2) owns one (sequence, query row, split). Tiles are 256
+//    tokens = 4 pages. Scores are computed transposed, S^T[token][head] = K . Q^T, with a
+//    2-SM MMA (cta_group::2, M = 256 tokens, N = 128 heads): each CTA supplies its 128
+//    tokens' 576-d keys and HALF of Q (its 64 heads), so Q costs 72 KB of shared memory
+//    per SM instead of 144 KB, and every MMA runs at full rate (N = 128).
+//  * The output is accumulated transposed, O^T[d_c][head] = V^T . P^T, again 2-SM
+//    (M = 256 latent rows per MMA, two MMAs per K step): each CTA holds half of O^T,
+//    256 TMEM columns, which leaves room for a double-buffered S^T (2 x 128 columns).
+//  * P^T is split by head: the CTA that computed a token's scores keeps its own head
+//    half and sends the other half (16 KB per tile) to the peer with st.async. The only
+//    other exchange is each tile's per-head maximum (512 B), so both CTAs take identical
+//    online-softmax decisions. Rescaling is lazy: a head's reference maximum moves only
+//    when a score exceeds it by more than 2^8, which keeps P in bf16 range and leaves
+//    O untouched on almost every tile.
+//  * The key tile is read from HBM once, as [128 tokens x 64 dims] chunks for S^T; the
+//    latent part is read a second time, 3/4 of a tile later, as [64 tokens x 256 d_c]
+//    chunks for O^T, normally from L2.
+//  * Warp roles: w0 TMA producer, w1 MMA issuer (even CTA) + TMEM owner, w2 relay (waits
+//    its CTA's loads, zeroes invalid rows on the last tile, signals the even CTA),
+//    w4..w11 softmax / epilogue (thread = TMEM lane; warps 4-7 heads 0-63, 8-11 heads 64-127).
+//  * Every wait is bounded; a timeout sets MLA_DEV_TIMEOUT and every role winds down.
+#include <math_constants.h>
+
 #include "mla_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace mla {
+namespace tc {
 
-bool tc_supported(const Dims&, int) { return false; }
+using namespace ptx;
 
-size_t tc_workspace_bytes(const Dims&, int, int, int, int, int) { return 0; }
+constexpr int kH = 128, kC = 512, kR = 64, kCR = 576, kP = 64;
+constexpr int kTile = 256;           // tokens per tile (4 pages)
+constexpr int kNS = 3;               // S-phase ring: [128 tok x 64 dims] bf16 = 16 KB
+constexpr int kNV = 2;               // V-phase ring: [64 tok x 256 d_c] bf16 = 32 KB
+constexpr int kKCh = kCR / 64;       // 9 dim chunks
+constexpr int kThreads = 384;
+constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
+constexpr int kPrefetchTiles = 2;    // this CTA's pages are prefetched into L2 this far ahead
+constexpr uint32_t kPageBytes = kP * kCR * 2;   // 73,728 B: one page is contiguous in the pool
 
-cudaError_t launch_decode_tc(const Dims&, const void*, const void*, const int32_t*, int, int,
-                             const int32_t*, int, int, int, int, void*, size_t, void*, float*,
-                             int32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int OFF_Q = 0;                           // 9 x [64 heads x 64 dims]  (8 KB each)
+constexpr int OFF_S = OFF_Q + kKCh * 8192;         // kNS x 16 KB
+constexpr int OFF_V = OFF_S + kNS * 16384;         // kNV x 32 KB
+constexpr int OFF_P = OFF_V + kNV * 32768;         // [256 tok x 64 heads] = 32 KB
+constexpr int OFF_F = OFF_P + 32768;               // fp32 scratch
+constexpr int F_COL = 0;       // [8 warps][64]   column max / column sum partials
+constexpr int F_CMLOC = 512;   // [128]
+constexpr int F_CMRCV = 640;   // [2][128]
+constexpr int F_M = 896;       // [128] running reference max (log2 units)
+constexpr int F_ALPHA = 1024;  // [128]
+constexpr int F_LLOC = 1152;   // [128]
+constexpr int F_LRCV = 1280;   // [128]
+constexpr int F_INV = 1408;    // [128]
+constexpr int F_FLAG = 1536;   // ints: [0] rescale, [1] abort
+constexpr int F_END = 1544;
+constexpr int OFF_BAR = OFF_F + F_END * 4;
+
+struct Bars {
+  uint64_t q_landed, q_ready;
+  uint64_t s_landed[kNS], s_ready[kNS], s_free[kNS];
+  uint64_t v_landed[kNV], v_ready[kNV], v_free[kNV];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_landed, p_ready;
+  uint64_t o_done;
+  uint64_t cm_landed[2];
+  uint64_t l_landed;
+  uint64_t teardown;
+  uint32_t tmem_base;
+};
+constexpr int kSmemBytes = OFF_BAR + (int)sizeof(Bars) + 1024;   // + alignment slack
+
+struct Params {
+  const uint8_t* pool;   // for L2 prefetch of whole pages
+  const int32_t* bt;
+  int maxp, num_pages;
+  const int32_t* seq_lens;
+  int B, n_q, max_seq_len, S;
+  float scale_log2;
+  __nv_bfloat16* o_lat;
+  float* lse;
+  float* ws_o;
+  float* ws_lse;
+  int32_t* status;
+};
+
+struct Ctx {
+  volatile int* abort_flag;
+  int32_t* status;
+};
+
+#ifdef MLA_TC_TRACE
+// Debug builds only: per-event %globaltimer stamps for the first kTraceUnits units.
+constexpr int kTraceUnits = 4, kTraceEvents = 16, kTraceTiles = 64;
+__device__ unsigned long long* g_tc_trace;
+__device__ __forceinline__ void trace(int unit, uint32_t rank, int ev, int t) {
+  if (g_tc_trace && unit < kTraceUnits && t < kTraceTiles) {
+    unsigned long long ns;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
+    g_tc_trace[(((size_t)unit * 2 + rank) * kTraceEvents + ev) * kTraceTiles + t] = ns;
+  }
+}
+#define TRACE(ev, t) trace(unit, rank, ev, t)
+#else
+#define TRACE(ev, t) ((void)0)
+#endif
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (*cx.abort_flag) return false;
+    if (mbar_try_wait(a, parity)) return true;
+    if (clock64() - t0 > kTimeout) {
+      *cx.abort_flag = 1;
+      flag_status(cx.status, MLA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait ignoring the abort flag (used while draining before exit), still bounded.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > kTimeout) return;
+  }
+}
+
+__device__ __forceinline__ void arrive_even(uint64_t* bar, uint32_t rank) {
+  if (rank == 0)
+    mbar_arrive(bar);
+  else
+    mbar_arrive_remote(mapa(smem_u32(bar), 0));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const Params prm) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  float* fs = reinterpret_cast<float*>(sm + OFF_F);
+  int* flags = reinterpret_cast<int*>(fs + F_FLAG);
+  Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+
+  // ---- which (sequence, query row, split) this pair owns
+  const int unit = blockIdx.x >> 1;
+  const int split = unit % prm.S;
+  const int row = unit / prm.S;           // b * n_q + j
+  const int b = row / prm.n_q, j = row % prm.n_q;
+  const int L = prm.seq_lens[b];
+  const bool bad_len = (L < prm.n_q || L > prm.max_seq_len);
+  const int visible = bad_len ? 0 : L - prm.n_q + j + 1;
+  int chunk = (visible + prm.S - 1) / prm.S;
+  chunk = (chunk + kTile - 1) / kTile * kTile;
+  const int lo = min(visible, split * chunk);
+  const int hi = min(visible, lo + chunk);
+  const int nt = (hi - lo + kTile - 1) / kTile;
+  const int valid_pages = (hi + kP - 1) / kP;   // pages holding tokens < hi
+
+  if (nt == 0) {
+    // nothing visible in this range: zero output, lse = -inf
+    if (bad_len && tid == 0 && rank == 0 && split == 0) flag_status(prm.status, MLA_DEV_BAD_SEQLEN);
+    for (int idx = tid; idx < kH * 256; idx += kThreads) {
+      const int h = idx >> 8, q = idx & 255;
+      const int dc = (q >> 7) * 256 + rank * 128 + (q & 127);
+      const size_t o = (size_t)row * kH + h;
+      if (prm.S == 1)
+        prm.o_lat[o * kC + dc] = __float2bfloat16_rn(0.f);
+      else
+        prm.ws_o[(o * prm.S + split) * kC + dc] = 0.f;
+    }
+    if (rank == 0 && tid < kH) {
+      const size_t o = (size_t)row * kH + tid;
+      if (prm.S == 1) {
+        if (prm.lse) prm.lse[o] = -CUDART_INF_F;
+      } else {
+        prm.ws_lse[o * prm.S + split] = -CUDART_INF_F;
+      }
+    }
+    return;
+  }
+
+  // ---- set-up
+  if (tid == 0) TRACE(11, 0);
+  if (tid == 0) {
+    mbar_init(&bars->q_landed, 1);
+    mbar_init(&bars->q_ready, 2);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&bars->s_landed[s], 1);
+      mbar_init(&bars->s_ready[s], 2);
+      mbar_init(&bars->s_free[s], 1);
+    }
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(&bars->v_landed[s], 1);
+      mbar_init(&bars->v_ready[s], 2);
+      mbar_init(&bars->v_free[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_empty[s], 16);
+      mbar_init(&bars->cm_landed[s], 1);
+    }
+    mbar_init(&bars->p_landed, 8);
+    mbar_init(&bars->p_ready, 2);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->l_landed, 1);
+    mbar_init(&bars->teardown, 1);
+    fence_mbarrier_init_cluster();
+  }
+  if (tid < kH) fs[F_M + tid] = -CUDART_INF_F;
+  if (tid < 2) flags[tid] = 0;
+  if (warp == 1) {
+    tmem_alloc_pair(&bars->tmem_base, 512);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  Ctx cx{reinterpret_cast<volatile int*>(&flags[1]), prm.status};
+
+  auto page_y = [&](int idx_in_unit) -> int {
+    const int pidx = lo / kP + idx_in_unit;
+    if (pidx >= valid_pages) return prm.num_pages * kP;   // past the range: TMA zero-fills
+    const int pg = prm.bt[(size_t)b * prm.maxp + pidx];
+    if (pg < 0 || pg >= prm.num_pages) {
+      flag_status(prm.status, MLA_DEV_INDEX_OUT_OF_RANGE);
+      return prm.num_pages * kP;
+    }
+    return pg * kP;
+  };
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      const uint64_t pol_q = policy_evict_last();
+      const uint64_t pol_s = policy_evict_normal();  // re-read soon for the V phase
+      const uint64_t pol_v = policy_evict_first();
+      mbar_arrive_expect_tx(&bars->q_landed, kKCh * 8192);
+      for (int c = 0; c < kKCh; ++c)
+        tma_load_2d(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
+                    &bars->q_landed, pol_q);
+      // pages of this CTA's token rows, prefetched into L2 ahead of the smem loads
+      auto prefetch_tile = [&](int t) {
+        if (t >= nt) return;
+        for (int q = 0; q < 2; ++q) {
+          const int y = page_y(4 * t + 2 * (int)rank + q);
+          if (y < prm.num_pages * kP) prefetch_l2(prm.pool + (size_t)y * kCR * 2, kPageBytes);
+        }
+      };
+      for (int t = 0; t < kPrefetchTiles; ++t) prefetch_tile(t);
+      int s_cnt = 0, v_cnt = 0;
+      bool ok = true;
+      auto load_v = [&](int tp, int v) -> bool {
+        const int st = v_cnt % kNV;
+        if (v_cnt >= kNV && !wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx)) return false;
+        mbar_arrive_expect_tx(&bars->v_landed[st], 32768);
+        const int y = page_y(4 * tp + v);
+        for (int q4 = 0; q4 < 4; ++q4)
+          tma_load_2d(sm + OFF_V + st * 32768 + q4 * 8192, &tmK,
+                      (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, &bars->v_landed[st],
+                      pol_v);
+        ++v_cnt;
+        return true;
+      };
+      for (int t = 0; t <= nt && ok; ++t) {
+        // V chunks of tile t-1 that fit in the ring go first, so they land while S^T(t) runs
+        int v_issued = 0;
+        if (t >= 1)
+          for (; v_issued < kNV && ok; ++v_issued) ok = load_v(t - 1, v_issued);
+        if (t < nt && ok) {
+          prefetch_tile(t + kPrefetchTiles);
+          const int y0 = page_y(4 * t + 2 * (int)rank), y1 = page_y(4 * t + 2 * (int)rank + 1);
+          for (int c = 0; c < kKCh && ok; ++c, ++s_cnt) {
+            const int st = s_cnt % kNS;
+            if (s_cnt >= kNS) ok = wait_bar(&bars->s_free[st], ((s_cnt / kNS) - 1) & 1, cx);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->s_landed[st], 16384);
+            if (c == 4) TRACE(15, t);
+            tma_load_2d(sm + OFF_S + st * 16384, &tmK, c * 64, y0, &bars->s_landed[st], pol_s);
+            tma_load_2d(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, &bars->s_landed[st], pol_s);
+          }
+          TRACE(8, t);
+        }
+        if (t >= 1)
+          for (; v_issued < 4 && ok; ++v_issued) ok = load_v(t - 1, v_issued);
+      }
+      if (!ok) {
+        // drain loads still in flight into this CTA's shared memory
+        for (int k = max(0, s_cnt - kNS); k < s_cnt; ++k) wait_drain(&bars->s_landed[k % kNS], (k / kNS) & 1);
+        for (int k = max(0, v_cnt - kNV); k < v_cnt; ++k) wait_drain(&bars->v_landed[k % kNV], (k / kNV) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(256, 128, 0, 0);
+      const uint32_t idPV = idesc_bf16_f32(256, 128, 1, 1);
+      const uint32_t sQ = smem_u32(sm + OFF_Q), sS = smem_u32(sm + OFF_S);
+      const uint32_t sV = smem_u32(sm + OFF_V), sP = smem_u32(sm + OFF_P);
+      bool ok = wait_bar(&bars->q_ready, 0, cx);
+      int s_cnt = 0, v_cnt = 0;
+      for (int t = 0; t <= nt && ok; ++t) {
+        if (t < nt) {
+          const int buf = t & 1;
+          if (t >= 2) ok = wait_bar(&bars->s_empty[buf], ((t - 2) >> 1) & 1, cx);
+          if (!ok) break;
+          tc_fence_after();
+          for (int c = 0; c < kKCh; ++c, ++s_cnt) {
+            const int st = s_cnt % kNS;
+            ok = wait_bar(&bars->s_ready[st], (s_cnt / kNS) & 1, cx);
+            if (!ok) break;
+            if (c == 0) TRACE(9, t);
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
+              const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
+              mma_bf16_pair(tmem + buf * 128, a, bd, idS, (c | k) != 0);
+            }
+            mma_commit_pair(&bars->s_free[st], 0x3);
+          }
+          if (!ok) break;
+          mma_commit_pair(&bars->s_full[buf], 0x3);
+          TRACE(0, t);
+        }
+        if (t >= 1) {
+          const int tp = t - 1;
+          ok = wait_bar(&bars->p_ready, tp & 1, cx);
+          if (!ok) break;
+          TRACE(1, tp);
+          tc_fence_after();
+          for (int v = 0; v < 4; ++v, ++v_cnt) {
+            const int st = v_cnt % kNV;
+            ok = wait_bar(&bars->v_ready[st], (v_cnt / kNV) & 1, cx);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t a = smem_desc(sV + st * 32768 + blk * 16384 + k * 2048, 8192, 1024, kSw128);
+                const uint64_t bd = smem_desc(sP + v * 8192 + k * 2048, 8192, 1024, kSw128);
+                mma_bf16_pair(tmem + 256 + blk * 128, a, bd, idPV, (tp | v | k) != 0);
+              }
+            mma_commit_pair(&bars->v_free[st], 0x3);
+          }
+          if (!ok) break;
+          mma_commit_pair(&bars->o_done, 0x3);
+          TRACE(2, tp);
+        }
+      }
+      // every MMA this thread issued (they write both CTAs' TMEM) completes before teardown
+      mma_commit_pair(&bars->teardown, 0x1);
+      wait_drain(&bars->teardown, 0);
+    }
+  } else if (warp == 2) {
+    // ================================================================ relay
+    int s_cnt = 0, v_cnt = 0;
+    bool ok = true;
+    if (lane == 0) ok = wait_bar(&bars->q_landed, 0, cx);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok && lane == 0) arrive_even(&bars->q_ready, rank);
+    for (int t = 0; t <= nt && ok; ++t) {
+      if (t < nt) {
+        for (int c = 0; c < kKCh && ok; ++c, ++s_cnt) {
+          const int st = s_cnt % kNS;
+          if (lane == 0) {
+            ok = wait_bar(&bars->s_landed[st], (s_cnt / kNS) & 1, cx);
+            if (c == 4) TRACE(14, t);
+            if (ok) arrive_even(&bars->s_ready[st], rank);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+      }
+      if (t >= 1 && ok) {
+        const int tp = t - 1;
+        if (lane == 0) {
+          ok = wait_bar(&bars->p_landed, tp & 1, cx);
+          TRACE(7, tp);
+          if (ok) arrive_even(&bars->p_ready, rank);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        for (int v = 0; v < 4 && ok; ++v, ++v_cnt) {
+          const int st = v_cnt % kNV;
+          if (lane == 0) ok = wait_bar(&bars->v_landed[st], (v_cnt / kNV) & 1, cx);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const int tok0 = lo + tp * kTile + v * kP;
+          const int nvalid = max(0, min(kP, hi - tok0));
+          if (nvalid < kP) {
+            // rows past the range may hold anything; P is 0 there, so make them 0 too
+            uint4* base = reinterpret_cast<uint4*>(sm + OFF_V + st * 32768);
+            const int nrow = kP - nvalid;
+            for (int idx = lane; idx < 4 * nrow * 8; idx += 32) {
+              const int sub = idx / (nrow * 8);
+              const int rr = nvalid + (idx / 8) % nrow;
+              base[sub * 512 + rr * 8 + (idx & 7)] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) arrive_even(&bars->v_ready[st], rank);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ================================================================ softmax / epilogue
+    const int sw = warp - 4;           // 0..7
+    const int g = sw >> 2;             // head group: heads [64g, 64g + 64)
+    const int qd = warp & 3;           // TMEM lane quadrant
+    const int i = qd * 32 + lane;      // this CTA's token row (S^T) / latent row (O^T)
+    const int stid = tid - 128;        // 0..255
+    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const uint32_t peer_cm = mapa(smem_u32(fs + F_CMRCV), peer);
+    const uint32_t peer_cm_bar0 = mapa(smem_u32(&bars->cm_landed[0]), peer);
+    const uint32_t peer_p = mapa(smem_u32(sm + OFF_P), peer);
+    const uint32_t peer_p_bar = mapa(smem_u32(&bars->p_landed), peer);
+    float l_acc[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) l_acc[c] = 0.f;
+    bool ok = true;
+    for (int t = 0; t < nt; ++t) {
+      const int buf = t & 1;
+      ok = wait_bar(&bars->s_full[buf], (t >> 1) & 1, cx);
+      ok = bar_and(1, 256, ok);
+      if (!ok) break;
+      if (stid == 0) {
+        flags[0] = 0;
+        TRACE(3, t);
+      }
+      tc_fence_after();
+      float s[64];
+      tmem_ld32(lane_addr + buf * 128 + 64 * g, s);
+      tmem_ld32(lane_addr + buf * 128 + 64 * g + 32, s + 32);
+      tmem_ld_wait();
+      if (stid == 0) TRACE(13, t);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_even(&bars->s_empty[buf], rank);
+      const int tok = lo + t * kTile + (int)rank * 128 + i;
+      const bool valid = tok < hi;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) s[c] = valid ? s[c] * prm.scale_log2 : -CUDART_INF_F;
+      // per-head maximum over this warp's 32 tokens
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float mx = warp_max_f32(s[c]);
+        if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
+      }
+      bar_and(2, 256, true);
+      if (stid < kH) {
+        const int h = stid, gg = h >> 6, cc = h & 63;
+        float mx = fs[F_COL + (gg * 4) * 64 + cc];
+#pragma unroll
+        for (int q = 1; q < 4; ++q) mx = fmaxf(mx, fs[F_COL + (gg * 4 + q) * 64 + cc]);
+        fs[F_CMLOC + h] = mx;
+        st_async_b32(peer_cm + (uint32_t)((buf * kH + h) * 4), __float_as_uint(mx),
+                     peer_cm_bar0 + buf * 8);
+      }
+      bool ok2 = true;
+      if (stid == 0) mbar_arrive_expect_tx(&bars->cm_landed[buf], kH * 4);
+      if (stid < kH) {
+        ok2 = wait_bar(&bars->cm_landed[buf], (t >> 1) & 1, cx);
+        const int h = stid;
+        const float tmax = fmaxf(fs[F_CMLOC + h], fs[F_CMRCV + buf * kH + h]);
+        const float mo = fs[F_M + h];
+        float alpha = 1.f;
+        if (tmax > mo + 8.f) {
+          alpha = ex2(mo - tmax);     // mo = -inf gives 0
+          fs[F_M + h] = tmax;
+          flags[0] = 1;
+        }
+        fs[F_ALPHA + h] = alpha;
+      }
+      ok = bar_and(3, 256, ok2);
+      if (!ok) break;
+      if (stid == 0) TRACE(4, t);
+      const bool any_rescale = flags[0] != 0;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = ex2(s[c] - fs[F_M + 64 * g + c]);
+        const float p1 = ex2(s[c + 1] - fs[F_M + 64 * g + c + 1]);
+        const uint32_t w2 = pack_bf16x2(p0, p1);
+        pk[c >> 1] = w2;
+        l_acc[c] = fmaf(l_acc[c], fs[F_ALPHA + 64 * g + c], __uint_as_float(w2 << 16));
+        l_acc[c + 1] = fmaf(l_acc[c + 1], fs[F_ALPHA + 64 * g + c + 1], __uint_as_float(w2 & 0xFFFF0000u));
+      }
+      if (t > 0) {
+        ok = wait_bar(&bars->o_done, (t - 1) & 1, cx);
+        ok = bar_and(4, 256, ok);
+        if (!ok) break;
+        if (stid == 0) TRACE(5, t);
+        tc_fence_after();
+        if (any_rescale) {
+#pragma unroll 1
+          for (int blk = 0; blk < 2; ++blk)
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+              float o[32];
+              const uint32_t ta = lane_addr + 256 + blk * 128 + 64 * g + hh * 32;
+              tmem_ld32(ta, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] *= fs[F_ALPHA + 64 * g + hh * 32 + x];
+              tmem_st32(ta, o);
+            }
+          tmem_st_wait();
+        }
+      }
+      // P^T row k of the tile: heads [64g, 64g+64) -> CTA g's shared memory
+      const int k = (int)rank * 128 + i;
+      const uint32_t roff = (uint32_t)(k * 128);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 v4 = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        const uint32_t off = roff + (uint32_t)((cc ^ (k & 7)) * 16);
+        if (g == (int)rank)
+          *reinterpret_cast<uint4*>(sm + OFF_P + off) = v4;
+        else
+          st_async_v4_b32(peer_p + off, v4, peer_p_bar);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && sw == 4) TRACE(12, t);
+      if (lane == 0) {
+        if (sw == 0) {
+          mbar_arrive_expect_tx(&bars->p_landed, 16384);
+          TRACE(6, t);
+        } else {
+          mbar_arrive(&bars->p_landed);
+        }
+      }
+    }
+    if (ok) {
+      // ------------------------------------------------------------ epilogue
+      ok = wait_bar(&bars->o_done, (nt - 1) & 1, cx);
+      ok = bar_and(5, 256, ok);
+      if (ok) {
+        tc_fence_after();
+        // per-head sums of P over this warp's tokens
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float v = l_acc[c];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = v;
+        }
+        bar_and(6, 256, true);
+        const uint32_t peer_l = mapa(smem_u32(fs + F_LRCV), peer);
+        const uint32_t peer_l_bar = mapa(smem_u32(&bars->l_landed), peer);
+        if (stid < kH) {
+          const int h = stid, gg = h >> 6, cc = h & 63;
+          float sum = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sum += fs[F_COL + (gg * 4 + q) * 64 + cc];
+          fs[F_LLOC + h] = sum;
+          st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(sum), peer_l_bar);
+        }
+        bool ok3 = true;
+        if (stid == 0) mbar_arrive_expect_tx(&bars->l_landed, kH * 4);
+        if (stid < kH) {
+          ok3 = wait_bar(&bars->l_landed, 0, cx);
+          const int h = stid;
+          const float mine = fs[F_LLOC + h], other = fs[F_LRCV + h];
+          const float Lsum = rank == 0 ? mine + other : other + mine;
+          fs[F_INV + h] = Lsum > 0.f ? 1.f / Lsum : 0.f;
+          if (rank == 0) {
+            const float lse = Lsum > 0.f ? (fs[F_M + h] + log2f(Lsum)) * 0.6931471805599453f
+                                         : -CUDART_INF_F;
+            const size_t o = (size_t)row * kH + h;
+            if (prm.S == 1) {
+              if (prm.lse) prm.lse[o] = lse;
+            } else {
+              prm.ws_lse[o * prm.S + split] = lse;
+            }
+          }
+        }
+        ok = bar_and(7, 256, ok3);
+        if (ok) {
+#pragma unroll 1
+          for (int blk = 0; blk < 2; ++blk) {
+            const int dc = blk * 256 + (int)rank * 128 + i;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+              float o[32];
+              tmem_ld32(lane_addr + 256 + blk * 128 + 64 * g + hh * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) {
+                const int h = 64 * g + hh * 32 + x;
+                const float val = o[x] * fs[F_INV + h];
+                const size_t orow = (size_t)row * kH + h;
+                if (prm.S == 1)
+                  prm.o_lat[orow * kC + dc] = __float2bfloat16_rn(val);
+                else
+                  prm.ws_o[(orow * prm.S + split) * kC + dc] = val;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown
+  if (tid == 128) TRACE(10, 0);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a [rows][576] row-major array, 64 x 64 boxes, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kCR, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kCR * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int pick_splits(int B, int n_q, int max_seq_len, int num_splits, int num_sms) {
+  if (num_splits > 0) return num_splits;
+  const int units = B * n_q;
+  const int pairs = num_sms / 2;
+  const int tiles = (max_seq_len + kTile - 1) / kTile;
+  if (units * 4 >= pairs * 3) return 1;   // the batch alone fills >= 3/4 of the pairs
+  int S = pairs / units;
+  if (S > tiles) S = tiles;
+  return S < 1 ? 1 : S;
+}
+
+}  // namespace tc
+
+bool tc_supported(const Dims& d, int n_q) {
+  return d.H == tc::kH && d.C == tc::kC && d.R == tc::kR && d.P == tc::kP &&
+         d.act_dtype == MLA_BF16 && d.cache_dtype == MLA_BF16 && n_q >= 1 && n_q <= 2;
+}
+
+size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,
+                          int num_sms) {
+  const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, num_sms);
+  if (S <= 1) return 0;
+  const size_t rows = (size_t)B * n_q * d.H;
+  return rows * S * ((size_t)d.C + 1) * sizeof(float);
+}
+
+cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool, const int32_t* bt,
+                             int maxp, int num_pages, const int32_t* seq_lens, int B, int n_q,
+                             int max_seq_len, int num_splits, void* ws, size_t ws_bytes,
+                             void* o_lat, float* lse, int32_t* status, cudaStream_t stream) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, sms);
+  CUtensorMap tmQ, tmK;
+  if (!tc::make_map(&tmQ, q_lat, (uint64_t)B * n_q * d.H)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&tmK, pool, (uint64_t)num_pages * d.P)) return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(tc::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tc::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  tc::Params prm;
+  prm.pool = static_cast<const uint8_t*>(pool);
+  prm.bt = bt;
+  prm.maxp = maxp;
+  prm.num_pages = num_pages;
+  prm.seq_lens = seq_lens;
+  prm.B = B;
+  prm.n_q = n_q;
+  prm.max_seq_len = max_seq_len;
+  prm.S = S;
+  prm.scale_log2 = d.scale * 1.4426950408889634f;
+  prm.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+  prm.lse = lse;
+  const size_t rows = (size_t)B * n_q * d.H;
+  prm.ws_o = S > 1 ? static_cast<float*>(ws) : nullptr;
+  prm.ws_lse = S > 1 ? static_cast<float*>(ws) + rows * S * d.C : nullptr;
+  prm.status = status;
+  (void)ws_bytes;
+  const unsigned grid = 2u * (unsigned)(B * n_q * S);
+  tc::decode_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tmQ, tmK, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || S == 1) return e;
+  return launch_combine(d.C, S, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, rows, stream);
 }
 
 }  // namespace mla
+
+#ifdef MLA_TC_TRACE
+extern "C" int mla_debug_set_tc_trace(void* p) {
+  return cudaMemcpyToSymbol(mla::tc::g_tc_trace, &p, sizeof(p)) == cudaSuccess ? 0 : -1;
+}
+#endif

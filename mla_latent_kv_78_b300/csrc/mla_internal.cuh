@@ -24,6 +24,10 @@ cudaError_t launch_decode_simt(const Dims& d, const void* q_lat, const void* poo
                                int B, int n_q, int max_seq_len, int S, void* ws, void* o_lat,
                                float* lse, int32_t* status, cudaStream_t stream);
 
+// Log-sum-exp merge of split partials ws_o [rows][S][C], ws_lse [rows][S] into o_lat, lse.
+cudaError_t launch_combine(int C, int S, const float* ws_o, const float* ws_lse, void* o_lat,
+                           int act_dtype, float* lse, size_t rows, cudaStream_t stream);
+
 // Tensor-core decode (tcgen05 + TMEM + TMA), V2 head shapes only.
 bool tc_supported(const Dims& d, int n_q);
 size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,

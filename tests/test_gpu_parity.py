@@ -23,6 +23,8 @@ needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a C
 SMALL_BF16 = W.small_v2(4, [65, 200, 7, 130], n_q=1, cache="bf16", seed=11)
 SMALL_FP8 = W.small_v2(3, [129, 64, 70], n_q=2, cache="fp8", seed=12)
 SMALL_BF16_MTP = W.small_v2(3, [2, 100, 191], n_q=2, cache="bf16", seed=13)
+SMALL_BF16_LONG = W.small_v2(4, [700, 257, 1000, 64], n_q=1, cache="bf16", seed=14)
+SMALL_BF16_LONG_MTP = W.small_v2(3, [513, 256, 900], n_q=2, cache="bf16", seed=15)
 TINY = W.config(1)
 TINY_PERM = W.config(1).with_(permute_pages=True)
 
@@ -116,8 +118,9 @@ def _decode_only(wl, kernel, num_splits=0):
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP],
-                         ids=lambda w: w.name + ("-perm" if w.permute_pages else ""))
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP,
+                                SMALL_BF16_LONG, SMALL_BF16_LONG_MTP],
+                         ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + f"-L{max(w.seq_lens)}")
 @pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
 def test_decode_latent_attention(wl, kernel):
     _decode_only(wl, kernel)
@@ -125,21 +128,31 @@ def test_decode_latent_attention(wl, kernel):
 
 @needs_cuda
 @pytest.mark.parametrize("splits", [2, 3, 7])
-def test_decode_splits_agree(splits):
-    wl = SMALL_BF16
-    base = _decode_only(wl, M.MLA_KERNEL_SIMT, 1)
-    other = _decode_only(wl, M.MLA_KERNEL_SIMT, splits)
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_decode_splits_agree(splits, kernel):
+    wl = SMALL_BF16_LONG
+    base = _decode_only(wl, kernel, 1)
+    other = _decode_only(wl, kernel, splits)
     a = base.step.o_lat.float().cpu().numpy()
     b = other.step.o_lat.float().cpu().numpy()
-    # split partials are fp32; only the final bf16 rounding may differ (one ulp)
+    # split partials are fp32; the final bf16 rounding may differ by one ulp, and the
+    # tensor-core kernel sums P after rounding it to bf16 relative to each split's own
+    # reference maximum, so lse may move by up to one bf16 rounding (2^-9 relative in l)
     assert np.max(np.abs(a - b)) <= 2.0 ** -8 * np.max(np.abs(a))
     np.testing.assert_allclose(other.step.lse.cpu().numpy(), base.step.lse.cpu().numpy(),
-                               rtol=1e-5, atol=1e-5)
+                               rtol=0, atol=2.0 ** -9)
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP],
-                         ids=lambda w: w.name + ("-perm" if w.permute_pages else ""))
+def test_tensor_core_kernel_is_selected_for_v2_shapes():
+    for wl in (SMALL_BF16, SMALL_BF16_MTP):
+        assert M.mla_decode_kernel(config_of(wl), wl.B, wl.n_q) == M.MLA_KERNEL_TC
+    assert M.mla_decode_kernel(config_of(TINY), TINY.B, 1) == M.MLA_KERNEL_SIMT
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP, SMALL_BF16_LONG],
+                         ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + f"-L{max(w.seq_lens)}")
 def test_decode_step_end_to_end(wl):
     """append -> absorb -> decode -> unabsorb against the non-absorbed oracle."""
     case = Case(wl)
@@ -153,9 +166,10 @@ def test_decode_step_end_to_end(wl):
 
 
 @needs_cuda
-def test_decode_is_deterministic():
-    wl = SMALL_BF16
-    case = Case(wl)
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_is_deterministic(splits):
+    wl = SMALL_BF16_LONG
+    case = Case(wl, num_splits=splits)
     case.run_step()
     first = case.step.o_lat.clone()
     for _ in range(3):
@@ -165,11 +179,12 @@ def test_decode_is_deterministic():
 
 
 @needs_cuda
-def test_bad_page_id_is_flagged_and_skipped():
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_bad_page_id_is_flagged_and_skipped(kernel):
     """A page id outside the pool sets MLA_DEV_INDEX_OUT_OF_RANGE; the other sequences'
     results are unaffected and nothing outside the pool is touched."""
     wl = SMALL_BF16
-    case = Case(wl)
+    case = Case(wl, kernel=kernel)
     case.run_step()
     good = case.step.o_lat.clone()
     bt = case.step.block_table.clone()
@@ -184,10 +199,11 @@ def test_bad_page_id_is_flagged_and_skipped():
 
 
 @needs_cuda
-def test_short_sequence_is_flagged():
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_short_sequence_is_flagged(kernel):
     """seq_lens[b] < n_q cannot hold this step's tokens: MLA_DEV_BAD_SEQLEN."""
     wl = SMALL_BF16_MTP
-    case = Case(wl)
+    case = Case(wl, kernel=kernel)
     case.run_step()
     sl = case.step.seq_lens.clone()
     sl[0] = 1
