@@ -41,38 +41,42 @@ using namespace ptx;
 constexpr int kH = 128, kC = 512, kR = 64, kCR = 576, kP = 64;
 constexpr int kTile = 256;           // tokens per tile (4 pages)
 constexpr int kNS = 3;               // S-phase ring: [128 tok x 64 dims] bf16 = 16 KB
-constexpr int kNV = 2;               // V-phase ring: [64 tok x 256 d_c] bf16 = 32 KB
-constexpr int kKCh = kCR / 64;       // 9 dim chunks
+constexpr int kNV = 2;               // V-phase ring: [32 tok x 256 d_c] bf16 = 16 KB
+constexpr int kKCh = kCR / 64;       // 9 dim chunks per tile
+constexpr int kVCh = kTile / 32;     // 8 latent chunks per tile
 constexpr int kThreads = 384;
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
-constexpr int kPrefetchTiles = 2;    // this CTA's pages are prefetched into L2 this far ahead
 constexpr uint32_t kPageBytes = kP * kCR * 2;   // 73,728 B: one page is contiguous in the pool
+constexpr int kPrefetch = 0;         // 1: prefetch the next tile's pages into L2 (measured slower)
+constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
+constexpr uint32_t kXBytes = kXPBytes + kH * 4;  // + that tile's per-head maxima
+constexpr size_t kXUnitBytes = 4 * (size_t)kXBytes + 2 * kH * 4;  // per (seq, row, split)
 
 constexpr int OFF_Q = 0;                           // 9 x [64 heads x 64 dims]  (8 KB each)
 constexpr int OFF_S = OFF_Q + kKCh * 8192;         // kNS x 16 KB
-constexpr int OFF_V = OFF_S + kNS * 16384;         // kNV x 32 KB
-constexpr int OFF_P = OFF_V + kNV * 32768;         // [256 tok x 64 heads] = 32 KB
-constexpr int OFF_F = OFF_P + 32768;               // fp32 scratch
+constexpr int OFF_V = OFF_S + kNS * 16384;         // kNV x 16 KB
+constexpr int OFF_P = OFF_V + kNV * 16384;         // 2 x [256 tok x 64 heads] = 2 x 32 KB
+constexpr int OFF_F = OFF_P + 2 * 32768;           // fp32 scratch
 constexpr int F_COL = 0;       // [8 warps][64]   column max / column sum partials
-constexpr int F_CMLOC = 512;   // [128]
-constexpr int F_CMRCV = 640;   // [2][128]
-constexpr int F_M = 896;       // [128] running reference max (log2 units)
-constexpr int F_ALPHA = 1024;  // [128]
-constexpr int F_LLOC = 1152;   // [128]
-constexpr int F_LRCV = 1280;   // [128]
-constexpr int F_INV = 1408;    // [128]
-constexpr int F_FLAG = 1536;   // ints: [0] rescale, [1] abort
-constexpr int F_END = 1544;
+constexpr int F_CMLOC = 512;   // [2][128] this CTA's per-head tile maxima
+constexpr int F_CMRCV = 768;   // [4][128] the peer's per-head tile maxima
+constexpr int F_M = 1280;      // [128] reference max (log2 units), identical in both CTAs
+constexpr int F_ALPHA = 1408;  // [128]
+constexpr int F_LLOC = 1536;   // [128]
+constexpr int F_LRCV = 1664;   // [128]
+constexpr int F_INV = 1792;    // [128]
+constexpr int F_FLAG = 1920;   // ints: [0] rescale, [1] abort
+constexpr int F_END = 1928;
 constexpr int OFF_BAR = OFF_F + F_END * 4;
 
 struct Bars {
-  uint64_t q_landed, q_ready;
-  uint64_t s_landed[kNS], s_ready[kNS], s_free[kNS];
+  uint64_t q_ready;
+  uint64_t s_ready[kNS], s_free[kNS];
   uint64_t v_landed[kNV], v_ready[kNV], v_free[kNV];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_landed, p_ready;
-  uint64_t o_done;
-  uint64_t cm_landed[2];
+  uint64_t p_landed[2], p_ready[2], o_done[2];
+  uint64_t x_ready[2];   // the peer has put P^T(t) and its maxima of tile t in global memory
+  uint64_t x0_ready;     // the peer has put its tile-0 maxima in global memory
   uint64_t l_landed;
   uint64_t teardown;
   uint32_t tmem_base;
@@ -90,6 +94,7 @@ struct Params {
   float* lse;
   float* ws_o;
   float* ws_lse;
+  uint8_t* xws;          // exchange area, kXUnitBytes per unit
   int32_t* status;
 };
 
@@ -147,7 +152,7 @@ __device__ __forceinline__ void arrive_even(uint64_t* bar, uint32_t rank) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const Params prm) {
+                  const __grid_constant__ CUtensorMap tmV, const Params prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -198,29 +203,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   }
 
+  // exchange area of this unit: [rank][parity] {P^T 16 KB, maxima 512 B}, then [rank] tile-0 maxima
+  uint8_t* xunit = prm.xws + (size_t)unit * kXUnitBytes;
+  auto x_slot = [&](uint32_t r, int par) { return xunit + (size_t)(r * 2 + par) * kXBytes; };
+  float* x0_mine = reinterpret_cast<float*>(xunit + 4 * (size_t)kXBytes + rank * kH * 4);
+  const float* x0_peer = reinterpret_cast<const float*>(xunit + 4 * (size_t)kXBytes + peer * kH * 4);
+
   // ---- set-up
   if (tid == 0) TRACE(11, 0);
   if (tid == 0) {
-    mbar_init(&bars->q_landed, 1);
-    mbar_init(&bars->q_ready, 2);
+    // *_ready live in the even CTA: one arrival (its producer registers both CTAs' bytes)
+    // plus the bytes of both CTAs' loads, which signal it directly
+    mbar_init(&bars->q_ready, 1);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&bars->s_landed[s], 1);
-      mbar_init(&bars->s_ready[s], 2);
+      mbar_init(&bars->s_ready[s], 1);
       mbar_init(&bars->s_free[s], 1);
     }
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&bars->v_landed[s], 1);
-      mbar_init(&bars->v_ready[s], 2);
+      mbar_init(&bars->v_ready[s], 1);
       mbar_init(&bars->v_free[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->s_empty[s], 16);
-      mbar_init(&bars->cm_landed[s], 1);
+      mbar_init(&bars->p_landed[s], 8);
+      mbar_init(&bars->p_ready[s], 2);
+      mbar_init(&bars->o_done[s], 1);
+      mbar_init(&bars->x_ready[s], 1);
     }
-    mbar_init(&bars->p_landed, 8);
-    mbar_init(&bars->p_ready, 2);
-    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->x0_ready, 1);
     mbar_init(&bars->l_landed, 1);
     mbar_init(&bars->teardown, 1);
     fence_mbarrier_init_cluster();
@@ -250,65 +262,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================================================================ TMA producer
+    // Q once, then every tile's key chunks in order
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
       const uint64_t pol_q = policy_evict_last();
       const uint64_t pol_s = policy_evict_normal();  // re-read soon for the V phase
-      const uint64_t pol_v = policy_evict_first();
-      mbar_arrive_expect_tx(&bars->q_landed, kKCh * 8192);
+      const bool even = rank == 0;
+      auto at_even = [&](uint64_t* bar) { return mapa(smem_u32(bar), 0); };
+      if (even) mbar_arrive_expect_tx(&bars->q_ready, 2 * kKCh * 8192);
       for (int c = 0; c < kKCh; ++c)
-        tma_load_2d(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
-                    &bars->q_landed, pol_q);
-      // pages of this CTA's token rows, prefetched into L2 ahead of the smem loads
-      auto prefetch_tile = [&](int t) {
-        if (t >= nt) return;
+        tma_load_2d_pair(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
+                         at_even(&bars->q_ready), pol_q);
+      int s_cnt = 0;
+      auto load_s_chunk = [&](int c, int y0, int y1) -> bool {
+        const int st = s_cnt % kNS;
+        if (s_cnt >= kNS && !wait_bar(&bars->s_free[st], ((s_cnt / kNS) - 1) & 1, cx)) return false;
+        if (even) mbar_arrive_expect_tx(&bars->s_ready[st], 2 * 16384);
+        const uint32_t bar = at_even(&bars->s_ready[st]);
+        tma_load_2d_pair(sm + OFF_S + st * 16384, &tmK, c * 64, y0, bar, pol_s);
+        tma_load_2d_pair(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, bar, pol_s);
+        ++s_cnt;
+        return true;
+      };
+      // this CTA's two pages of a future tile, into L2 (kPrefetch = 0 disables)
+      auto prefetch_next = [&](int t) {
+        if (kPrefetch == 0 || t >= nt) return;
         for (int q = 0; q < 2; ++q) {
           const int y = page_y(4 * t + 2 * (int)rank + q);
           if (y < prm.num_pages * kP) prefetch_l2(prm.pool + (size_t)y * kCR * 2, kPageBytes);
         }
       };
-      for (int t = 0; t < kPrefetchTiles; ++t) prefetch_tile(t);
-      int s_cnt = 0, v_cnt = 0;
+      // key chunks of every tile in order (the latent chunks have their own producer)
       bool ok = true;
-      auto load_v = [&](int tp, int v) -> bool {
-        const int st = v_cnt % kNV;
-        if (v_cnt >= kNV && !wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx)) return false;
-        mbar_arrive_expect_tx(&bars->v_landed[st], 32768);
-        const int y = page_y(4 * tp + v);
-        for (int q4 = 0; q4 < 4; ++q4)
-          tma_load_2d(sm + OFF_V + st * 32768 + q4 * 8192, &tmK,
-                      (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, &bars->v_landed[st],
-                      pol_v);
-        ++v_cnt;
-        return true;
-      };
-      for (int t = 0; t <= nt && ok; ++t) {
-        // V chunks of tile t-1 that fit in the ring go first, so they land while S^T(t) runs
-        int v_issued = 0;
-        if (t >= 1)
-          for (; v_issued < kNV && ok; ++v_issued) ok = load_v(t - 1, v_issued);
-        if (t < nt && ok) {
-          prefetch_tile(t + kPrefetchTiles);
-          const int y0 = page_y(4 * t + 2 * (int)rank), y1 = page_y(4 * t + 2 * (int)rank + 1);
-          for (int c = 0; c < kKCh && ok; ++c, ++s_cnt) {
-            const int st = s_cnt % kNS;
-            if (s_cnt >= kNS) ok = wait_bar(&bars->s_free[st], ((s_cnt / kNS) - 1) & 1, cx);
-            if (!ok) break;
-            mbar_arrive_expect_tx(&bars->s_landed[st], 16384);
-            if (c == 4) TRACE(15, t);
-            tma_load_2d(sm + OFF_S + st * 16384, &tmK, c * 64, y0, &bars->s_landed[st], pol_s);
-            tma_load_2d(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, &bars->s_landed[st], pol_s);
-          }
-          TRACE(8, t);
+      for (int k = 0; k < nt && ok; ++k) {
+        prefetch_next(k + 1);
+        const int ys0 = page_y(4 * k + 2 * (int)rank);
+        const int ys1 = page_y(4 * k + 2 * (int)rank + 1);
+        for (int c = 0; c < kKCh && ok; ++c) {
+          if (c == 4) TRACE(15, k);
+          ok = load_s_chunk(c, ys0, ys1);
         }
-        if (t >= 1)
-          for (; v_issued < 4 && ok; ++v_issued) ok = load_v(t - 1, v_issued);
       }
       if (!ok) {
-        // drain loads still in flight into this CTA's shared memory
-        for (int k = max(0, s_cnt - kNS); k < s_cnt; ++k) wait_drain(&bars->s_landed[k % kNS], (k / kNS) & 1);
-        for (int k = max(0, v_cnt - kNV); k < v_cnt; ++k) wait_drain(&bars->v_landed[k % kNV], (k / kNV) & 1);
+        // drain this CTA's loads still in flight: wait until the even CTA's MMA issuer has
+        // stopped and enough time has passed for any issued load to land
+        const long long t0 = clock64();
+        while (clock64() - t0 < 2000000) {
+        }
       }
     }
   } else if (warp == 1) {
@@ -318,56 +320,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t idPV = idesc_bf16_f32(256, 128, 1, 1);
       const uint32_t sQ = smem_u32(sm + OFF_Q), sS = smem_u32(sm + OFF_S);
       const uint32_t sV = smem_u32(sm + OFF_V), sP = smem_u32(sm + OFF_P);
-      bool ok = wait_bar(&bars->q_ready, 0, cx);
       int s_cnt = 0, v_cnt = 0;
-      for (int t = 0; t <= nt && ok; ++t) {
-        if (t < nt) {
-          const int buf = t & 1;
-          if (t >= 2) ok = wait_bar(&bars->s_empty[buf], ((t - 2) >> 1) & 1, cx);
-          if (!ok) break;
-          tc_fence_after();
-          for (int c = 0; c < kKCh; ++c, ++s_cnt) {
-            const int st = s_cnt % kNS;
-            ok = wait_bar(&bars->s_ready[st], (s_cnt / kNS) & 1, cx);
-            if (!ok) break;
-            if (c == 0) TRACE(9, t);
-            tc_fence_after();
+      auto mma_s_chunk = [&](int t, int c) -> bool {
+        const int st = s_cnt % kNS;
+        if (!wait_bar(&bars->s_ready[st], (s_cnt / kNS) & 1, cx)) return false;
+        tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
-              const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
-              mma_bf16_pair(tmem + buf * 128, a, bd, idS, (c | k) != 0);
-            }
-            mma_commit_pair(&bars->s_free[st], 0x3);
-          }
-          if (!ok) break;
-          mma_commit_pair(&bars->s_full[buf], 0x3);
-          TRACE(0, t);
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
+          const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
+          mma_bf16_pair(tmem + (t & 1) * 128, a, bd, idS, (c | k) != 0);
         }
-        if (t >= 1) {
-          const int tp = t - 1;
-          ok = wait_bar(&bars->p_ready, tp & 1, cx);
-          if (!ok) break;
-          TRACE(1, tp);
-          tc_fence_after();
-          for (int v = 0; v < 4; ++v, ++v_cnt) {
-            const int st = v_cnt % kNV;
-            ok = wait_bar(&bars->v_ready[st], (v_cnt / kNV) & 1, cx);
-            if (!ok) break;
-            tc_fence_after();
+        mma_commit_pair(&bars->s_free[st], 0x3);
+        ++s_cnt;
+        return true;
+      };
+      auto mma_v_chunk = [&](int t, int v) -> bool {
+        const int st = v_cnt % kNV;
+        if (!wait_bar(&bars->v_ready[st], (v_cnt / kNV) & 1, cx)) return false;
+        tc_fence_after();
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
+        for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t a = smem_desc(sV + st * 32768 + blk * 16384 + k * 2048, 8192, 1024, kSw128);
-                const uint64_t bd = smem_desc(sP + v * 8192 + k * 2048, 8192, 1024, kSw128);
-                mma_bf16_pair(tmem + 256 + blk * 128, a, bd, idPV, (tp | v | k) != 0);
-              }
-            mma_commit_pair(&bars->v_free[st], 0x3);
+          for (int k = 0; k < 2; ++k) {
+            const uint64_t a = smem_desc(sV + st * 16384 + blk * 8192 + k * 2048, 4096, 1024, kSw128);
+            const uint64_t bd = smem_desc(sP + (t & 1) * 32768 + v * 4096 + k * 2048, 8192, 1024, kSw128);
+            mma_bf16_pair(tmem + 256 + blk * 128, a, bd, idPV, (t | v | k) != 0);
           }
-          if (!ok) break;
-          mma_commit_pair(&bars->o_done, 0x3);
-          TRACE(2, tp);
+        mma_commit_pair(&bars->v_free[st], 0x3);
+        ++v_cnt;
+        return true;
+      };
+      bool ok = wait_bar(&bars->q_ready, 0, cx);
+      // step k: S^T(k) interleaved chunk for chunk with PV(k-2)
+      for (int k = 0; k < nt + 2 && ok; ++k) {
+        const bool do_s = k < nt, do_v = k >= 2;
+        if (do_s && k >= 2) ok = wait_bar(&bars->s_empty[k & 1], ((k >> 1) - 1) & 1, cx);
+        if (do_s && ok) TRACE(9, k);
+        for (int c = 0; c < kKCh && ok; ++c) {
+          if (do_s) ok = mma_s_chunk(k, c);
+          if (do_s && c == 4) TRACE(13, k);
+          if (ok && do_v && c == 0) {
+            ok = wait_bar(&bars->p_ready[k & 1], ((k - 2) >> 1) & 1, cx);
+            TRACE(1, k - 2);
+            tc_fence_after();
+          }
+          if (ok && do_v && c < kVCh) ok = mma_v_chunk(k - 2, c);
+        }
+        if (!ok) break;
+        if (do_s) {
+          mma_commit_pair(&bars->s_full[k & 1], 0x3);
+          TRACE(0, k);
+        }
+        if (do_v) {
+          mma_commit_pair(&bars->o_done[k & 1], 0x3);
+          TRACE(2, k - 2);
         }
       }
       // every MMA this thread issued (they write both CTAs' TMEM) completes before teardown
@@ -375,53 +382,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_drain(&bars->teardown, 0);
     }
   } else if (warp == 2) {
-    // ================================================================ relay
-    int s_cnt = 0, v_cnt = 0;
+    // ================================================================ latent-chunk producer
+    // Loads each tile's latent rows (this CTA's 256 d_c columns, 32 tokens per chunk) in the
+    // MMA issuer's order. On the last tile the rows past the range may hold anything (P is 0
+    // there): those chunks land on this CTA's own barrier, the warp zeroes the rows, and only
+    // then are the bytes counted on the even CTA's barrier.
+    const uint64_t pol_v = policy_evict_first();
+    const bool even = rank == 0;
+    const uint32_t even_v0 = mapa(smem_u32(&bars->v_ready[0]), 0);
+    int v_cnt = 0;
     bool ok = true;
-    if (lane == 0) ok = wait_bar(&bars->q_landed, 0, cx);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok && lane == 0) arrive_even(&bars->q_ready, rank);
-    for (int t = 0; t <= nt && ok; ++t) {
-      if (t < nt) {
-        for (int c = 0; c < kKCh && ok; ++c, ++s_cnt) {
-          const int st = s_cnt % kNS;
-          if (lane == 0) {
-            ok = wait_bar(&bars->s_landed[st], (s_cnt / kNS) & 1, cx);
-            if (c == 4) TRACE(14, t);
-            if (ok) arrive_even(&bars->s_ready[st], rank);
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+    auto finish_last = [&](int v) -> bool {   // zero + count chunk v of the last tile
+      const int st = v % kNV;                 // the last tile starts at an even chunk count
+      bool r = true;
+      if (lane == 0) r = wait_bar(&bars->v_landed[st], (v / kNV) & 1, cx);
+      if (!__shfl_sync(0xffffffffu, r, 0)) return false;
+      const int tok0 = lo + (nt - 1) * kTile + v * 32;
+      const int nvalid = max(0, min(32, hi - tok0));
+      if (nvalid < 32) {
+        uint4* base = reinterpret_cast<uint4*>(sm + OFF_V + st * 16384);
+        const int nrow = 32 - nvalid;
+        for (int idx = lane; idx < 4 * nrow * 8; idx += 32) {
+          const int sub = idx / (nrow * 8);
+          const int rr = nvalid + (idx / 8) % nrow;
+          base[sub * 256 + rr * 8 + (idx & 7)] = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      if (t >= 1 && ok) {
-        const int tp = t - 1;
+      __syncwarp();
+      if (lane == 0) {
+        fence_acq_rel_cluster();
+        mbar_complete_tx(even_v0 + st * 8, 16384);
+      }
+      return true;
+    };
+    for (int t = 0; t < nt && ok; ++t) {
+      const bool last = t == nt - 1;
+      for (int v = 0; v < kVCh && ok; ++v, ++v_cnt) {
+        const int st = v_cnt % kNV;
+        // before a slot is reused on the last tile, the chunk that held it must be counted
+        if (last && v >= kNV) ok = finish_last(v - kNV);
+        if (!ok) break;
         if (lane == 0) {
-          ok = wait_bar(&bars->p_landed, tp & 1, cx);
-          TRACE(7, tp);
-          if (ok) arrive_even(&bars->p_ready, rank);
+          if (v_cnt >= kNV) ok = wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx);
+          if (ok) {
+            if (even) mbar_arrive_expect_tx(&bars->v_ready[st], 2 * 16384);
+            uint32_t bar;
+            if (last) {
+              mbar_arrive_expect_tx(&bars->v_landed[st], 16384);
+              bar = smem_u32(&bars->v_landed[st]);
+            } else {
+              bar = mapa(smem_u32(&bars->v_ready[st]), 0);
+            }
+            const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;
+            for (int q4 = 0; q4 < 4; ++q4)
+              tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
+                               (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        for (int v = 0; v < 4 && ok; ++v, ++v_cnt) {
-          const int st = v_cnt % kNV;
-          if (lane == 0) ok = wait_bar(&bars->v_landed[st], (v_cnt / kNV) & 1, cx);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          const int tok0 = lo + tp * kTile + v * kP;
-          const int nvalid = max(0, min(kP, hi - tok0));
-          if (nvalid < kP) {
-            // rows past the range may hold anything; P is 0 there, so make them 0 too
-            uint4* base = reinterpret_cast<uint4*>(sm + OFF_V + st * 32768);
-            const int nrow = kP - nvalid;
-            for (int idx = lane; idx < 4 * nrow * 8; idx += 32) {
-              const int sub = idx / (nrow * 8);
-              const int rr = nvalid + (idx / 8) % nrow;
-              base[sub * 512 + rr * 8 + (idx & 7)] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-          if (lane == 0) arrive_even(&bars->v_ready[st], rank);
-        }
+      }
+      if (last && ok)
+        for (int v = kVCh - kNV; v < kVCh && ok; ++v) ok = finish_last(v);
+    }
+  } else if (warp == 3) {
+    // ================================================================ exchange
+    // Fetches the peer's P^T half and tile maxima once the peer has put them in global
+    // memory; reports this CTA's P^T buffer complete to the even CTA.
+    if (lane == 0) {
+      bool ok = true;
+      for (int t = 0; t < nt && ok; ++t) {
+        const int par = t & 1;
+        ok = wait_bar(&bars->x_ready[par], (t >> 1) & 1, cx);
+        if (!ok) break;
+        const uint8_t* src = x_slot(peer, par);
+        bulk_g2s(sm + OFF_P + par * 32768 + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
+        bulk_g2s(fs + F_CMRCV + (t & 3) * kH, src + kXPBytes, kH * 4, &bars->p_landed[par]);
+        ok = wait_bar(&bars->p_landed[par], (t >> 1) & 1, cx);
+        TRACE(7, t);
+        if (ok) arrive_even(&bars->p_ready[par], rank);
       }
     }
   } else if (warp >= 4) {
@@ -432,17 +471,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int i = qd * 32 + lane;      // this CTA's token row (S^T) / latent row (O^T)
     const int stid = tid - 128;        // 0..255
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
-    const uint32_t peer_cm = mapa(smem_u32(fs + F_CMRCV), peer);
-    const uint32_t peer_cm_bar0 = mapa(smem_u32(&bars->cm_landed[0]), peer);
-    const uint32_t peer_p = mapa(smem_u32(sm + OFF_P), peer);
-    const uint32_t peer_p_bar = mapa(smem_u32(&bars->p_landed), peer);
     float l_acc[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) l_acc[c] = 0.f;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
-      const int buf = t & 1;
-      ok = wait_bar(&bars->s_full[buf], (t >> 1) & 1, cx);
+      const int par = t & 1;
+      ok = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
       ok = bar_and(1, 256, ok);
       if (!ok) break;
       if (stid == 0) {
@@ -451,13 +486,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[64];
-      tmem_ld32(lane_addr + buf * 128 + 64 * g, s);
-      tmem_ld32(lane_addr + buf * 128 + 64 * g + 32, s + 32);
+      tmem_ld32(lane_addr + par * 128 + 64 * g, s);
+      tmem_ld32(lane_addr + par * 128 + 64 * g + 32, s + 32);
       tmem_ld_wait();
-      if (stid == 0) TRACE(13, t);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) arrive_even(&bars->s_empty[buf], rank);
+      if (lane == 0) arrive_even(&bars->s_empty[par], rank);
       const int tok = lo + t * kTile + (int)rank * 128 + i;
       const bool valid = tok < hi;
 #pragma unroll
@@ -469,29 +503,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
       }
       bar_and(2, 256, true);
+      // this CTA's maximum of tile t; the reference for tile t combines both CTAs'
+      // maxima of tile t-2 (tiles 0 and 1 use tile 0's, agreed before any P is made)
+      float my_max = 0.f;
+      bool ok2 = true;
       if (stid < kH) {
         const int h = stid, gg = h >> 6, cc = h & 63;
-        float mx = fs[F_COL + (gg * 4) * 64 + cc];
+        my_max = fs[F_COL + (gg * 4) * 64 + cc];
 #pragma unroll
-        for (int q = 1; q < 4; ++q) mx = fmaxf(mx, fs[F_COL + (gg * 4 + q) * 64 + cc]);
-        fs[F_CMLOC + h] = mx;
-        st_async_b32(peer_cm + (uint32_t)((buf * kH + h) * 4), __float_as_uint(mx),
-                     peer_cm_bar0 + buf * 8);
+        for (int q = 1; q < 4; ++q) my_max = fmaxf(my_max, fs[F_COL + (gg * 4 + q) * 64 + cc]);
       }
-      bool ok2 = true;
-      if (stid == 0) mbar_arrive_expect_tx(&bars->cm_landed[buf], kH * 4);
-      if (stid < kH) {
-        ok2 = wait_bar(&bars->cm_landed[buf], (t >> 1) & 1, cx);
+      if (t == 0) {
+        if (stid < kH) x0_mine[stid] = my_max;
+        __threadfence();
+        bar_and(6, 256, true);
+        if (stid == 0) mbar_arrive_remote(mapa(smem_u32(&bars->x0_ready), peer));
+        if (stid < kH) {
+          const int h = stid;
+          ok2 = wait_bar(&bars->x0_ready, 0, cx);
+          const float other = __ldcg(x0_peer + h);
+          fs[F_M + h] = fmaxf(my_max, other);
+          fs[F_ALPHA + h] = 1.f;
+          fs[F_CMLOC + h] = my_max;
+        }
+      } else if (stid < kH) {
         const int h = stid;
-        const float tmax = fmaxf(fs[F_CMLOC + h], fs[F_CMRCV + buf * kH + h]);
-        const float mo = fs[F_M + h];
         float alpha = 1.f;
-        if (tmax > mo + 8.f) {
-          alpha = ex2(mo - tmax);     // mo = -inf gives 0
-          fs[F_M + h] = tmax;
-          flags[0] = 1;
+        if (t >= 2) {
+          // tile t-2's maxima: this CTA's from shared memory, the peer's from its payload
+          ok2 = wait_bar(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
+          const float cand = fmaxf(fs[F_CMLOC + par * kH + h], fs[F_CMRCV + ((t - 2) & 3) * kH + h]);
+          const float mo = fs[F_M + h];
+          if (cand > mo + 8.f) {
+            alpha = ex2(mo - cand);
+            fs[F_M + h] = cand;
+            flags[0] = 1;
+          }
         }
         fs[F_ALPHA + h] = alpha;
+        fs[F_CMLOC + par * kH + h] = my_max;
       }
       ok = bar_and(3, 256, ok2);
       if (!ok) break;
@@ -507,57 +557,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_acc[c] = fmaf(l_acc[c], fs[F_ALPHA + 64 * g + c], __uint_as_float(w2 << 16));
         l_acc[c + 1] = fmaf(l_acc[c + 1], fs[F_ALPHA + 64 * g + c + 1], __uint_as_float(w2 & 0xFFFF0000u));
       }
-      if (t > 0) {
-        ok = wait_bar(&bars->o_done, (t - 1) & 1, cx);
-        ok = bar_and(4, 256, ok);
-        if (!ok) break;
-        if (stid == 0) TRACE(5, t);
-        tc_fence_after();
-        if (any_rescale) {
+      // O must be stable to rescale (PV(t-1) done); otherwise only P's buffer must be free (PV(t-2))
+      bool ok3 = true;
+      if (any_rescale && t >= 1)
+        ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
+      else if (t >= 2)
+        ok3 = wait_bar(&bars->o_done[par], ((t - 2) >> 1) & 1, cx);
+      ok = bar_and(4, 256, ok3);
+      if (!ok) break;
+      if (stid == 0) TRACE(5, t);
+      tc_fence_after();
+      if (any_rescale && t >= 1) {
 #pragma unroll 1
-          for (int blk = 0; blk < 2; ++blk)
+        for (int blk = 0; blk < 2; ++blk)
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
-              float o[32];
-              const uint32_t ta = lane_addr + 256 + blk * 128 + 64 * g + hh * 32;
-              tmem_ld32(ta, o);
-              tmem_ld_wait();
+          for (int hh = 0; hh < 2; ++hh) {
+            float o[32];
+            const uint32_t ta = lane_addr + 256 + blk * 128 + 64 * g + hh * 32;
+            tmem_ld32(ta, o);
+            tmem_ld_wait();
 #pragma unroll
-              for (int x = 0; x < 32; ++x) o[x] *= fs[F_ALPHA + 64 * g + hh * 32 + x];
-              tmem_st32(ta, o);
-            }
-          tmem_st_wait();
-        }
+            for (int x = 0; x < 32; ++x) o[x] *= fs[F_ALPHA + 64 * g + hh * 32 + x];
+            tmem_st32(ta, o);
+          }
+        tmem_st_wait();
       }
-      // P^T row k of the tile: heads [64g, 64g+64) -> CTA g's shared memory
+      // P^T row k of the tile, heads [64g, 64g+64): kept here if they are this CTA's heads,
+      // else written to global memory for the peer (same swizzled bytes either way)
       const int k = (int)rank * 128 + i;
-      const uint32_t roff = (uint32_t)(k * 128);
+      const uint32_t sw_off = (uint32_t)(((k & 7)) * 16);
+      if (g == (int)rank) {
+        uint8_t* dst = sm + OFF_P + par * 32768 + k * 128;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint4 v4 = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        const uint32_t off = roff + (uint32_t)((cc ^ (k & 7)) * 16);
-        if (g == (int)rank)
-          *reinterpret_cast<uint4*>(sm + OFF_P + off) = v4;
-        else
-          st_async_v4_b32(peer_p + off, v4, peer_p_bar);
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_proxy_async_smem();
+      } else {
+        uint8_t* dst = x_slot(rank, par) + i * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       }
-      fence_proxy_async_smem();
+      if (stid < kH) reinterpret_cast<float*>(x_slot(rank, par) + kXPBytes)[stid] = my_max;
+      fence_proxy_async_global();
       tc_fence_before();
+      bar_and(5, 256, true);
+      if (stid == 0) mbar_arrive_remote(mapa(smem_u32(&bars->x_ready[par]), peer));
       __syncwarp();
-      if (lane == 0 && sw == 4) TRACE(12, t);
       if (lane == 0) {
         if (sw == 0) {
-          mbar_arrive_expect_tx(&bars->p_landed, 16384);
+          mbar_arrive_expect_tx(&bars->p_landed[par], kXBytes);
           TRACE(6, t);
         } else {
-          mbar_arrive(&bars->p_landed);
+          mbar_arrive(&bars->p_landed[par]);
         }
       }
     }
     if (ok) {
       // ------------------------------------------------------------ epilogue
-      ok = wait_bar(&bars->o_done, (nt - 1) & 1, cx);
-      ok = bar_and(5, 256, ok);
+      ok = wait_bar(&bars->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
+      ok = bar_and(7, 256, ok);
       if (ok) {
         tc_fence_after();
         // per-head sums of P over this warp's tokens
@@ -568,7 +629,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
           if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = v;
         }
-        bar_and(6, 256, true);
+        bar_and(8, 256, true);
         const uint32_t peer_l = mapa(smem_u32(fs + F_LRCV), peer);
         const uint32_t peer_l_bar = mapa(smem_u32(&bars->l_landed), peer);
         if (stid < kH) {
@@ -579,10 +640,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fs[F_LLOC + h] = sum;
           st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(sum), peer_l_bar);
         }
-        bool ok3 = true;
+        bool ok4 = true;
         if (stid == 0) mbar_arrive_expect_tx(&bars->l_landed, kH * 4);
         if (stid < kH) {
-          ok3 = wait_bar(&bars->l_landed, 0, cx);
+          ok4 = wait_bar(&bars->l_landed, 0, cx);
           const int h = stid;
           const float mine = fs[F_LLOC + h], other = fs[F_LRCV + h];
           const float Lsum = rank == 0 ? mine + other : other + mine;
@@ -598,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
-        ok = bar_and(7, 256, ok3);
+        ok = bar_and(9, 256, ok4);
         if (ok) {
 #pragma unroll 1
           for (int blk = 0; blk < 2; ++blk) {
@@ -652,13 +713,13 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a [rows][576] row-major array, 64 x 64 boxes, 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
+// 2-D bf16 map over a [rows][576] row-major array, 64 x box_rows boxes, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kCR, rows};
   cuuint64_t strides[1] = {(cuuint64_t)kCR * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -683,12 +744,17 @@ bool tc_supported(const Dims& d, int n_q) {
          d.act_dtype == MLA_BF16 && d.cache_dtype == MLA_BF16 && n_q >= 1 && n_q <= 2;
 }
 
-size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,
-                          int num_sms) {
-  const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, num_sms);
+static size_t partial_bytes(const Dims& d, int B, int n_q, int S) {
   if (S <= 1) return 0;
   const size_t rows = (size_t)B * n_q * d.H;
   return rows * S * ((size_t)d.C + 1) * sizeof(float);
+}
+
+size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,
+                          int num_sms) {
+  const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, num_sms);
+  const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
+  return part + (size_t)B * n_q * S * tc::kXUnitBytes;
 }
 
 cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool, const int32_t* bt,
@@ -699,9 +765,10 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, sms);
-  CUtensorMap tmQ, tmK;
-  if (!tc::make_map(&tmQ, q_lat, (uint64_t)B * n_q * d.H)) return cudaErrorInvalidValue;
-  if (!tc::make_map(&tmK, pool, (uint64_t)num_pages * d.P)) return cudaErrorInvalidValue;
+  CUtensorMap tmQ, tmK, tmV;
+  if (!tc::make_map(&tmQ, q_lat, (uint64_t)B * n_q * d.H, 64)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&tmK, pool, (uint64_t)num_pages * d.P, 64)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&tmV, pool, (uint64_t)num_pages * d.P, 32)) return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(tc::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -709,6 +776,9 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  const size_t rows = (size_t)B * n_q * d.H;
+  const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
+  if (ws_bytes < part + (size_t)B * n_q * S * tc::kXUnitBytes) return cudaErrorInvalidValue;
   tc::Params prm;
   prm.pool = static_cast<const uint8_t*>(pool);
   prm.bt = bt;
@@ -722,13 +792,12 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.scale_log2 = d.scale * 1.4426950408889634f;
   prm.o_lat = static_cast<__nv_bfloat16*>(o_lat);
   prm.lse = lse;
-  const size_t rows = (size_t)B * n_q * d.H;
   prm.ws_o = S > 1 ? static_cast<float*>(ws) : nullptr;
   prm.ws_lse = S > 1 ? static_cast<float*>(ws) + rows * S * d.C : nullptr;
+  prm.xws = static_cast<uint8_t*>(ws) + part;
   prm.status = status;
-  (void)ws_bytes;
   const unsigned grid = 2u * (unsigned)(B * n_q * S);
-  tc::decode_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tmQ, tmK, prm);
+  tc::decode_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tmQ, tmK, tmV, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return e;
   return launch_combine(d.C, S, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, rows, stream);
