@@ -1,0 +1,305 @@
+// K2 / K5 on tensor cores: query-side and output-side absorption for the V2 head shapes
+// (d_h = 128, d_c = 512, d_h^R = 64, bf16), one CTA per (head, token tile).
+//
+// 「一文通透DeepSeek-V2」 §2.2.1 (last paragraph): W^{UK} is absorbed into the query side and
+// W^{UV} into the output side. Per head i these are small GEMMs whose cost is reading the
+// head's 128 KB weight block once:
+//   absorb:   q_lat[t][i][0:512]  = q_c[t][i][:] . W_UK[i]      (D = W_UK[i]^T . q_c^T: M = 512 latent
+//             rows in four 128-row tiles, N = tokens, K = 128; W_UK[i] is the MN-major A operand)
+//             q_lat[t][i][512:576] = RoPE_pos[t](q_r[t][i])
+//   unabsorb: o[t][i][0:128]      = W_UV[i] . o_lat[t][i][:]    (D = W_UV[i] . o_lat^T: M = 128,
+//             N = tokens, K = 512)
+// Operands arrive by TMA (128-byte swizzle), the MMAs are tcgen05 kind::f16 with fp32 TMEM
+// accumulators, and the epilogue reads TMEM lane = output column.
+#include "mla_internal.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.cuh"
+
+namespace mla {
+namespace tca {
+
+using namespace ptx;
+
+constexpr int kD = 128, kC = 512, kR = 64;
+constexpr long long kTimeout = 4000000000LL;
+
+struct AbsorbParams {
+  int T, H;
+  const __nv_bfloat16* q_r;
+  const int32_t* pos;
+  __nv_bfloat16* q_lat;
+  int32_t* status;
+  float theta_hi[kR / 2], theta_lo[kR / 2];   // RoPE frequencies base^(-2k/R) as hi + lo floats
+};
+
+struct UnabsorbParams {
+  int T, H;
+  float* o;
+  int32_t* status;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity)) {
+    if (clock64() - t0 > kTimeout) {
+      flag_status(status, MLA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// cos/sin of pos * theta without fp64: the angle is carried as a float pair (exact product of
+// the integer position with theta_hi via FMA, plus pos * theta_lo), reduced by 2*pi with a
+// three-part Cody-Waite split (6.28125 + 0.0019350051879882812 + 3.0199160e-07; the first two
+// products are exact for |n| < 2^15, i.e. positions up to ~2e5), then evaluated with sincosf.
+__device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float* c, float* s) {
+  const float p = (float)pos;
+  const float a_hi = p * th_hi;
+  const float a_lo = fmaf(p, th_hi, -a_hi) + p * th_lo;
+  const float n = rintf(a_hi * 0.15915493667125702f);
+  float r = fmaf(-n, 6.28125f, a_hi);
+  r = fmaf(-n, 0.0019350051879882812f, r);
+  r = fmaf(-n, 3.019916050561733e-07f, r);
+  r += a_lo;
+  sincosf(r, s, c);
+}
+
+// ------------------------------------------------------------------ absorb
+// D[token][c] = q_c[token] . W_UK[i][:, c]: M = 128 tokens (TMEM lane = token), N = 2 x 256
+// latent columns, K = 128. A = q_c tile, 2 boxes [128 t x 64 d] (K-major);
+// B = W_UK[i] as 8 boxes [128 d x 64 c] (MN-major: latent columns contiguous).
+constexpr int kAbsNT = 128;
+constexpr int kAbsSmem = 2 * 16384 + 8 * 16384 + 64 + 1024;
+
+__global__ void __launch_bounds__(128, 1)
+    absorb_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
+                     const AbsorbParams p) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;                 // q_c
+  uint8_t* sB = sm + 2 * 16384;     // W_UK[i]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 8 * 16384);   // [0] loads, [1] mma
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int i = blockIdx.x, t0 = blockIdx.y * kAbsNT;
+  const int nt = min(kAbsNT, p.T - t0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(&bars[0], 10 * 16384);
+    for (int kb = 0; kb < 2; ++kb) tma_load_3d(sA + kb * 16384, &tmQ, kb * 64, i, t0, &bars[0], pol);
+    for (int j = 0; j < 8; ++j) tma_load_2d(sB + j * 16384, &tmW, j * 64, i * kD, &bars[0], pol);
+    if (wait_bounded(&bars[0], 0, p.status)) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16_f32(128, 256, 0, 1);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int n = 0; n < 2; ++n)
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSw128);
+          const uint64_t b = smem_desc(b0 + n * 4 * 16384 + kk * 2048, 16384, 1024, kSw128);
+          mma_bf16(tmem + n * 256, a, b, id, kk > 0);
+        }
+    }
+    mma_commit(&bars[1]);
+  }
+  // this thread's token: RoPE part while the MMAs run
+  const int t = warp * 32 + lane;
+  const bool valid = t < nt;
+  const size_t row = ((size_t)(t0 + t) * p.H + i);
+  if (valid) {
+    const int pos = p.pos[t0 + t];
+    const uint4* src = reinterpret_cast<const uint4*>(p.q_r + row * kR);
+    uint4* dst = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + kC);
+#pragma unroll
+    for (int q = 0; q < kR / 8; ++q) {
+      const uint4 x = src[q];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = q * 4 + e;
+        float c, s;
+        rope_cs(pos, p.theta_hi[k], p.theta_lo[k], &c, &s);
+        const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
+        o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+      }
+      dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  wait_bounded(&bars[1], 0, p.status);
+  tc_fence_after();
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  uint4* out = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR));
+#pragma unroll 1
+  for (int cc = 0; cc < kC / 32; ++cc) {
+    float v[32];
+    tmem_ld32(lane_base + cc * 32, v);
+    tmem_ld_wait();
+    if (valid) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        out[cc * 4 + q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                     pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ unabsorb
+// smem: A = W_UV[i] as 8 boxes [128 r x 64 c] (16 KB) | B = o_lat tile as 8 boxes [64 t x 64 c]
+constexpr int kUnNT = 64;
+constexpr int kUnSmem = 8 * 16384 + 8 * 8192 + 64 + 1024;
+
+__global__ void __launch_bounds__(128, 1)
+    unabsorb_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmO,
+                       const UnabsorbParams p) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = sm;
+  uint8_t* sB = sm + 8 * 16384;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 8 * 8192);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int i = blockIdx.x, t0 = blockIdx.y * kUnNT;
+  const int nt = min(kUnNT, p.T - t0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(slot, 64);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(&bars[0], 8 * 16384 + 8 * 8192);
+    for (int j = 0; j < 8; ++j) tma_load_2d(sA + j * 16384, &tmW, j * 64, i * kD, &bars[0], pol);
+    for (int j = 0; j < 8; ++j) tma_load_3d(sB + j * 8192, &tmO, j * 64, i, t0, &bars[0], pol);
+    if (wait_bounded(&bars[0], 0, p.status)) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16_f32(128, kUnNT, 0, 0);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int kk = 0; kk < 32; ++kk) {
+        const uint64_t a = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSw128);
+        const uint64_t b = smem_desc(b0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSw128);
+        mma_bf16(tmem, a, b, id, kk > 0);
+      }
+    }
+    mma_commit(&bars[1]);
+  }
+  wait_bounded(&bars[1], 0, p.status);
+  tc_fence_after();
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  const int r = warp * 32 + lane;
+  for (int cc = 0; cc < kUnNT / 32; ++cc) {
+    float v[32];
+    tmem_ld32(lane_base + cc * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      const int t = cc * 32 + x;
+      if (t < nt) p.o[((size_t)(t0 + t) * p.H + i) * kD + r] = v[x];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+}  // namespace tca
+
+bool absorb_tc_supported(const Dims& d) {
+  return d.act_dtype == MLA_BF16 && d.D == tca::kD && d.C == tca::kC && d.R == tca::kR;
+}
+
+cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, const int32_t* pos,
+                             int T, const void* w_uk, void* q_lat, cudaStream_t stream) {
+  CUtensorMap tmW, tmQ;
+  {
+    const uint64_t dims[2] = {(uint64_t)tca::kC, (uint64_t)d.H * tca::kD};
+    const uint64_t st[1] = {(uint64_t)tca::kC * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_bf16_map(&tmW, w_uk, 2, dims, st, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)tca::kD, (uint64_t)d.H, (uint64_t)T};
+    const uint64_t st[2] = {(uint64_t)tca::kD * 2, (uint64_t)d.H * tca::kD * 2};
+    const uint32_t box[3] = {64, 1, tca::kAbsNT};
+    if (!encode_bf16_map(&tmQ, q_c, 3, dims, st, box)) return cudaErrorInvalidValue;
+  }
+  tca::AbsorbParams p;
+  p.T = T;
+  p.H = d.H;
+  p.q_r = static_cast<const __nv_bfloat16*>(q_r);
+  p.pos = pos;
+  p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
+  p.status = nullptr;
+  for (int k = 0; k < tca::kR / 2; ++k) {
+    const double th = pow((double)d.rope_base, -2.0 * (double)k / (double)tca::kR);
+    p.theta_hi[k] = (float)th;
+    p.theta_lo[k] = (float)(th - (double)p.theta_hi[k]);
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tca::absorb_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tca::kAbsSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(d.H, (T + tca::kAbsNT - 1) / tca::kAbsNT);
+  tca::absorb_tc_kernel<<<grid, 128, tca::kAbsSmem, stream>>>(tmW, tmQ, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unabsorb_tc(const Dims& d, const void* o_lat, int T, const void* w_uv, float* o,
+                               cudaStream_t stream) {
+  CUtensorMap tmW, tmO;
+  {
+    const uint64_t dims[2] = {(uint64_t)tca::kC, (uint64_t)d.H * tca::kD};
+    const uint64_t st[1] = {(uint64_t)tca::kC * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_bf16_map(&tmW, w_uv, 2, dims, st, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)tca::kC, (uint64_t)d.H, (uint64_t)T};
+    const uint64_t st[2] = {(uint64_t)tca::kC * 2, (uint64_t)d.H * tca::kC * 2};
+    const uint32_t box[3] = {64, 1, tca::kUnNT};
+    if (!encode_bf16_map(&tmO, o_lat, 3, dims, st, box)) return cudaErrorInvalidValue;
+  }
+  tca::UnabsorbParams p;
+  p.T = T;
+  p.H = d.H;
+  p.o = o;
+  p.status = nullptr;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tca::unabsorb_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tca::kUnSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(d.H, (T + tca::kUnNT - 1) / tca::kUnNT);
+  tca::unabsorb_tc_kernel<<<grid, 128, tca::kUnSmem, stream>>>(tmW, tmO, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

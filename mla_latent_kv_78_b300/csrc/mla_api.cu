@@ -121,6 +121,11 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
   if (num_tokens < 0) return MLA_ERR_INVALID_ARG;
   if (num_tokens == 0) return MLA_OK;
   if (!q_c || (!q_r && d.R > 0) || !pos || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
+  if (mla::absorb_tc_supported(d) && cfg->kernel != MLA_KERNEL_SIMT) {
+    if (!aligned16(q_c) || !aligned16(q_r) || !aligned16(w_uk) || !aligned16(q_lat))
+      return MLA_ERR_ALIGNMENT;
+    return cuda_rc(mla::launch_absorb_tc(d, q_c, q_r, pos, num_tokens, w_uk, q_lat, (cudaStream_t)stream));
+  }
   return cuda_rc(mla::launch_absorb(d, q_c, q_r, pos, num_tokens, w_uk, q_lat, (cudaStream_t)stream));
 }
 
@@ -189,6 +194,10 @@ int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, c
   if (num_tokens < 0) return MLA_ERR_INVALID_ARG;
   if (num_tokens == 0) return MLA_OK;
   if (!o_lat || !w_uv || !o) return MLA_ERR_INVALID_ARG;
+  if (mla::absorb_tc_supported(d) && cfg->kernel != MLA_KERNEL_SIMT) {
+    if (!aligned16(o_lat) || !aligned16(w_uv)) return MLA_ERR_ALIGNMENT;
+    return cuda_rc(mla::launch_unabsorb_tc(d, o_lat, num_tokens, w_uv, o, (cudaStream_t)stream));
+  }
   return cuda_rc(mla::launch_unabsorb(d, o_lat, num_tokens, w_uv, o, (cudaStream_t)stream));
 }
 

@@ -15,6 +15,13 @@ cudaError_t launch_absorb(const Dims& d, const void* q_c, const void* q_r, const
 cudaError_t launch_unabsorb(const Dims& d, const void* o_lat, int T, const void* w_uv, float* o,
                             cudaStream_t stream);
 
+// Tensor-core absorb / unabsorb (d_h = 128, d_c = 512, d_h^R = 64, bf16).
+bool absorb_tc_supported(const Dims& d);
+cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, const int32_t* pos,
+                             int T, const void* w_uk, void* q_lat, cudaStream_t stream);
+cudaError_t launch_unabsorb_tc(const Dims& d, const void* o_lat, int T, const void* w_uv, float* o,
+                               cudaStream_t stream);
+
 // Generic CUDA-core decode: grid (H, n_q, B * S). With S > 1 it writes
 // normalised partials to the workspace and a combine kernel merges them.
 size_t simt_workspace_bytes(const Dims& d, int B, int n_q, int S);

@@ -25,6 +25,8 @@ SMALL_FP8 = W.small_v2(3, [129, 64, 70], n_q=2, cache="fp8", seed=12)
 SMALL_BF16_MTP = W.small_v2(3, [2, 100, 191], n_q=2, cache="bf16", seed=13)
 SMALL_BF16_LONG = W.small_v2(4, [700, 257, 1000, 64], n_q=1, cache="bf16", seed=14)
 SMALL_BF16_LONG_MTP = W.small_v2(3, [513, 256, 900], n_q=2, cache="bf16", seed=15)
+# 200 query rows: token tiles of the absorb kernels (128 / 64) with a ragged tail
+SMALL_BF16_T200 = W.small_v2(100, [3] * 100, n_q=2, cache="bf16", seed=16)
 TINY = W.config(1)
 TINY_PERM = W.config(1).with_(permute_pages=True)
 
@@ -75,9 +77,11 @@ def test_append_writes_each_token_to_its_slot(wl):
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_FP8], ids=lambda w: w.name)
-def test_absorb_q(wl):
-    case = Case(wl, prefill=False)
+@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_FP8, SMALL_BF16_LONG_MTP, SMALL_BF16_T200],
+                         ids=lambda w: w.name + f"-T{w.B * w.n_q}")
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_absorb_q(wl, kernel):
+    case = Case(wl, kernel=kernel, prefill=False)
     case.step.absorb(case.q_c, case.q_r)
     torch.cuda.synchronize()
     pos = np.concatenate([wl.positions(b) for b in range(wl.B)])
@@ -89,9 +93,10 @@ def test_absorb_q(wl):
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, SMALL_BF16], ids=lambda w: w.name)
-def test_unabsorb(wl):
-    case = Case(wl, prefill=False)
+@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_BF16_T200], ids=lambda w: w.name + f"-T{w.B * w.n_q}")
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_unabsorb(wl, kernel):
+    case = Case(wl, kernel=kernel, prefill=False)
     g = np.random.default_rng(5)
     o_lat = W.round_to_storage(g.standard_normal((wl.B * wl.n_q, wl.H, wl.C)).astype(np.float32) * 0.1, wl.act)
     case.step.o_lat.copy_(dev(o_lat, ACT[wl.act]))
