@@ -19,8 +19,9 @@
  *
  * Conventions for every call
  *   - All array pointers are DEVICE pointers, allocated and owned by the
- *     caller; the library keeps no device allocation and no state between
- *     calls. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *     caller. Apart from the fixed scratch array of mla_decode_noalloc (see
+ *     there) the library allocates no device memory and keeps no state
+ *     between calls. `stream` is a cudaStream_t (NULL = legacy default stream).
  *   - Arrays are dense, row-major, with the shapes given below; element
  *     types follow cfg->act_dtype / cfg->cache_dtype.
  *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code. Arguments are
@@ -55,6 +56,7 @@ extern "C" {
 #define MLA_ERR_WORKSPACE -3     /* workspace_bytes < mla_decode_workspace_size() */
 #define MLA_ERR_ALIGNMENT -4     /* a pointer misses the 16-byte alignment a kernel needs */
 #define MLA_ERR_CUDA -5          /* a CUDA runtime/driver call failed */
+#define MLA_ERR_SCRATCH_LIMIT -6 /* mla_decode_noalloc: the sizes need more than its fixed scratch */
 
 /* ---- device status bits (OR-ed into *dev_status) ----------------------- */
 #define MLA_DEV_INDEX_OUT_OF_RANGE 1  /* page id / sequence id / position outside its table */
@@ -131,7 +133,9 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
                  int32_t num_tokens, const void* w_uk, void* q_lat, void* stream);
 
 /*
- * Workspace bytes mla_decode needs for these sizes (0 when no split is needed).
+ * Workspace bytes mla_decode needs for these sizes (0 when the chosen kernel needs none:
+ * the CUDA-core kernel without splits). The tensor-core kernel always needs some (its CTA
+ * pairs exchange data through it).
  * num_splits as for mla_decode; max_seq_len bounds every seq_lens[b].
  */
 size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n_q,
@@ -176,6 +180,35 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
  */
 int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, const void* w_uv,
                  float* o, void* stream);
+
+/*
+ * mla_decode_noalloc — mla_decode for callers that cannot allocate device memory. The pages
+ * have no counterpart to this call; it is a convenience of this library.
+ *
+ * Who needs it: hosts that give the library only the tensors they own and no way to get more
+ * device memory (a serving framework's plugin interface whose memory pool is managed
+ * elsewhere), processes that must not have a library call cudaMalloc in the middle of a decode
+ * loop (it may block on the device or fail under memory pressure), and callers from runtimes
+ * that have no CUDA allocator binding.
+ *
+ * Arguments and results are those of mla_decode, without workspace / workspace_bytes: the
+ * scratch is a fixed MLA_NOALLOC_SCRATCH_BYTES array in the library's device image, which every
+ * GPU that loads the library holds until the process exits. The call allocates nothing.
+ *   - If mla_decode_workspace_size() for these sizes exceeds MLA_NOALLOC_SCRATCH_BYTES the call
+ *     returns MLA_ERR_SCRATCH_LIMIT and launches nothing.
+ *   - The first call on a device looks up the scratch's device address on that device (with
+ *     it current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents behind. Nothing in it
+ *     needs to start at zero (each call writes what it later reads), but calls whose work
+ *     overlaps on the GPU (different streams, or different host threads) race on it: keep them
+ *     ordered, for example on one stream.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, const void* kv_pool,
+                       const int32_t* block_table, int32_t max_pages_per_seq, int32_t num_pages,
+                       const int32_t* seq_lens, int32_t batch, int32_t n_q, int32_t max_seq_len,
+                       int32_t num_splits, void* o_lat, float* lse, int32_t* dev_status,
+                       void* stream);
 
 /* Human-readable text of a return code (static storage). */
 const char* mla_status_string(int code);

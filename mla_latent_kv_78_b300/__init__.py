@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401
     mla_config,
     mla_decode,
     mla_decode_kernel,
+    mla_decode_noalloc,
     mla_decode_workspace_size,
     mla_status_string,
     mla_unabsorb,

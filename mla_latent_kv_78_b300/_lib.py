@@ -23,6 +23,8 @@ MLA_ERR_UNSUPPORTED = -2
 MLA_ERR_WORKSPACE = -3
 MLA_ERR_ALIGNMENT = -4
 MLA_ERR_CUDA = -5
+MLA_ERR_SCRATCH_LIMIT = -6
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 MLA_DEV_INDEX_OUT_OF_RANGE = 1
 MLA_DEV_BAD_SEQLEN = 2
@@ -76,6 +78,8 @@ _SIGS = {
     "mla_decode": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _I, _I, _P, _I, _I, _I,
                                   _I, _P, ctypes.c_size_t, _P, _P, _P, _P]),
     "mla_unabsorb": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _I, _P, _P, _P]),
+    "mla_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _I, _I, _P, _I,
+                                          _I, _I, _I, _P, _P, _P, _P]),
     "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 EXPORTED = tuple(_SIGS)
@@ -163,6 +167,20 @@ def mla_decode(cfg: mla_config, q_lat, kv_pool, block_table, seq_lens, n_q: int,
         ctypes.byref(cfg), _ptr(q_lat), _ptr(kv_pool), _ptr(block_table), maxp, num_pages,
         _ptr(seq_lens), batch, n_q, max_seq_len, num_splits, _ptr(workspace), ws_bytes,
         _ptr(o_lat), _ptr(lse), _ptr(dev_status), _stream(stream)))
+
+
+def mla_decode_noalloc(cfg: mla_config, q_lat, kv_pool, block_table, seq_lens, n_q: int,
+                       max_seq_len: int, o_lat, lse=None, num_splits: int = 0,
+                       num_pages: Optional[int] = None, dev_status=None, stream=None) -> None:
+    """mla_decode with the library's fixed device scratch instead of a workspace argument
+    (for callers that cannot allocate device memory)."""
+    batch, maxp = block_table.shape
+    if num_pages is None:
+        num_pages = kv_pool.shape[0]
+    _check("mla_decode_noalloc", lib().mla_decode_noalloc(
+        ctypes.byref(cfg), _ptr(q_lat), _ptr(kv_pool), _ptr(block_table), maxp, num_pages,
+        _ptr(seq_lens), batch, n_q, max_seq_len, num_splits, _ptr(o_lat), _ptr(lse),
+        _ptr(dev_status), _stream(stream)))
 
 
 def mla_unabsorb(cfg: mla_config, o_lat, w_uv, o, stream=None) -> None:

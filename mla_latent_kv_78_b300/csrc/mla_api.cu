@@ -90,6 +90,7 @@ const char* mla_status_string(int code) {
     case MLA_ERR_WORKSPACE: return "workspace too small";
     case MLA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_SCRATCH_LIMIT: return "sizes exceed the fixed scratch of mla_decode_noalloc";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,69 @@
+"""mla_decode_noalloc: the decode for callers that cannot allocate device memory.
+
+It runs the same decode as mla_decode but takes its scratch from a fixed array inside the
+library instead of a caller-provided workspace. This file sorts last so that a run that stops
+at the first failure has already run every other test; it also passes on its own in a fresh
+process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_78_b300 as M
+import workloads as W
+from mla_latent_kv_78_b300 import _lib as L
+
+from _support import ACT, Case, assert_close, dev
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")
+
+
+def _both(wl, kernel, num_splits):
+    """Run mla_decode (torch workspace) and mla_decode_noalloc on the same inputs."""
+    case = Case(wl, kernel=kernel, num_splits=num_splits)
+    case.step.append(case.new_c, case.new_r)
+    q_lat = dev(wl.latent_queries().reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act])
+    st = case.step
+    st.decode(q_lat)
+    ref_o, ref_lse = st.o_lat.clone(), st.lse.clone()
+    o = torch.full_like(st.o_lat, float("nan"))
+    lse = torch.full_like(st.lse, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.mla_decode_noalloc(st.cfg, q_lat, st.pool, st.block_table, st.seq_lens, wl.n_q,
+                         st.max_seq_len, o, lse, num_splits=num_splits, num_pages=st.num_pages,
+                         dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and st.status() == 0
+    return ref_o, ref_lse, o, lse
+
+
+@needs_cuda
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_AUTO, M.MLA_KERNEL_SIMT], ids=["tc", "simt"])
+def test_noalloc_matches_decode_on_consecutive_calls(kernel):
+    # two calls in a row with different sizes and split counts: the second must not depend on
+    # what the first left in the shared scratch
+    calls = [
+        (W.small_v2(3, [700, 257, 64], n_q=1, cache="bf16", seed=21), 3),
+        (W.small_v2(2, [300, 1000], n_q=2, cache="bf16", seed=22), 0),
+    ]
+    for wl, splits in calls:
+        ref_o, ref_lse, o, lse = _both(wl, kernel, splits)
+        assert_close(wl, o.float().cpu().numpy(), ref_o.float().cpu().numpy(), "o_lat noalloc")
+        assert_close(wl, lse.cpu().numpy(), ref_lse.cpu().numpy(), "lse noalloc")
+
+
+@needs_cuda
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    wl = W.small_v2(2, [64, 64], n_q=1, cache="bf16", seed=23)
+    cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act)
+    batch = 2048   # the tensor-core exchange area alone then exceeds the fixed scratch
+    assert M.mla_decode_workspace_size(cfg, batch, 1, 4096) > L.NOALLOC_SCRATCH_BYTES
+    lib = M.lib()
+    rc = lib.mla_decode_noalloc(ctypes.byref(cfg), 16, 16, 16, 64, 64, 16, batch, 1, 4096, 0,
+                                16, None, None, None)
+    assert rc == L.MLA_ERR_SCRATCH_LIMIT
+    assert "scratch" in M.mla_status_string(rc)
