@@ -54,26 +54,25 @@ class Case:
                                  wl.num_pages, dev(self.w_uk_np, act), dev(self.w_uv_np, act),
                                  num_splits=num_splits)
         lat = ACT[wl.latent_storage]
-        if prefill:
-            # upload in chunks of whole sequences to bound host memory
-            buf_c, buf_r, buf_s, buf_p, n = [], [], [], [], 0
-            for b in range(wl.B):
-                c, r = wl.latents(b)
-                keep = wl.seq_lens[b] - wl.n_q
-                if keep > 0:
-                    buf_c.append(c[:keep]); buf_r.append(r[:keep])
-                    buf_s.append(np.full(keep, b, np.int32)); buf_p.append(np.arange(keep, dtype=np.int32))
-                    n += keep
-                if n >= chunk_tokens or (b == wl.B - 1 and n):
-                    self.step.prefill(dev(np.concatenate(buf_c), lat), dev(np.concatenate(buf_r), lat),
-                                      torch.from_numpy(np.concatenate(buf_s)).cuda(),
-                                      torch.from_numpy(np.concatenate(buf_p)).cuda())
-                    buf_c, buf_r, buf_s, buf_p, n = [], [], [], [], 0
-        # this step's inputs, t = b * n_q + j
+        # this step's inputs, t = b * n_q + j, collected while the cache is filled
         new_c, new_r = [], []
+        buf_c, buf_r, buf_s, buf_p, n = [], [], [], [], 0
         for b in range(wl.B):
             c, r = wl.latents(b)
             new_c.append(c[-wl.n_q:]); new_r.append(r[-wl.n_q:])
+            if not prefill:
+                continue
+            keep = wl.seq_lens[b] - wl.n_q
+            if keep > 0:
+                buf_c.append(c[:keep]); buf_r.append(r[:keep])
+                buf_s.append(np.full(keep, b, np.int32)); buf_p.append(np.arange(keep, dtype=np.int32))
+                n += keep
+            # upload in chunks of whole sequences to bound host memory
+            if n >= chunk_tokens or (b == wl.B - 1 and n):
+                self.step.prefill(dev(np.concatenate(buf_c), lat), dev(np.concatenate(buf_r), lat),
+                                  torch.from_numpy(np.concatenate(buf_s)).cuda(),
+                                  torch.from_numpy(np.concatenate(buf_p)).cuda())
+                buf_c, buf_r, buf_s, buf_p, n = [], [], [], [], 0
         self.new_c = dev(np.concatenate(new_c), lat)
         self.new_r = dev(np.concatenate(new_r), lat)
         q_c, q_r = wl.queries()
