@@ -106,7 +106,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _cpu_oracle_sample(wl, budget_s: float = 12.0, max_heads: int = 128):
+def _cpu_oracle_sample(wl, budget_s: float = 12.0, max_heads: int = 1 << 30):
     """Time the fp64 oracle (as it stands) on whole heads of sequence 0, then 1, ...
     until about budget_s of CPU work. Returns (GB/s equivalent, sample description, threads)."""
     from oracle import mla_oracle as O
@@ -135,10 +135,37 @@ def _cpu_oracle_sample(wl, budget_s: float = 12.0, max_heads: int = 128):
         if t_total >= budget_s or heads_done >= max_heads:
             break
     threads = _blas_threads()
-    sample = (f"fp64 oracle (explicit k^C/v^C decompression per head) on {heads_done} of "
-              f"{wl.H} heads across {seqs} sequence(s) of L={wl.seq_lens[0]}; bytes credited = "
-              f"L * {bytes_per_tok} B * heads/{wl.H} per sequence")
+    sample = (f"fp64 oracle (explicit k^C/v^C decompression per head) on the first {seqs} "
+              f"sequence(s) of L={wl.seq_lens[0]} ({heads_done} (sequence, head) pairs of "
+              f"{wl.B * wl.H}); bytes credited = L * {bytes_per_tok} B * heads/{wl.H} per sequence")
     return done_bytes / t_total / 1e9, sample, threads, t_total
+
+
+def reduce_max_over_ranks(xs, device):
+    """Element-wise max of xs over all ranks (the slowest rank's times); identity when the
+    process group is absent or has one rank."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(list(xs), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_gbs(world: int, bytes_per_step: float, steps: int, total_ms: float) -> float:
+    """Latent-cache GB/s of the whole job: every rank's replica moved bytes_per_step per step,
+    and the job took the slowest rank's total_ms."""
+    return world * bytes_per_step * steps / (total_ms * 1e-3) / 1e9
+
+
+def _combine_launches(M, cfg, wl, splits) -> int:
+    """1 if mla_decode runs a split-KV combine kernel for this workload, else 0."""
+    if M.mla_decode_kernel(cfg, wl.B, wl.n_q) == M.MLA_KERNEL_TC:
+        # the tensor-core kernel's workspace holds partials only when it splits
+        base = M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, wl.max_seq_len, 1)
+        return int(M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, wl.max_seq_len, splits) > base)
+    return int(M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, wl.max_seq_len, splits) > 0)
 
 
 def _blas_threads() -> int:
@@ -226,19 +253,14 @@ def run_ours(args, world, rank, local_rank):
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
-    splits_used = M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, wl.max_seq_len, args.splits) > 0
-    launches_per_step = 4 + (1 if splits_used else 0)
+    launches_per_step = 4 + _combine_launches(M, cfg, wl, args.splits)
 
-    def one_step():
-        step.step(inputs_dev["c"], inputs_dev["r"], inputs_dev["qc"], inputs_dev["qr"])
-
+    # the step as one CUDA graph (events around the step and around mla_decode inside it)
+    step.capture(inputs_dev["c"], inputs_dev["r"], inputs_dev["qc"], inputs_dev["qr"], timing=True)
     for _ in range(args.warmup):
-        one_step()
+        step.replay()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -246,27 +268,23 @@ def run_ours(args, world, rank, local_rank):
     clocks.start()
     time.sleep(0.25)
     t_wall0 = time.perf_counter()
+    step_ms, dec_ms = [], []
     for k in range(args.steps):
+        # L2 flush between timed steps (a 2 x L2 write), outside the step's events
         flush.fill_(float(k))
-        s0, d0, d1, s1 = ev[k]
-        s0.record(stream)
-        step.append(inputs_dev["c"], inputs_dev["r"])
-        step.absorb(inputs_dev["qc"], inputs_dev["qr"])
-        d0.record(stream)
-        step.decode()
-        d1.record(stream)
-        step.unabsorb()
-        s1.record(stream)
-    torch.cuda.synchronize()
+        step.replay()
+        torch.cuda.synchronize()
+        step_ms.append(step.step_ms())
+        dec_ms.append(step.decode_ms())
     wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
+    torch.cuda.synchronize()
     clk = clocks.stop()
-    step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
-    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     assert step.status() == 0, f"device status {step.status()} after timed steps"
 
-    # end to end through the public API, host buffers in and out
+    # end to end through the public API: pinned host inputs copied in, the step's graph,
+    # o copied back, all inside the timed region
     e2e_ms = []
     h2d = sum(t.numel() * t.element_size() for t in inputs_host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -276,7 +294,7 @@ def run_ours(args, world, rank, local_rank):
         a.record(stream)
         for key, t in inputs_host.items():
             inputs_dev[key].copy_(t, non_blocking=True)
-        one_step()
+        step.replay()
         out_host.copy_(step.o, non_blocking=True)
         b_.record(stream)
         b_.synchronize()
@@ -284,15 +302,10 @@ def run_ours(args, world, rank, local_rank):
             e2e_ms.append(a.elapsed_time(b_))
 
     cache_bytes, qo_bytes, flops = _workload_sizes(wl)
-    total_ms = sum(step_ms)
-    total_e2e = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, total_e2e = float(t[0]), float(t[1])
+    total_ms, total_e2e = reduce_max_over_ranks([sum(step_ms), sum(e2e_ms)], dev)
     ms_per_step = total_ms / args.steps
-    value = world * cache_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    e2e_value = world * cache_bytes * args.steps / (total_e2e * 1e-3) / 1e9
+    value = whole_job_gbs(world, cache_bytes, args.steps, total_ms)
+    e2e_value = whole_job_gbs(world, cache_bytes, args.steps, total_e2e)
     peaks = _peaks()
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = cache_bytes + qo_bytes
@@ -320,6 +333,7 @@ def run_ours(args, world, rank, local_rank):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": total_e2e / args.steps},
         "gpu_launches": launches_per_step * args.steps,
+        "launch": "one CUDA graph per step (append, absorb_q, decode, unabsorb)",
         "clocks": clk,
         "wall_s_timed": wall,
     }
@@ -335,8 +349,8 @@ def run_ours(args, world, rank, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 SIMT, 2 tensor-core decode")
     ap.add_argument("--splits", type=int, default=0)

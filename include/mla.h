@@ -62,6 +62,11 @@ extern "C" {
 #define MLA_DEV_INDEX_OUT_OF_RANGE 1  /* page id / sequence id / position outside its table */
 #define MLA_DEV_BAD_SEQLEN 2          /* seq_lens[b] < n_q or > max_seq_len */
 #define MLA_DEV_TIMEOUT 4             /* a bounded barrier wait gave up; outputs invalid */
+#define MLA_DEV_SCORE_RANGE 8         /* tensor-core decode: a scaled score exceeded the
+                                         running maximum of its head (over the tiles two or
+                                         more before its own) by more than 66.5, a weight
+                                         ratio above 2^96; those weights were clamped and the
+                                         row's output is approximate */
 
 /* ---- element types ----------------------------------------------------- */
 #define MLA_F32 0

@@ -48,25 +48,33 @@ constexpr int kThreads = 384;
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
 constexpr uint32_t kPageBytes = kP * kCR * 2;   // 73,728 B: one page is contiguous in the pool
 constexpr int kPrefetch = 0;         // 1: prefetch the next tile's pages into L2 (measured slower)
+constexpr int kXSlots = 4;                      // exchange slots per CTA: tile t uses t % 4
 constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
-constexpr uint32_t kXBytes = kXPBytes + kH * 4;  // + that tile's per-head maxima
-constexpr size_t kXUnitBytes = 4 * (size_t)kXBytes + 2 * kH * 4;  // per (seq, row, split)
+constexpr uint32_t kXHdrBytes = 16;             // flag word (1: the tile's maxima follow) + pad
+constexpr uint32_t kXBytes = kXPBytes + kXHdrBytes + kH * 4;   // + that tile's per-head maxima
+constexpr size_t kXUnitBytes = 2 * kXSlots * (size_t)kXBytes + 2 * kH * 4;  // per (seq, row, split)
+constexpr float kLazy = 8.f;    // log2 units a score may exceed the reference before it moves
+constexpr float kRange = 96.f;  // larger excesses are clamped and flagged (MLA_DEV_SCORE_RANGE)
 
 constexpr int OFF_Q = 0;                           // 9 x [64 heads x 64 dims]  (8 KB each)
 constexpr int OFF_S = OFF_Q + kKCh * 8192;         // kNS x 16 KB
 constexpr int OFF_V = OFF_S + kNS * 16384;         // kNV x 16 KB
 constexpr int OFF_P = OFF_V + kNV * 16384;         // 2 x [256 tok x 64 heads] = 2 x 32 KB
 constexpr int OFF_F = OFF_P + 2 * 32768;           // fp32 scratch
+constexpr int kRcvFloats = (int)(kXBytes - kXPBytes) / 4;   // 132: flag word, pad, 128 maxima
 constexpr int F_COL = 0;       // [8 warps][64]   column max / column sum partials
-constexpr int F_CMLOC = 512;   // [2][128] this CTA's per-head tile maxima
-constexpr int F_CMRCV = 768;   // [4][128] the peer's per-head tile maxima
-constexpr int F_M = 1280;      // [128] reference max (log2 units), identical in both CTAs
-constexpr int F_ALPHA = 1408;  // [128]
-constexpr int F_LLOC = 1536;   // [128]
-constexpr int F_LRCV = 1664;   // [128]
-constexpr int F_INV = 1792;    // [128]
-constexpr int F_FLAG = 1920;   // ints: [0] rescale, [1] abort
-constexpr int F_END = 1928;
+constexpr int F_CMLOC = 512;   // [2][128] this CTA's published per-head tile maxima
+constexpr int F_RCV = 768;     // [4][132] the peer's flag word + per-head tile maxima, by slot
+constexpr int F_M = F_RCV + kXSlots * kRcvFloats;   // [128] reference (log2 units), same in both CTAs
+constexpr int F_ALPHA = F_M + 128;   // [128]
+constexpr int F_LLOC = F_ALPHA + 128;  // [128]
+constexpr int F_LRCV = F_LLOC + 128;   // [128]
+constexpr int F_INV = F_LRCV + 128;    // [128]
+constexpr int F_FLAG = F_INV + 128;    // ints, see FL_*
+constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for this tile
+constexpr int FL_ABORT = 2;    // a bounded wait gave up
+constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
+constexpr int F_END = F_FLAG + 6;
 constexpr int OFF_BAR = OFF_F + F_END * 4;
 
 struct Bars {
@@ -96,6 +104,9 @@ struct Params {
   float* ws_lse;
   uint8_t* xws;          // exchange area, kXUnitBytes per unit
   int32_t* status;
+#ifdef MLA_TC_TRACE
+  unsigned long long* trace;
+#endif
 };
 
 struct Ctx {
@@ -105,18 +116,35 @@ struct Ctx {
 
 #ifdef MLA_TC_TRACE
 // Debug builds only: per-event %globaltimer stamps for the first kTraceUnits units.
-constexpr int kTraceUnits = 4, kTraceEvents = 16, kTraceTiles = 64;
-__device__ unsigned long long* g_tc_trace;
-__device__ __forceinline__ void trace(int unit, uint32_t rank, int ev, int t) {
-  if (g_tc_trace && unit < kTraceUnits && t < kTraceTiles) {
+constexpr int kTraceUnits = 2, kTraceEvents = 24, kTraceTiles = 1024;
+static void* g_tc_trace_host = nullptr;
+__device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_t rank, int ev,
+                                      int t) {
+  if (buf && unit < kTraceUnits && t < kTraceTiles) {
     unsigned long long ns;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
-    g_tc_trace[(((size_t)unit * 2 + rank) * kTraceEvents + ev) * kTraceTiles + t] = ns;
+    buf[(((size_t)unit * 2 + rank) * kTraceEvents + ev) * kTraceTiles + t] = ns;
   }
 }
-#define TRACE(ev, t) trace(unit, rank, ev, t)
+#define TRACE(ev, t) trace(prm.trace, unit, rank, ev, t)
+// cycle totals of one thread's activities (slot < 8), stored at the end of event row 15
+#define PROF(slot, stmt)                    \
+  do {                                      \
+    const long long p0_ = clock64();        \
+    stmt;                                   \
+    prof[slot] += clock64() - p0_;          \
+  } while (0)
+#define PROF_STORE()                                                                          \
+  do {                                                                                      \
+    if (prm.trace && unit < kTraceUnits)                                                    \
+      for (int q = 0; q < 8; ++q)                                                           \
+        prm.trace[(((size_t)unit * 2 + rank) * kTraceEvents + 15) * kTraceTiles + 512 + q] = \
+            (unsigned long long)prof[q];                                                    \
+  } while (0)
 #else
 #define TRACE(ev, t) ((void)0)
+#define PROF(slot, stmt) stmt
+#define PROF_STORE() ((void)0)
 #endif
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
@@ -203,11 +231,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // exchange area of this unit: [rank][parity] {P^T 16 KB, maxima 512 B}, then [rank] tile-0 maxima
+  // exchange area of this unit: [rank][slot] {P^T 16 KB, flag word, maxima 512 B}, then [rank]
+  // tile-0 maxima
   uint8_t* xunit = prm.xws + (size_t)unit * kXUnitBytes;
-  auto x_slot = [&](uint32_t r, int par) { return xunit + (size_t)(r * 2 + par) * kXBytes; };
-  float* x0_mine = reinterpret_cast<float*>(xunit + 4 * (size_t)kXBytes + rank * kH * 4);
-  const float* x0_peer = reinterpret_cast<const float*>(xunit + 4 * (size_t)kXBytes + peer * kH * 4);
+  auto x_slot = [&](uint32_t r, int slot) {
+    return xunit + (size_t)(r * kXSlots + slot) * kXBytes;
+  };
+  float* x0_mine = reinterpret_cast<float*>(xunit + 2 * kXSlots * (size_t)kXBytes + rank * kH * 4);
+  const float* x0_peer =
+      reinterpret_cast<const float*>(xunit + 2 * kXSlots * (size_t)kXBytes + peer * kH * 4);
 
   // ---- set-up
   if (tid == 0) TRACE(11, 0);
@@ -238,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbarrier_init_cluster();
   }
   if (tid < kH) fs[F_M + tid] = -CUDART_INF_F;
-  if (tid < 2) flags[tid] = 0;
+  if (tid < F_END - F_FLAG) flags[tid] = 0;
   if (warp == 1) {
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
@@ -247,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  Ctx cx{reinterpret_cast<volatile int*>(&flags[1]), prm.status};
+  Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status};
 
   auto page_y = [&](int idx_in_unit) -> int {
     const int pidx = lo / kP + idx_in_unit;
@@ -283,6 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t bar = at_even(&bars->s_ready[st]);
         tma_load_2d_pair(sm + OFF_S + st * 16384, &tmK, c * 64, y0, bar, pol_s);
         tma_load_2d_pair(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, bar, pol_s);
+        TRACE(16, s_cnt);
         ++s_cnt;
         return true;
       };
@@ -321,33 +354,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t sQ = smem_u32(sm + OFF_Q), sS = smem_u32(sm + OFF_S);
       const uint32_t sV = smem_u32(sm + OFF_V), sP = smem_u32(sm + OFF_P);
       int s_cnt = 0, v_cnt = 0;
+#ifdef MLA_TC_TRACE
+      long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      const long long prof_start = clock64();
+#endif
       auto mma_s_chunk = [&](int t, int c) -> bool {
         const int st = s_cnt % kNS;
-        if (!wait_bar(&bars->s_ready[st], (s_cnt / kNS) & 1, cx)) return false;
+        TRACE(17, s_cnt);
+        bool r;
+        PROF(0, r = wait_bar(&bars->s_ready[st], (s_cnt / kNS) & 1, cx));
+        if (!r) return false;
+        TRACE(18, s_cnt);
         tc_fence_after();
+        PROF(1, {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
-          mma_bf16_pair(tmem + (t & 1) * 128, a, bd, idS, (c | k) != 0);
-        }
-        mma_commit_pair(&bars->s_free[st], 0x3);
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
+            const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
+            mma_bf16_pair(tmem + (t & 1) * 128, a, bd, idS, (c | k) != 0);
+          }
+        });
+        PROF(2, mma_commit_pair(&bars->s_free[st], 0x3));
         ++s_cnt;
         return true;
       };
       auto mma_v_chunk = [&](int t, int v) -> bool {
         const int st = v_cnt % kNV;
-        if (!wait_bar(&bars->v_ready[st], (v_cnt / kNV) & 1, cx)) return false;
+        TRACE(20, v_cnt);
+        bool r;
+        PROF(3, r = wait_bar(&bars->v_ready[st], (v_cnt / kNV) & 1, cx));
+        if (!r) return false;
+        TRACE(21, v_cnt);
         tc_fence_after();
+        PROF(4, {
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
+          for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint64_t a = smem_desc(sV + st * 16384 + blk * 8192 + k * 2048, 4096, 1024, kSw128);
-            const uint64_t bd = smem_desc(sP + (t & 1) * 32768 + v * 4096 + k * 2048, 8192, 1024, kSw128);
-            mma_bf16_pair(tmem + 256 + blk * 128, a, bd, idPV, (t | v | k) != 0);
-          }
-        mma_commit_pair(&bars->v_free[st], 0x3);
+            for (int k = 0; k < 2; ++k) {
+              const uint64_t a = smem_desc(sV + st * 16384 + blk * 8192 + k * 2048, 4096, 1024, kSw128);
+              const uint64_t bd = smem_desc(sP + (t & 1) * 32768 + v * 4096 + k * 2048, 8192, 1024, kSw128);
+              mma_bf16_pair(tmem + 256 + blk * 128, a, bd, idPV, (t | v | k) != 0);
+            }
+        });
+        PROF(5, mma_commit_pair(&bars->v_free[st], 0x3));
         ++v_cnt;
         return true;
       };
@@ -355,13 +404,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // step k: S^T(k) interleaved chunk for chunk with PV(k-2)
       for (int k = 0; k < nt + 2 && ok; ++k) {
         const bool do_s = k < nt, do_v = k >= 2;
-        if (do_s && k >= 2) ok = wait_bar(&bars->s_empty[k & 1], ((k >> 1) - 1) & 1, cx);
+        if (do_s) TRACE(22, k);
+        if (do_s && k >= 2) PROF(6, ok = wait_bar(&bars->s_empty[k & 1], ((k >> 1) - 1) & 1, cx));
         if (do_s && ok) TRACE(9, k);
         for (int c = 0; c < kKCh && ok; ++c) {
           if (do_s) ok = mma_s_chunk(k, c);
           if (do_s && c == 4) TRACE(13, k);
           if (ok && do_v && c == 0) {
-            ok = wait_bar(&bars->p_ready[k & 1], ((k - 2) >> 1) & 1, cx);
+            TRACE(23, k - 2);
+            PROF(6, ok = wait_bar(&bars->p_ready[k & 1], ((k - 2) >> 1) & 1, cx));
             TRACE(1, k - 2);
             tc_fence_after();
           }
@@ -377,6 +428,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           TRACE(2, k - 2);
         }
       }
+#ifdef MLA_TC_TRACE
+      prof[7] = clock64() - prof_start;
+      PROF_STORE();
+#endif
       // every MMA this thread issued (they write both CTAs' TMEM) completes before teardown
       mma_commit_pair(&bars->teardown, 0x1);
       wait_drain(&bars->teardown, 0);
@@ -438,6 +493,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int q4 = 0; q4 < 4; ++q4)
               tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
                                (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
+            TRACE(19, v_cnt);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -447,17 +503,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 3) {
     // ================================================================ exchange
-    // Fetches the peer's P^T half and tile maxima once the peer has put them in global
-    // memory; reports this CTA's P^T buffer complete to the even CTA.
+    // Fetches the peer's P^T half, flag word and tile maxima once the peer has put them in
+    // global memory, into this CTA's P^T buffer of that tile's parity (after PV of the tile
+    // two back has finished reading it); reports the buffer complete to the even CTA.
     if (lane == 0) {
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
-        const int par = t & 1;
+        const int par = t & 1, slot = t & (kXSlots - 1);
         ok = wait_bar(&bars->x_ready[par], (t >> 1) & 1, cx);
+        if (ok && t >= 2) ok = wait_bar(&bars->o_done[par], ((t - 2) >> 1) & 1, cx);
         if (!ok) break;
-        const uint8_t* src = x_slot(peer, par);
+        TRACE(8, t);
+        const uint8_t* src = x_slot(peer, slot);
         bulk_g2s(sm + OFF_P + par * 32768 + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
-        bulk_g2s(fs + F_CMRCV + (t & 3) * kH, src + kXPBytes, kH * 4, &bars->p_landed[par]);
+        bulk_g2s(fs + F_RCV + slot * kRcvFloats, src + kXPBytes, kXBytes - kXPBytes,
+                 &bars->p_landed[par]);
         ok = wait_bar(&bars->p_landed[par], (t >> 1) & 1, cx);
         TRACE(7, t);
         if (ok) arrive_even(&bars->p_ready[par], rank);
@@ -465,25 +525,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ================================================================ softmax / epilogue
+    // Thread = one TMEM lane: token i of this CTA's half tile for the scores, latent row i for
+    // the output. Each thread handles one head group (64 heads) of its token.
+    //
+    // Online softmax with a lazy reference (log2 units) M[h], identical in both CTAs: tile 0
+    // sets it from both CTAs' maxima; afterwards a tile whose scores exceed M by more than
+    // kLazy publishes its per-head maxima, and two tiles later both CTAs move M (and rescale
+    // O and the running sums) from the same published data. Tiles in between use the old
+    // reference, so their weights may exceed 1 (up to 2^kRange, which fp32 sums and bf16 P
+    // hold without loss); the common tile needs no cross-thread reduction at all.
     const int sw = warp - 4;           // 0..7
     const int g = sw >> 2;             // head group: heads [64g, 64g + 64)
     const int qd = warp & 3;           // TMEM lane quadrant
     const int i = qd * 32 + lane;      // this CTA's token row (S^T) / latent row (O^T)
     const int stid = tid - 128;        // 0..255
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const float* Mg = fs + F_M + 64 * g;
     float l_acc[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) l_acc[c] = 0.f;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
-      const int par = t & 1;
-      ok = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
-      ok = bar_and(1, 256, ok);
-      if (!ok) break;
-      if (stid == 0) {
-        flags[0] = 0;
-        TRACE(3, t);
+      const int par = t & 1, slot = t & (kXSlots - 1);
+      // ---- reference for tile t, from tile t-2's published maxima (both CTAs)
+      bool ok1 = true;
+      if (t >= 2 && stid < kH) {
+        const int h = stid;
+        ok1 = wait_bar(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
+        const float* rcv = fs + F_RCV + ((t - 2) & (kXSlots - 1)) * kRcvFloats;
+        float cand = -CUDART_INF_F;
+        if (flags[FL_PUB + par]) cand = fs[F_CMLOC + par * kH + h];
+        if (__float_as_uint(rcv[0]) != 0u) cand = fmaxf(cand, rcv[4 + h]);
+        const float mo = fs[F_M + h];
+        float alpha = 1.f;
+        if (cand > mo + kLazy) {
+          alpha = ex2(mo - cand);
+          fs[F_M + h] = cand;
+          flags[FL_RESCALE + par] = 1;
+        }
+        fs[F_ALPHA + h] = alpha;
       }
+      if (ok1) ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
+      ok = bar_and(1, 256, ok1);
+      if (!ok) break;
+      if (stid == 0) TRACE(3, t);
+      const bool rescale = flags[FL_RESCALE + par] != 0;
       tc_fence_after();
       float s[64];
       tmem_ld32(lane_addr + par * 128 + 64 * g, s);
@@ -492,82 +578,124 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) arrive_even(&bars->s_empty[par], rank);
+      if (stid == 0) TRACE(12, t);
       const int tok = lo + t * kTile + (int)rank * 128 + i;
       const bool valid = tok < hi;
 #pragma unroll
       for (int c = 0; c < 64; ++c) s[c] = valid ? s[c] * prm.scale_log2 : -CUDART_INF_F;
-      // per-head maximum over this warp's 32 tokens
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float mx = warp_max_f32(s[c]);
-        if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
-      }
-      bar_and(2, 256, true);
-      // this CTA's maximum of tile t; the reference for tile t combines both CTAs'
-      // maxima of tile t-2 (tiles 0 and 1 use tile 0's, agreed before any P is made)
-      float my_max = 0.f;
-      bool ok2 = true;
-      if (stid < kH) {
-        const int h = stid, gg = h >> 6, cc = h & 63;
-        my_max = fs[F_COL + (gg * 4) * 64 + cc];
-#pragma unroll
-        for (int q = 1; q < 4; ++q) my_max = fmaxf(my_max, fs[F_COL + (gg * 4 + q) * 64 + cc]);
-      }
       if (t == 0) {
-        if (stid < kH) x0_mine[stid] = my_max;
-        __threadfence();
-        bar_and(6, 256, true);
+        // ---- the first reference: per-head maxima over both CTAs' tokens of tile 0
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float mx = warp_max_f32(s[c]);
+          if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
+        }
+        bar_sync(2, 256);
+        float my_max = -CUDART_INF_F;
+        if (stid < kH) {
+          const int h = stid, gg = h >> 6, cc = h & 63;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) my_max = fmaxf(my_max, fs[F_COL + (gg * 4 + q) * 64 + cc]);
+          x0_mine[h] = my_max;
+          __threadfence();
+        }
+        bar_sync(3, 256);
         if (stid == 0) mbar_arrive_remote(mapa(smem_u32(&bars->x0_ready), peer));
+        bool okx = true;
         if (stid < kH) {
           const int h = stid;
-          ok2 = wait_bar(&bars->x0_ready, 0, cx);
-          const float other = __ldcg(x0_peer + h);
-          fs[F_M + h] = fmaxf(my_max, other);
+          okx = wait_bar(&bars->x0_ready, 0, cx);
+          fs[F_M + h] = fmaxf(my_max, __ldcg(x0_peer + h));
           fs[F_ALPHA + h] = 1.f;
-          fs[F_CMLOC + h] = my_max;
         }
-      } else if (stid < kH) {
-        const int h = stid;
-        float alpha = 1.f;
-        if (t >= 2) {
-          // tile t-2's maxima: this CTA's from shared memory, the peer's from its payload
-          ok2 = wait_bar(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
-          const float cand = fmaxf(fs[F_CMLOC + par * kH + h], fs[F_CMRCV + ((t - 2) & 3) * kH + h]);
-          const float mo = fs[F_M + h];
-          if (cand > mo + 8.f) {
-            alpha = ex2(mo - cand);
-            fs[F_M + h] = cand;
-            flags[0] = 1;
-          }
-        }
-        fs[F_ALPHA + h] = alpha;
-        fs[F_CMLOC + par * kH + h] = my_max;
+        ok = bar_and(4, 256, okx);
+        if (!ok) break;
       }
-      ok = bar_and(3, 256, ok2);
-      if (!ok) break;
       if (stid == 0) TRACE(4, t);
-      const bool any_rescale = flags[0] != 0;
+      // ---- weights p = 2^(s - M) in bf16, with the overshoot checks
       uint32_t pk[32];
+      bool over = false, extreme = false;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = ex2(s[c] - fs[F_M + 64 * g + c]);
-        const float p1 = ex2(s[c + 1] - fs[F_M + 64 * g + c + 1]);
-        const uint32_t w2 = pack_bf16x2(p0, p1);
-        pk[c >> 1] = w2;
-        l_acc[c] = fmaf(l_acc[c], fs[F_ALPHA + 64 * g + c], __uint_as_float(w2 << 16));
-        l_acc[c + 1] = fmaf(l_acc[c + 1], fs[F_ALPHA + 64 * g + c + 1], __uint_as_float(w2 & 0xFFFF0000u));
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(Mg + 4 * c4);
+        const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float d = s[4 * c4 + e] - m[e];
+          over |= d > kLazy;
+          extreme |= d > kRange;
+          d = fminf(d, kRange);
+          p[e] = ex2(d);
+        }
+        pk[2 * c4] = pack_bf16x2(p[0], p[1]);
+        pk[2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
+      }
+      if (extreme) flag_status(prm.status, MLA_DEV_SCORE_RANGE);
+      if (rescale) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) l_acc[c] *= fs[F_ALPHA + 64 * g + c];
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        l_acc[2 * c] += __uint_as_float(pk[c] << 16);
+        l_acc[2 * c + 1] += __uint_as_float(pk[c] & 0xFFFF0000u);
+      }
+      if (stid == 0) TRACE(14, t);
+      // ---- the peer's head half of P^T goes out first (same swizzled bytes as in shared
+      // memory); the slot was last read four tiles ago
+      const uint32_t sw_off = (uint32_t)((i & 7) * 16);
+      if (g != (int)rank) {
+        uint8_t* dst = x_slot(rank, slot) + i * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_proxy_async_global();
       }
       // O must be stable to rescale (PV(t-1) done); otherwise only P's buffer must be free (PV(t-2))
       bool ok3 = true;
-      if (any_rescale && t >= 1)
+      if (rescale)
         ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
       else if (t >= 2)
         ok3 = wait_bar(&bars->o_done[par], ((t - 2) >> 1) & 1, cx);
-      ok = bar_and(4, 256, ok3);
-      if (!ok) break;
-      if (stid == 0) TRACE(5, t);
+      bool any_over = false;
+      if (bar_or(5, 256, over || !ok3)) {
+        ok = bar_and(6, 256, ok3);
+        if (!ok) break;
+        any_over = true;
+        // ---- this tile's per-head maxima, published for the reference two tiles on: the
+        // largest weight of each head (all relative to the same M) gives max s = M + log2(p)
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const uint32_t w = pk[c >> 1];
+          const float pv = __uint_as_float((c & 1) ? (w & 0xFFFF0000u) : (w << 16));
+          const float mx = warp_max_f32(pv);
+          if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
+        }
+        bar_sync(2, 256);
+        if (stid < kH) {
+          const int h = stid, gg = h >> 6, cc = h & 63;
+          float pmax = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) pmax = fmaxf(pmax, fs[F_COL + (gg * 4 + q) * 64 + cc]);
+          const float my_max = pmax > 0.f ? fs[F_M + h] + log2f(pmax) : -CUDART_INF_F;
+          fs[F_CMLOC + par * kH + h] = my_max;
+          reinterpret_cast<float*>(x_slot(rank, slot) + kXPBytes + kXHdrBytes)[h] = my_max;
+          fence_proxy_async_global();
+        }
+        bar_sync(3, 256);
+      }
+      if (stid == 0) {
+        flags[FL_PUB + par] = any_over ? 1 : 0;
+        flags[FL_RESCALE + par] = 0;   // every thread has read it (barrier 5)
+        *reinterpret_cast<uint32_t*>(x_slot(rank, slot) + kXPBytes) = any_over ? 1u : 0u;
+        fence_proxy_async_global();
+        mbar_arrive_remote(mapa(smem_u32(&bars->x_ready[par]), peer));
+        TRACE(5, t);
+      }
       tc_fence_after();
-      if (any_rescale && t >= 1) {
+      if (rescale) {
 #pragma unroll 1
         for (int blk = 0; blk < 2; ++blk)
 #pragma unroll 1
@@ -582,29 +710,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         tmem_st_wait();
       }
-      // P^T row k of the tile, heads [64g, 64g+64): kept here if they are this CTA's heads,
-      // else written to global memory for the peer (same swizzled bytes either way)
-      const int k = (int)rank * 128 + i;
-      const uint32_t sw_off = (uint32_t)(((k & 7)) * 16);
+      // ---- this CTA's own head half of P^T, rows of its tokens
       if (g == (int)rank) {
+        const int k = (int)rank * 128 + i;
         uint8_t* dst = sm + OFF_P + par * 32768 + k * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_smem();
-      } else {
-        uint8_t* dst = x_slot(rank, par) + i * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       }
-      if (stid < kH) reinterpret_cast<float*>(x_slot(rank, par) + kXPBytes)[stid] = my_max;
-      fence_proxy_async_global();
       tc_fence_before();
-      bar_and(5, 256, true);
-      if (stid == 0) mbar_arrive_remote(mapa(smem_u32(&bars->x_ready[par]), peer));
       __syncwarp();
       if (lane == 0) {
         if (sw == 0) {
@@ -796,6 +912,9 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.ws_lse = S > 1 ? static_cast<float*>(ws) + rows * S * d.C : nullptr;
   prm.xws = static_cast<uint8_t*>(ws) + part;
   prm.status = status;
+#ifdef MLA_TC_TRACE
+  prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);
+#endif
   const unsigned grid = 2u * (unsigned)(B * n_q * S);
   tc::decode_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tmQ, tmK, tmV, prm);
   cudaError_t e = cudaGetLastError();
@@ -807,6 +926,7 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
 
 #ifdef MLA_TC_TRACE
 extern "C" int mla_debug_set_tc_trace(void* p) {
-  return cudaMemcpyToSymbol(mla::tc::g_tc_trace, &p, sizeof(p)) == cudaSuccess ? 0 : -1;
+  mla::tc::g_tc_trace_host = p;
+  return 0;
 }
 #endif

@@ -22,6 +22,9 @@ class DecodeStep:
     tensors. All tensors are allocated on ``device``.
     """
 
+    _graph = None
+    _graph_events = None
+
     def __init__(self, cfg: L.mla_config, block_table: torch.Tensor, seq_lens: Sequence[int],
                  n_q: int, num_pages: int, w_uk: torch.Tensor, w_uv: torch.Tensor,
                  num_splits: int = 0, device: str = "cuda"):
@@ -88,6 +91,56 @@ class DecodeStep:
         self.decode(None, stream)
         self.unabsorb(stream)
         return self.o
+
+    # -- the step as one CUDA graph ----------------------------------------
+    def capture(self, c_kv_new, k_r_new, q_c, q_r, timing: bool = False) -> None:
+        """Record append -> absorb -> decode -> unabsorb over these input tensors as one CUDA
+        graph, so a step costs one graph launch instead of four host-side library calls.
+
+        The graph keeps the inputs' device addresses: write each step's inputs into the same
+        tensors (copy_) before replay(). One eager step runs first, outside the capture, so
+        the library's one-time per-process set-up never happens inside it. With timing=True
+        the graph also records events around the whole step and around mla_decode; read them
+        with step_ms() / decode_ms() after the replay has finished.
+        """
+        dev = self.device
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self.step(c_kv_new, k_r_new, q_c, q_r)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        ev = ([torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+              if timing else None)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            if ev:
+                ev[0].record()
+            self.append(c_kv_new, k_r_new)
+            self.absorb(q_c, q_r)
+            if ev:
+                ev[1].record()
+            self.decode()
+            if ev:
+                ev[2].record()
+            self.unabsorb()
+            if ev:
+                ev[3].record()
+        self._graph = graph
+        self._graph_events = ev
+
+    def replay(self) -> torch.Tensor:
+        """Launch the captured step on the current stream; returns o."""
+        self._graph.replay()
+        return self.o
+
+    def step_ms(self) -> float:
+        e = self._graph_events
+        return e[0].elapsed_time(e[3])
+
+    def decode_ms(self) -> float:
+        e = self._graph_events
+        return e[1].elapsed_time(e[2])
 
     def status(self) -> int:
         return int(self.dev_status.item())
