@@ -46,8 +46,6 @@ constexpr int kKCh = kCR / 64;       // 9 dim chunks per tile
 constexpr int kVCh = kTile / 32;     // 8 latent chunks per tile
 constexpr int kThreads = 384;
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
-constexpr uint32_t kPageBytes = kP * kCR * 2;   // 73,728 B: one page is contiguous in the pool
-constexpr int kPrefetch = 0;         // 1: prefetch the next tile's pages into L2 (measured slower)
 constexpr int kXSlots = 4;                      // exchange slots per CTA: tile t uses t % 4
 constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
 constexpr uint32_t kXHdrBytes = 16;             // flag word (1: the tile's maxima follow) + pad
@@ -92,7 +90,6 @@ struct Bars {
 constexpr int kSmemBytes = OFF_BAR + (int)sizeof(Bars) + 1024;   // + alignment slack
 
 struct Params {
-  const uint8_t* pool;   // for L2 prefetch of whole pages
   const int32_t* bt;
   int maxp, num_pages;
   const int32_t* seq_lens;
@@ -126,7 +123,11 @@ __device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_
     buf[(((size_t)unit * 2 + rank) * kTraceEvents + ev) * kTraceTiles + t] = ns;
   }
 }
+#ifdef MLA_TC_PROF_ONLY
+#define TRACE(ev, t) ((void)0)
+#else
 #define TRACE(ev, t) trace(prm.trace, unit, rank, ev, t)
+#endif
 // cycle totals of one thread's activities (slot < 8), stored at the end of event row 15
 #define PROF(slot, stmt)                    \
   do {                                      \
@@ -134,17 +135,17 @@ __device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_
     stmt;                                   \
     prof[slot] += clock64() - p0_;          \
   } while (0)
-#define PROF_STORE()                                                                          \
+#define PROF_STORE(base)                                                                   \
   do {                                                                                      \
     if (prm.trace && unit < kTraceUnits)                                                    \
       for (int q = 0; q < 8; ++q)                                                           \
-        prm.trace[(((size_t)unit * 2 + rank) * kTraceEvents + 15) * kTraceTiles + 512 + q] = \
+        prm.trace[(((size_t)unit * 2 + rank) * kTraceEvents + 15) * kTraceTiles + (base) + q] = \
             (unsigned long long)prof[q];                                                    \
   } while (0)
 #else
 #define TRACE(ev, t) ((void)0)
 #define PROF(slot, stmt) stmt
-#define PROF_STORE() ((void)0)
+#define PROF_STORE(base) ((void)0)
 #endif
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
@@ -281,69 +282,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status};
 
-  auto page_y = [&](int idx_in_unit) -> int {
-    const int pidx = lo / kP + idx_in_unit;
-    if (pidx >= valid_pages) return prm.num_pages * kP;   // past the range: TMA zero-fills
-    const int pg = prm.bt[(size_t)b * prm.maxp + pidx];
+  // Page ids of this unit's range, read by a whole producer warp 32 pages at a time (lane j
+  // holds page 32*batch + j of the range) one batch ahead of use, so no TMA issue waits on a
+  // block-table load. Pages past the range, or with an id outside the pool (flagged), map to
+  // the row one past the pool, which TMA fills with zeros.
+  auto fetch_pid = [&](int batch) -> int {
+    const int pidx = lo / kP + batch * 32 + lane;
+    if (pidx >= valid_pages) return -1;
+    const int pg = __ldg(prm.bt + (size_t)b * prm.maxp + pidx);
     if (pg < 0 || pg >= prm.num_pages) {
       flag_status(prm.status, MLA_DEV_INDEX_OUT_OF_RANGE);
-      return prm.num_pages * kP;
+      return -1;
     }
-    return pg * kP;
+    return pg;
+  };
+  int pid_batch = 0, pid_cur = 0, pid_next = 0;
+  // first row of page idx_in_unit (warp-uniform, non-decreasing across calls)
+  auto page_y = [&](int idx_in_unit) -> int {
+    while ((idx_in_unit >> 5) > pid_batch) {
+      ++pid_batch;
+      pid_cur = pid_next;
+      pid_next = fetch_pid(pid_batch + 1);
+    }
+    const int pg = __shfl_sync(0xffffffffu, pid_cur, idx_in_unit & 31);
+    return pg < 0 ? prm.num_pages * kP : pg * kP;
   };
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    // Q once, then every tile's key chunks in order
-    if (lane == 0) {
+    // Q once, then every tile's key chunks in order (lane 0 issues; the warp keeps page ids)
+    pid_cur = fetch_pid(0);
+    pid_next = fetch_pid(1);
+    const bool leader = lane == 0;
+    const uint64_t pol_s = policy_evict_normal();  // re-read soon for the V phase
+    const bool even = rank == 0;
+    auto at_even = [&](uint64_t* bar) { return mapa(smem_u32(bar), 0); };
+    if (leader) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       const uint64_t pol_q = policy_evict_last();
-      const uint64_t pol_s = policy_evict_normal();  // re-read soon for the V phase
-      const bool even = rank == 0;
-      auto at_even = [&](uint64_t* bar) { return mapa(smem_u32(bar), 0); };
       if (even) mbar_arrive_expect_tx(&bars->q_ready, 2 * kKCh * 8192);
       for (int c = 0; c < kKCh; ++c)
         tma_load_2d_pair(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
                          at_even(&bars->q_ready), pol_q);
-      int s_cnt = 0;
-      auto load_s_chunk = [&](int c, int y0, int y1) -> bool {
-        const int st = s_cnt % kNS;
-        if (s_cnt >= kNS && !wait_bar(&bars->s_free[st], ((s_cnt / kNS) - 1) & 1, cx)) return false;
-        if (even) mbar_arrive_expect_tx(&bars->s_ready[st], 2 * 16384);
-        const uint32_t bar = at_even(&bars->s_ready[st]);
-        tma_load_2d_pair(sm + OFF_S + st * 16384, &tmK, c * 64, y0, bar, pol_s);
-        tma_load_2d_pair(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, bar, pol_s);
-        TRACE(16, s_cnt);
-        ++s_cnt;
-        return true;
-      };
-      // this CTA's two pages of a future tile, into L2 (kPrefetch = 0 disables)
-      auto prefetch_next = [&](int t) {
-        if (kPrefetch == 0 || t >= nt) return;
-        for (int q = 0; q < 2; ++q) {
-          const int y = page_y(4 * t + 2 * (int)rank + q);
-          if (y < prm.num_pages * kP) prefetch_l2(prm.pool + (size_t)y * kCR * 2, kPageBytes);
-        }
-      };
-      // key chunks of every tile in order (the latent chunks have their own producer)
-      bool ok = true;
-      for (int k = 0; k < nt && ok; ++k) {
-        prefetch_next(k + 1);
-        const int ys0 = page_y(4 * k + 2 * (int)rank);
-        const int ys1 = page_y(4 * k + 2 * (int)rank + 1);
-        for (int c = 0; c < kKCh && ok; ++c) {
+    }
+    int s_cnt = 0;
+#ifdef MLA_TC_TRACE
+    long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const long long prof_start = clock64();
+#endif
+    auto load_s_chunk = [&](int c, int y0, int y1) -> bool {
+      const int st = s_cnt % kNS;
+      bool r = true;
+      if (s_cnt >= kNS) PROF(0, r = wait_bar(&bars->s_free[st], ((s_cnt / kNS) - 1) & 1, cx));
+      if (!r) return false;
+      if (even) mbar_arrive_expect_tx(&bars->s_ready[st], 2 * 16384);
+      const uint32_t bar = at_even(&bars->s_ready[st]);
+      tma_load_2d_pair(sm + OFF_S + st * 16384, &tmK, c * 64, y0, bar, pol_s);
+      tma_load_2d_pair(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, bar, pol_s);
+      TRACE(16, s_cnt);
+      ++s_cnt;
+      return true;
+    };
+    // key chunks of every tile in order (the latent chunks have their own producer)
+    bool ok = true;
+    for (int k = 0; k < nt && ok; ++k) {
+      const int ys0 = page_y(4 * k + 2 * (int)rank);
+      const int ys1 = page_y(4 * k + 2 * (int)rank + 1);
+      for (int c = 0; c < kKCh && ok; ++c) {
+        if (leader) {
           if (c == 4) TRACE(15, k);
           ok = load_s_chunk(c, ys0, ys1);
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (!ok) {
-        // drain this CTA's loads still in flight: wait until the even CTA's MMA issuer has
-        // stopped and enough time has passed for any issued load to land
-        const long long t0 = clock64();
-        while (clock64() - t0 < 2000000) {
-        }
+    }
+#ifdef MLA_TC_TRACE
+    prof[7] = clock64() - prof_start;
+    if (leader) PROF_STORE(520);
+#endif
+    if (!ok && leader) {
+      // drain this CTA's loads still in flight: wait until the even CTA's MMA issuer has
+      // stopped and enough time has passed for any issued load to land
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000) {
       }
     }
   } else if (warp == 1) {
@@ -367,7 +390,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         TRACE(18, s_cnt);
         tc_fence_after();
         PROF(1, {
-#pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
             const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
@@ -387,9 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         TRACE(21, v_cnt);
         tc_fence_after();
         PROF(4, {
-#pragma unroll
           for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
             for (int k = 0; k < 2; ++k) {
               const uint64_t a = smem_desc(sV + st * 16384 + blk * 8192 + k * 2048, 4096, 1024, kSw128);
               const uint64_t bd = smem_desc(sP + (t & 1) * 32768 + v * 4096 + k * 2048, 8192, 1024, kSw128);
@@ -430,7 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
 #ifdef MLA_TC_TRACE
       prof[7] = clock64() - prof_start;
-      PROF_STORE();
+      PROF_STORE(512);
 #endif
       // every MMA this thread issued (they write both CTAs' TMEM) completes before teardown
       mma_commit_pair(&bars->teardown, 0x1);
@@ -442,11 +462,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // MMA issuer's order. On the last tile the rows past the range may hold anything (P is 0
     // there): those chunks land on this CTA's own barrier, the warp zeroes the rows, and only
     // then are the bytes counted on the even CTA's barrier.
+    pid_cur = fetch_pid(0);
+    pid_next = fetch_pid(1);
     const uint64_t pol_v = policy_evict_first();
     const bool even = rank == 0;
     const uint32_t even_v0 = mapa(smem_u32(&bars->v_ready[0]), 0);
     int v_cnt = 0;
     bool ok = true;
+#ifdef MLA_TC_TRACE
+    long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const long long prof_start = clock64();
+#endif
     auto finish_last = [&](int v) -> bool {   // zero + count chunk v of the last tile
       const int st = v % kNV;                 // the last tile starts at an even chunk count
       bool r = true;
@@ -478,8 +504,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // before a slot is reused on the last tile, the chunk that held it must be counted
         if (last && v >= kNV) ok = finish_last(v - kNV);
         if (!ok) break;
+        const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;   // whole warp
         if (lane == 0) {
-          if (v_cnt >= kNV) ok = wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx);
+          if (v_cnt >= kNV) PROF(0, ok = wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx));
           if (ok) {
             if (even) mbar_arrive_expect_tx(&bars->v_ready[st], 2 * 16384);
             uint32_t bar;
@@ -489,7 +516,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             } else {
               bar = mapa(smem_u32(&bars->v_ready[st]), 0);
             }
-            const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;
             for (int q4 = 0; q4 < 4; ++q4)
               tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
                                (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
@@ -501,6 +527,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (last && ok)
         for (int v = kVCh - kNV; v < kVCh && ok; ++v) ok = finish_last(v);
     }
+#ifdef MLA_TC_TRACE
+    prof[7] = clock64() - prof_start;
+    if (lane == 0) PROF_STORE(528);
+#endif
   } else if (warp == 3) {
     // ================================================================ exchange
     // Fetches the peer's P^T half, flag word and tile maxima once the peer has put them in
@@ -896,7 +926,6 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
   if (ws_bytes < part + (size_t)B * n_q * S * tc::kXUnitBytes) return cudaErrorInvalidValue;
   tc::Params prm;
-  prm.pool = static_cast<const uint8_t*>(pool);
   prm.bt = bt;
   prm.maxp = maxp;
   prm.num_pages = num_pages;
