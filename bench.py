@@ -141,6 +141,34 @@ def _cpu_oracle_sample(wl, budget_s: float = 12.0, max_heads: int = 1 << 30):
     return done_bytes / t_total / 1e9, sample, threads, t_total
 
 
+PROFILE = os.path.join(ROOT, "profiles", "decode_tc_v2_b64_l4096.md")
+DECODE_SOURCE = os.path.join(ROOT, "mla_latent_kv_78_b300", "csrc", "decode_tc.cu")
+
+
+def _ncu_traffic():
+    """DRAM bytes (read + write) per decode launch from the committed ncu summary, or None when
+    the summary is missing or was taken on a different decode_tc.cu (its recorded sha256)."""
+    import hashlib
+
+    try:
+        text = open(PROFILE).read()
+        sha = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`").lstrip("- ")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("decode_tc.cu sha256") != sha:
+        return None
+    try:
+        return int(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def reduce_max_over_ranks(xs, device):
     """Element-wise max of xs over all ranks (the slowest rank's times); identity when the
     process group is absent or has one rank."""
@@ -327,7 +355,7 @@ def run_ours(args, world, rank, local_rank):
                    "tflops": flops / (dec_avg_ms * 1e-3) / 1e12,
                    "algorithmic_bytes": dec_bytes, "flops": flops},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": _ncu_traffic(),
                      "kernel": "mla_decode", "peak_source": peaks["source"],
                      "tensor_frac": flops / (dec_avg_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,

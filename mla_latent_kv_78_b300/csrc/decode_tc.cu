@@ -16,17 +16,20 @@
 //    (M = 256 latent rows per MMA, two MMAs per K step): each CTA holds half of O^T,
 //    256 TMEM columns, which leaves room for a double-buffered S^T (2 x 128 columns).
 //  * P^T is split by head: the CTA that computed a token's scores keeps its own head
-//    half and sends the other half (16 KB per tile) to the peer with st.async. The only
-//    other exchange is each tile's per-head maximum (512 B), so both CTAs take identical
-//    online-softmax decisions. Rescaling is lazy: a head's reference maximum moves only
-//    when a score exceeds it by more than 2^8, which keeps P in bf16 range and leaves
-//    O untouched on almost every tile.
+//    half and sends the other half (16 KB per tile) to the peer through a 4-slot exchange
+//    ring in global memory (normally L2), with a flag word and, rarely, the tile's maxima.
+//    Both CTAs take identical online-softmax decisions from the same data: the reference
+//    maximum of a head moves only when a tile's published maximum exceeds it by more than
+//    2^8, two tiles later, so the common tile needs no cross-thread reduction.
 //  * The key tile is read from HBM once, as [128 tokens x 64 dims] chunks for S^T; the
-//    latent part is read a second time, 3/4 of a tile later, as [64 tokens x 256 d_c]
+//    latent part is read a second time, about a tile later, as [32 tokens x 256 d_c]
 //    chunks for O^T, normally from L2.
-//  * Warp roles: w0 TMA producer, w1 MMA issuer (even CTA) + TMEM owner, w2 relay (waits
-//    its CTA's loads, zeroes invalid rows on the last tile, signals the even CTA),
-//    w4..w11 softmax / epilogue (thread = TMEM lane; warps 4-7 heads 0-63, 8-11 heads 64-127).
+//  * Two threads issue MMAs: one thread cannot issue 2-SM MMAs as fast as the tensor pipe
+//    retires them (~85 cycles per instruction against 64), two can.
+//  * Warp roles: w0 key-chunk TMA producer (+Q), w1 S^T issuer (even CTA) + TMEM owner,
+//    w2 latent-chunk producer (+ zeroing of rows past the range on the last tile),
+//    w3 exchange, w4..w11 softmax / epilogue (thread = TMEM lane; warps 4-7 heads 0-63,
+//    8-11 heads 64-127), w12 P.V issuer (even CTA).
 //  * Every wait is bounded; a timeout sets MLA_DEV_TIMEOUT and every role winds down.
 #include <math_constants.h>
 
@@ -41,10 +44,11 @@ using namespace ptx;
 constexpr int kH = 128, kC = 512, kR = 64, kCR = 576, kP = 64;
 constexpr int kTile = 256;           // tokens per tile (4 pages)
 constexpr int kNS = 3;               // S-phase ring: [128 tok x 64 dims] bf16 = 16 KB
-constexpr int kNV = 2;               // V-phase ring: [32 tok x 256 d_c] bf16 = 16 KB
+constexpr int kNV = 4;               // V-phase ring: [32 tok x 256 d_c] bf16 = 16 KB
 constexpr int kKCh = kCR / 64;       // 9 dim chunks per tile
 constexpr int kVCh = kTile / 32;     // 8 latent chunks per tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;          // 13 warps
+constexpr int kPvWarp = 12;             // the P.V issuer
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
 constexpr int kXSlots = 4;                      // exchange slots per CTA: tile t uses t % 4
 constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
@@ -57,8 +61,8 @@ constexpr float kRange = 96.f;  // larger excesses are clamped and flagged (MLA_
 constexpr int OFF_Q = 0;                           // 9 x [64 heads x 64 dims]  (8 KB each)
 constexpr int OFF_S = OFF_Q + kKCh * 8192;         // kNS x 16 KB
 constexpr int OFF_V = OFF_S + kNS * 16384;         // kNV x 16 KB
-constexpr int OFF_P = OFF_V + kNV * 16384;         // 2 x [256 tok x 64 heads] = 2 x 32 KB
-constexpr int OFF_F = OFF_P + 2 * 32768;           // fp32 scratch
+constexpr int OFF_P = OFF_V + kNV * 16384;         // [256 tok x 64 heads] = 32 KB
+constexpr int OFF_F = OFF_P + 32768;               // fp32 scratch
 constexpr int kRcvFloats = (int)(kXBytes - kXPBytes) / 4;   // 132: flag word, pad, 128 maxima
 constexpr int F_COL = 0;       // [8 warps][64]   column max / column sum partials
 constexpr int F_CMLOC = 512;   // [2][128] this CTA's published per-head tile maxima
@@ -147,6 +151,23 @@ __device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_
 #define PROF(slot, stmt) stmt
 #define PROF_STORE(base) ((void)0)
 #endif
+
+// Sum over the warp's 32 lanes of each of 32 values per lane; lane j returns the sum of
+// value j. Halving exchange: at each step a lane keeps one half of its values, sends the
+// other half to its partner and adds what it receives (31 shuffles in all).
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int q = 0; q < w; ++q) {
+      const float keep = hi ? v[q + w] : v[q];
+      const float send = hi ? v[q] : v[q + w];
+      v[q] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
   const uint32_t a = smem_u32(bar);
@@ -267,7 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->x0_ready, 1);
     mbar_init(&bars->l_landed, 1);
-    mbar_init(&bars->teardown, 1);
+    mbar_init(&bars->teardown, 2);   // both issuing threads' last commits
     fence_mbarrier_init_cluster();
   }
   if (tid < kH) fs[F_M + tid] = -CUDART_INF_F;
@@ -370,89 +391,118 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ================================================================ MMA issuer (even CTA)
+    // ================================================================ S^T issuer (even CTA)
+    // Scores of every tile: S^T(t) = K(t) . Q^T into TMEM buffer t % 2. The P.V products have
+    // their own issuing thread (warp 12): one thread cannot issue 2-SM MMAs as fast as the
+    // tensor pipe retires them, two can.
     if (rank == 0 && lane == 0) {
       const uint32_t idS = idesc_bf16_f32(256, 128, 0, 0);
-      const uint32_t idPV = idesc_bf16_f32(256, 128, 1, 1);
-      const uint32_t sQ = smem_u32(sm + OFF_Q), sS = smem_u32(sm + OFF_S);
-      const uint32_t sV = smem_u32(sm + OFF_V), sP = smem_u32(sm + OFF_P);
-      int s_cnt = 0, v_cnt = 0;
+      // operand descriptors; an operand's start moves by adding (byte offset >> 4)
+      const uint64_t dS = smem_desc(smem_u32(sm + OFF_S), 16, 1024, kSw128);
+      const uint64_t dQ = smem_desc(smem_u32(sm + OFF_Q), 16, 1024, kSw128);
+      uint32_t s_st = 0, s_ph = 0;
 #ifdef MLA_TC_TRACE
+      int s_cnt = 0;
       long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       const long long prof_start = clock64();
 #endif
-      auto mma_s_chunk = [&](int t, int c) -> bool {
-        const int st = s_cnt % kNS;
-        TRACE(17, s_cnt);
-        bool r;
-        PROF(0, r = wait_bar(&bars->s_ready[st], (s_cnt / kNS) & 1, cx));
-        if (!r) return false;
-        TRACE(18, s_cnt);
-        tc_fence_after();
-        PROF(1, {
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = smem_desc(sS + st * 16384 + k * 32, 16, 1024, kSw128);
-            const uint64_t bd = smem_desc(sQ + c * 8192 + k * 32, 16, 1024, kSw128);
-            mma_bf16_pair(tmem + (t & 1) * 128, a, bd, idS, (c | k) != 0);
-          }
-        });
-        PROF(2, mma_commit_pair(&bars->s_free[st], 0x3));
-        ++s_cnt;
-        return true;
-      };
-      auto mma_v_chunk = [&](int t, int v) -> bool {
-        const int st = v_cnt % kNV;
-        TRACE(20, v_cnt);
-        bool r;
-        PROF(3, r = wait_bar(&bars->v_ready[st], (v_cnt / kNV) & 1, cx));
-        if (!r) return false;
-        TRACE(21, v_cnt);
-        tc_fence_after();
-        PROF(4, {
-          for (int blk = 0; blk < 2; ++blk)
-            for (int k = 0; k < 2; ++k) {
-              const uint64_t a = smem_desc(sV + st * 16384 + blk * 8192 + k * 2048, 4096, 1024, kSw128);
-              const uint64_t bd = smem_desc(sP + (t & 1) * 32768 + v * 4096 + k * 2048, 8192, 1024, kSw128);
-              mma_bf16_pair(tmem + 256 + blk * 128, a, bd, idPV, (t | v | k) != 0);
-            }
-        });
-        PROF(5, mma_commit_pair(&bars->v_free[st], 0x3));
-        ++v_cnt;
-        return true;
-      };
       bool ok = wait_bar(&bars->q_ready, 0, cx);
-      // step k: S^T(k) interleaved chunk for chunk with PV(k-2)
-      for (int k = 0; k < nt + 2 && ok; ++k) {
-        const bool do_s = k < nt, do_v = k >= 2;
-        if (do_s) TRACE(22, k);
-        if (do_s && k >= 2) PROF(6, ok = wait_bar(&bars->s_empty[k & 1], ((k >> 1) - 1) & 1, cx));
-        if (do_s && ok) TRACE(9, k);
+      for (int t = 0; t < nt && ok; ++t) {
+        TRACE(22, t);
+        // TMEM buffer t % 2 is free once the softmax has read S^T(t-2)
+        if (t >= 2) PROF(6, ok = wait_bar(&bars->s_empty[t & 1], ((t >> 1) - 1) & 1, cx));
+        if (!ok) break;
+        TRACE(9, t);
+        const uint32_t d = tmem + (uint32_t)(t & 1) * 128u;
         for (int c = 0; c < kKCh && ok; ++c) {
-          if (do_s) ok = mma_s_chunk(k, c);
-          if (do_s && c == 4) TRACE(13, k);
-          if (ok && do_v && c == 0) {
-            TRACE(23, k - 2);
-            PROF(6, ok = wait_bar(&bars->p_ready[k & 1], ((k - 2) >> 1) & 1, cx));
-            TRACE(1, k - 2);
-            tc_fence_after();
+          TRACE(17, s_cnt);
+          PROF(0, ok = wait_bar(&bars->s_ready[s_st], s_ph, cx));
+          if (!ok) break;
+          TRACE(18, s_cnt);
+          PROF(2, tc_fence_after());
+          // K chunk c (128 tokens x 64 dims per CTA) . Q chunk c^T, four K=16 steps
+          const uint64_t a0 = dS + s_st * 1024u, b0 = dQ + (uint32_t)c * 512u;
+          PROF(1, {
+            mma_bf16_pair(d, a0, b0, idS, c != 0);
+            mma_bf16_pair(d, a0 + 2, b0 + 2, idS, 1);
+            mma_bf16_pair(d, a0 + 4, b0 + 4, idS, 1);
+            mma_bf16_pair(d, a0 + 6, b0 + 6, idS, 1);
+          });
+          PROF(2, mma_commit_pair(&bars->s_free[s_st], 0x3));
+          if (++s_st == kNS) {
+            s_st = 0;
+            s_ph ^= 1u;
           }
-          if (ok && do_v && c < kVCh) ok = mma_v_chunk(k - 2, c);
+#ifdef MLA_TC_TRACE
+          ++s_cnt;
+#endif
+          if (c == 4) TRACE(13, t);
         }
         if (!ok) break;
-        if (do_s) {
-          mma_commit_pair(&bars->s_full[k & 1], 0x3);
-          TRACE(0, k);
-        }
-        if (do_v) {
-          mma_commit_pair(&bars->o_done[k & 1], 0x3);
-          TRACE(2, k - 2);
-        }
+        mma_commit_pair(&bars->s_full[t & 1], 0x3);
+        TRACE(0, t);
       }
 #ifdef MLA_TC_TRACE
       prof[7] = clock64() - prof_start;
       PROF_STORE(512);
 #endif
       // every MMA this thread issued (they write both CTAs' TMEM) completes before teardown
+      mma_commit_pair(&bars->teardown, 0x1);
+      wait_drain(&bars->teardown, 0);
+    }
+  } else if (warp == kPvWarp) {
+    // ================================================================ P.V issuer (even CTA)
+    // O^T += V^T(t) . P^T(t) for every tile once both CTAs' P^T halves are in place.
+    if (rank == 0 && lane == 0) {
+      const uint32_t idPV = idesc_bf16_f32(256, 128, 1, 1);
+      const uint64_t dV = smem_desc(smem_u32(sm + OFF_V), 4096, 1024, kSw128);
+      const uint64_t dP = smem_desc(smem_u32(sm + OFF_P), 8192, 1024, kSw128);
+      uint32_t v_st = 0, v_ph = 0;
+#ifdef MLA_TC_TRACE
+      int v_cnt = 0;
+      long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      const long long prof_start = clock64();
+#endif
+      bool ok = true;
+      for (int t = 0; t < nt && ok; ++t) {
+        TRACE(23, t);
+        PROF(6, ok = wait_bar(&bars->p_ready[t & 1], (t >> 1) & 1, cx));
+        if (!ok) break;
+        TRACE(1, t);
+        tc_fence_after();
+        for (int v = 0; v < kVCh && ok; ++v) {
+          TRACE(20, v_cnt);
+          PROF(3, ok = wait_bar(&bars->v_ready[v_st], v_ph, cx));
+          if (!ok) break;
+          TRACE(21, v_cnt);
+          PROF(5, tc_fence_after());
+          // this CTA's 2 x 128 latent rows x 32 tokens (V^T) . P^T rows v of tile t
+          const uint64_t a0 = dV + v_st * 1024u;
+          const uint64_t b0 = dP + (uint32_t)v * 256u;
+          const uint32_t acc = (t | v) != 0;
+          PROF(4, {
+            mma_bf16_pair(tmem + 256, a0, b0, idPV, acc);
+            mma_bf16_pair(tmem + 256, a0 + 128, b0 + 128, idPV, 1);
+            mma_bf16_pair(tmem + 384, a0 + 512, b0, idPV, acc);
+            mma_bf16_pair(tmem + 384, a0 + 640, b0 + 128, idPV, 1);
+          });
+          PROF(5, mma_commit_pair(&bars->v_free[v_st], 0x3));
+          if (++v_st == kNV) {
+            v_st = 0;
+            v_ph ^= 1u;
+          }
+#ifdef MLA_TC_TRACE
+          ++v_cnt;
+#endif
+        }
+        if (!ok) break;
+        mma_commit_pair(&bars->o_done[t & 1], 0x3);
+        TRACE(2, t);
+      }
+#ifdef MLA_TC_TRACE
+      prof[7] = clock64() - prof_start;
+      PROF_STORE(536);
+#endif
       mma_commit_pair(&bars->teardown, 0x1);
       wait_drain(&bars->teardown, 0);
     }
@@ -474,9 +524,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const long long prof_start = clock64();
 #endif
     auto finish_last = [&](int v) -> bool {   // zero + count chunk v of the last tile
-      const int st = v % kNV;                 // the last tile starts at an even chunk count
+      const int base = (nt - 1) * kVCh;       // chunk count before the last tile
+      const int st = (base + v) % kNV;
+      const int first = (st - base % kNV + kNV) % kNV;   // the last tile's first chunk in slot st
       bool r = true;
-      if (lane == 0) r = wait_bar(&bars->v_landed[st], (v / kNV) & 1, cx);
+      if (lane == 0) r = wait_bar(&bars->v_landed[st], ((v - first) / kNV) & 1, cx);
       if (!__shfl_sync(0xffffffffu, r, 0)) return false;
       const int tok0 = lo + (nt - 1) * kTile + v * 32;
       const int nvalid = max(0, min(32, hi - tok0));
@@ -541,11 +593,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int t = 0; t < nt && ok; ++t) {
         const int par = t & 1, slot = t & (kXSlots - 1);
         ok = wait_bar(&bars->x_ready[par], (t >> 1) & 1, cx);
-        if (ok && t >= 2) ok = wait_bar(&bars->o_done[par], ((t - 2) >> 1) & 1, cx);
+        // the single P^T buffer is free once P.V of the previous tile has read it
+        if (ok && t >= 1) ok = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
         if (!ok) break;
         TRACE(8, t);
         const uint8_t* src = x_slot(peer, slot);
-        bulk_g2s(sm + OFF_P + par * 32768 + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
+        bulk_g2s(sm + OFF_P + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
         bulk_g2s(fs + F_RCV + slot * kRcvFloats, src + kXPBytes, kXBytes - kXPBytes,
                  &bars->p_landed[par]);
         ok = wait_bar(&bars->p_landed[par], (t >> 1) & 1, cx);
@@ -553,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok) arrive_even(&bars->p_ready[par], rank);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ================================================================ softmax / epilogue
     // Thread = one TMEM lane: token i of this CTA's half tile for the scores, latent row i for
     // the output. Each thread handles one head group (64 heads) of its token.
@@ -571,9 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int stid = tid - 128;        // 0..255
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
     const float* Mg = fs + F_M + 64 * g;
-    float l_acc[64];
-#pragma unroll
-    for (int c = 0; c < 64; ++c) l_acc[c] = 0.f;
+    float l_w[2] = {0.f, 0.f};   // sums of P of this warp's tokens for heads 64g + 32 h2 + lane
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int par = t & 1, slot = t & (kXSlots - 1);
@@ -601,24 +652,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (stid == 0) TRACE(3, t);
       const bool rescale = flags[FL_RESCALE + par] != 0;
       tc_fence_after();
-      float s[64];
-      tmem_ld32(lane_addr + par * 128 + 64 * g, s);
-      tmem_ld32(lane_addr + par * 128 + 64 * g + 32, s + 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_even(&bars->s_empty[par], rank);
-      if (stid == 0) TRACE(12, t);
+      const uint32_t s_addr = lane_addr + par * 128 + 64 * g;
       const int tok = lo + t * kTile + (int)rank * 128 + i;
       const bool valid = tok < hi;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) s[c] = valid ? s[c] * prm.scale_log2 : -CUDART_INF_F;
       if (t == 0) {
         // ---- the first reference: per-head maxima over both CTAs' tokens of tile 0
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float s[32];
+          tmem_ld32(s_addr + 32 * h2, s);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float mx = warp_max_f32(s[c]);
-          if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
+          for (int c = 0; c < 32; ++c) {
+            const float mx = warp_max_f32(valid ? s[c] * prm.scale_log2 : -CUDART_INF_F);
+            if (lane == c) fs[F_COL + sw * 64 + 32 * h2 + c] = mx;
+          }
         }
         bar_sync(2, 256);
         float my_max = -CUDART_INF_F;
@@ -642,35 +690,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       if (stid == 0) TRACE(4, t);
-      // ---- weights p = 2^(s - M) in bf16, with the overshoot checks
+      // ---- weights p = 2^(s - M) in bf16 (32 heads at a time), the overshoot checks, and
+      // the running per-head sums of this warp's tokens (lane j keeps head 32 h2 + j)
       uint32_t pk[32];
       bool over = false, extreme = false;
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(Mg + 4 * c4);
-        const float m[4] = {m4.x, m4.y, m4.z, m4.w};
-        float p[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float d = s[4 * c4 + e] - m[e];
-          over |= d > kLazy;
-          extreme |= d > kRange;
-          d = fminf(d, kRange);
-          p[e] = ex2(d);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float s[32];
+        tmem_ld32(s_addr + 32 * h2, s);
+        tmem_ld_wait();
+        if (h2 == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_even(&bars->s_empty[par], rank);
+          if (stid == 0) TRACE(12, t);
         }
-        pk[2 * c4] = pack_bf16x2(p[0], p[1]);
-        pk[2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(Mg + 32 * h2 + 4 * c4);
+          const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+          float p[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float d = (valid ? s[4 * c4 + e] * prm.scale_log2 : -CUDART_INF_F) - m[e];
+            over |= d > kLazy;
+            extreme |= d > kRange;
+            d = fminf(d, kRange);
+            p[e] = ex2(d);
+          }
+          pk[16 * h2 + 2 * c4] = pack_bf16x2(p[0], p[1]);
+          pk[16 * h2 + 2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
+        }
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          v[2 * c] = __uint_as_float(pk[16 * h2 + c] << 16);
+          v[2 * c + 1] = __uint_as_float(pk[16 * h2 + c] & 0xFFFF0000u);
+        }
+        const float lsum = warp_transpose_sum32(v, lane);
+        if (rescale) l_w[h2] *= fs[F_ALPHA + 64 * g + 32 * h2 + lane];
+        l_w[h2] += lsum;
       }
       if (extreme) flag_status(prm.status, MLA_DEV_SCORE_RANGE);
-      if (rescale) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) l_acc[c] *= fs[F_ALPHA + 64 * g + c];
-      }
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        l_acc[2 * c] += __uint_as_float(pk[c] << 16);
-        l_acc[2 * c + 1] += __uint_as_float(pk[c] & 0xFFFF0000u);
-      }
       if (stid == 0) TRACE(14, t);
       // ---- the peer's head half of P^T goes out first (same swizzled bytes as in shared
       // memory); the slot was last read four tiles ago
@@ -683,12 +744,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_global();
       }
-      // O must be stable to rescale (PV(t-1) done); otherwise only P's buffer must be free (PV(t-2))
+      // P^T's buffer is free, and O is stable to rescale, once P.V of the previous tile is done
       bool ok3 = true;
-      if (rescale)
-        ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
-      else if (t >= 2)
-        ok3 = wait_bar(&bars->o_done[par], ((t - 2) >> 1) & 1, cx);
+      if (t >= 1) ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
       bool any_over = false;
       if (bar_or(5, 256, over || !ok3)) {
         ok = bar_and(6, 256, ok3);
@@ -743,7 +801,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- this CTA's own head half of P^T, rows of its tokens
       if (g == (int)rank) {
         const int k = (int)rank * 128 + i;
-        uint8_t* dst = sm + OFF_P + par * 32768 + k * 128;
+        uint8_t* dst = sm + OFF_P + k * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
@@ -768,13 +826,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         // per-head sums of P over this warp's tokens
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float v = l_acc[c];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-          if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = v;
-        }
+        fs[F_COL + sw * 64 + lane] = l_w[0];
+        fs[F_COL + sw * 64 + 32 + lane] = l_w[1];
         bar_and(8, 256, true);
         const uint32_t peer_l = mapa(smem_u32(fs + F_LRCV), peer);
         const uint32_t peer_l_bar = mapa(smem_u32(&bars->l_landed), peer);
