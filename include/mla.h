@@ -77,7 +77,11 @@ extern "C" {
 #define MLA_KERNEL_AUTO 0   /* tensor-core kernel when the shape allows, else SIMT */
 #define MLA_KERNEL_SIMT 1   /* generic CUDA-core kernel, any shape */
 #define MLA_KERNEL_TC 2     /* tcgen05/TMEM kernel: n_heads=128, d_latent=512, d_rope=64,
-                               page_size=64, bf16 act, bf16 or FP8 cache, n_q in {1,2} */
+                               page_size=64, bf16 act, bf16 or FP8 cache, n_q in {1,2}.
+                               With an FP8 cache the operands are f16 (codes * scales,
+                               queries and softmax weights), so latents and absorbed
+                               queries must lie within f16 range (|x| < 65504); values
+                               below 2^-14 keep f16's subnormal precision only */
 
 typedef struct mla_config {
   int32_t n_heads;      /* H  = n_h                                               */

@@ -32,6 +32,7 @@
 //    8-11 heads 64-127), w12 P.V issuer (even CTA).
 //  * Every wait is bounded; a timeout sets MLA_DEV_TIMEOUT and every role winds down.
 #include <math_constants.h>
+#include <string.h>
 
 #include "mla_internal.cuh"
 #include "tc_ptx.cuh"
@@ -43,12 +44,10 @@ using namespace ptx;
 
 constexpr int kH = 128, kC = 512, kR = 64, kCR = 576, kP = 64;
 constexpr int kTile = 256;           // tokens per tile (4 pages)
-constexpr int kNS = 3;               // S-phase ring: [128 tok x 64 dims] bf16 = 16 KB
-constexpr int kNV = 4;               // V-phase ring: [32 tok x 256 d_c] bf16 = 16 KB
 constexpr int kKCh = kCR / 64;       // 9 dim chunks per tile
 constexpr int kVCh = kTile / 32;     // 8 latent chunks per tile
-constexpr int kThreads = 416;          // 13 warps
 constexpr int kPvWarp = 12;             // the P.V issuer
+constexpr int kCvtWarp0 = 13;           // FP8 cache: warps 13-15 convert codes to f16 tiles
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
 constexpr int kXSlots = 4;                      // exchange slots per CTA: tile t uses t % 4
 constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
@@ -56,13 +55,13 @@ constexpr uint32_t kXHdrBytes = 16;             // flag word (1: the tile's maxi
 constexpr uint32_t kXBytes = kXPBytes + kXHdrBytes + kH * 4;   // + that tile's per-head maxima
 constexpr size_t kXUnitBytes = 2 * kXSlots * (size_t)kXBytes + 2 * kH * 4;  // per (seq, row, split)
 constexpr float kLazy = 8.f;    // log2 units a score may exceed the reference before it moves
-constexpr float kRange = 96.f;  // larger excesses are clamped and flagged (MLA_DEV_SCORE_RANGE)
+// Larger excesses are clamped and flagged (MLA_DEV_SCORE_RANGE): bf16 P holds 2^96, f16 P
+// (FP8 cache) 2^15.
+template <bool F8>
+constexpr float kRange = F8 ? 15.f : 96.f;
+constexpr int kRawS = 8192 + 2048;   // FP8 key chunk: [128 tok x 64 codes] + [128 tok x 4 scales]
+constexpr int kRawV = 8192 + 512;    // FP8 latent chunk: 4 x [32 tok x 64 codes] + [32 tok x 4 scales]
 
-constexpr int OFF_Q = 0;                           // 9 x [64 heads x 64 dims]  (8 KB each)
-constexpr int OFF_S = OFF_Q + kKCh * 8192;         // kNS x 16 KB
-constexpr int OFF_V = OFF_S + kNS * 16384;         // kNV x 16 KB
-constexpr int OFF_P = OFF_V + kNV * 16384;         // [256 tok x 64 heads] = 32 KB
-constexpr int OFF_F = OFF_P + 32768;               // fp32 scratch
 constexpr int kRcvFloats = (int)(kXBytes - kXPBytes) / 4;   // 132: flag word, pad, 128 maxima
 constexpr int F_COL = 0;       // [8 warps][64]   column max / column sum partials
 constexpr int F_CMLOC = 512;   // [2][128] this CTA's published per-head tile maxima
@@ -77,12 +76,36 @@ constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for th
 constexpr int FL_ABORT = 2;    // a bounded wait gave up
 constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
 constexpr int F_END = F_FLAG + 6;
-constexpr int OFF_BAR = OFF_F + F_END * 4;
+// Shared-memory layout. bf16 cache: keys and latents arrive by TMA in their MMA layout.
+// FP8 cache: raw codes and scales arrive by TMA in staging rings (RS, RV slots) and the
+// converter warps write f16 operand tiles into the S and V rings.
+template <bool F8>
+struct Lay {
+  static constexpr int NS = F8 ? 2 : 3;     // S-phase ring: [128 tok x 64 dims] 16-bit = 16 KB
+  static constexpr int NV = F8 ? 2 : 4;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
+  static constexpr int RS = F8 ? 3 : 0;     // raw key-chunk slots (kRawS bytes)
+  static constexpr int RV = F8 ? 2 : 0;     // raw latent-chunk slots (kRawV bytes)
+  static constexpr int THREADS = F8 ? 512 : 416;
+  static constexpr int OFF_Q = 0;                        // 9 x [64 heads x 64 dims] (8 KB each)
+  static constexpr int OFF_S = OFF_Q + kKCh * 8192;
+  static constexpr int OFF_V = OFF_S + NS * 16384;
+  static constexpr int OFF_P = OFF_V + NV * 16384;       // [256 tok x 64 heads] = 32 KB
+  static constexpr int OFF_RS = OFF_P + 32768;
+  static constexpr int OFF_RV = OFF_RS + RS * kRawS;
+  static constexpr int OFF_F = OFF_RV + RV * kRawV;      // fp32 scratch
+  static constexpr int OFF_BAR = OFF_F + F_END * 4;
+};
 
-struct Bars {
+template <bool F8>
+struct BarsT {
+  static constexpr int NS = Lay<F8>::NS, NV = Lay<F8>::NV;
+  static constexpr int RS = Lay<F8>::RS > 0 ? Lay<F8>::RS : 1;
+  static constexpr int RV = Lay<F8>::RV > 0 ? Lay<F8>::RV : 1;
   uint64_t q_ready;
-  uint64_t s_ready[kNS], s_free[kNS];
-  uint64_t v_landed[kNV], v_ready[kNV], v_free[kNV];
+  uint64_t q_conv;       // FP8: both CTAs' Q halves converted to f16 (even CTA, 2 arrivals)
+  uint64_t s_ready[NS], s_free[NS];
+  uint64_t v_landed[NV], v_ready[NV], v_free[NV];
+  uint64_t rs_ready[RS], rs_free[RS], rv_ready[RV], rv_free[RV];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_landed[2], p_ready[2], o_done[2];
   uint64_t x_ready[2];   // the peer has put P^T(t) and its maxima of tile t in global memory
@@ -91,7 +114,21 @@ struct Bars {
   uint64_t teardown;
   uint32_t tmem_base;
 };
-constexpr int kSmemBytes = OFF_BAR + (int)sizeof(Bars) + 1024;   // + alignment slack
+template <bool F8>
+constexpr int kSmemBytes = Lay<F8>::OFF_BAR + (int)sizeof(BarsT<F8>) + 1024;   // + alignment slack
+static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "shared memory");
+
+// Tensor maps of one launch (bf16 cache: q, k, v; FP8 cache: q and the raw maps).
+struct Maps {
+  CUtensorMap q;     // q_lat rows of 576 bf16, box 64 x 64, 128-byte swizzle
+  CUtensorMap k;     // bf16 pool rows, box 64 x 64, swizzled
+  CUtensorMap v;     // bf16 pool rows, box 64 x 32, swizzled
+  CUtensorMap cs;    // FP8 pool rows of 656 bytes, box 64 B x 64 rows
+  CUtensorMap cv;    // box 64 B x 32 rows
+  CUtensorMap ss;    // box 16 B x 64 rows (the 4 scales of a token)
+  CUtensorMap sv;    // box 16 B x 32 rows
+  CUtensorMap kr;    // box 128 B x 64 rows (bf16 RoPE keys)
+};
 
 struct Params {
   const int32_t* bt;
@@ -152,6 +189,15 @@ __device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_
 #define PROF_STORE(base) ((void)0)
 #endif
 
+// One 16-bit weight (bf16, or f16 with an FP8 cache) -> fp32, exactly.
+template <bool F8>
+__device__ __forceinline__ float p16_to_f32(uint32_t h) {
+  if constexpr (F8)
+    return f16_to_f32(h);
+  else
+    return __uint_as_float(h << 16);
+}
+
 // Sum over the warp's 32 lanes of each of 32 values per lane; lane j returns the sum of
 // value j. Halving exchange: at each step a lane keeps one half of its values, sends the
 // other half to its partner and adds what it receives (31 shuffles in all).
@@ -200,9 +246,17 @@ __device__ __forceinline__ void arrive_even(uint64_t* bar, uint32_t rank) {
     mbar_arrive_remote(mapa(smem_u32(bar), 0));
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const Params prm) {
+template <bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
+    decode_kernel(const __grid_constant__ Maps maps, const Params prm) {
+  using Ly = Lay<F8>;
+  using Bars = BarsT<F8>;
+  constexpr int kNS = Ly::NS, kNV = Ly::NV, kThreads = Ly::THREADS;
+  constexpr int OFF_Q = Ly::OFF_Q, OFF_S = Ly::OFF_S, OFF_V = Ly::OFF_V, OFF_P = Ly::OFF_P;
+  constexpr int OFF_F = Ly::OFF_F, OFF_BAR = Ly::OFF_BAR;
+  const CUtensorMap& tmQ = maps.q;
+  const CUtensorMap& tmK = maps.k;
+  const CUtensorMap& tmV = maps.v;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -268,15 +322,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     // *_ready live in the even CTA: one arrival (its producer registers both CTAs' bytes)
     // plus the bytes of both CTAs' loads, which signal it directly
+    // (FP8 cache: each CTA's converter warps arrive once on the even CTA's s_ready / v_ready
+    // after writing their f16 tile; the raw staging rings are CTA-local)
     mbar_init(&bars->q_ready, 1);
+    mbar_init(&bars->q_conv, 2);
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&bars->s_ready[s], 1);
+      mbar_init(&bars->s_ready[s], F8 ? 2 : 1);
       mbar_init(&bars->s_free[s], 1);
     }
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&bars->v_landed[s], 1);
-      mbar_init(&bars->v_ready[s], 1);
+      mbar_init(&bars->v_ready[s], F8 ? 2 : 1);
       mbar_init(&bars->v_free[s], 1);
+    }
+    for (int s = 0; s < Ly::RS; ++s) {
+      mbar_init(&bars->rs_ready[s], 1);
+      mbar_init(&bars->rs_free[s], 1);
+    }
+    for (int s = 0; s < Ly::RV; ++s) {
+      mbar_init(&bars->rv_ready[s], 1);
+      mbar_init(&bars->rv_free[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -340,13 +405,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto at_even = [&](uint64_t* bar) { return mapa(smem_u32(bar), 0); };
     if (leader) {
       prefetch_tensormap(&tmQ);
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
       const uint64_t pol_q = policy_evict_last();
-      if (even) mbar_arrive_expect_tx(&bars->q_ready, 2 * kKCh * 8192);
-      for (int c = 0; c < kKCh; ++c)
-        tma_load_2d_pair(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
-                         at_even(&bars->q_ready), pol_q);
+      if constexpr (F8) {
+        prefetch_tensormap(&maps.cs);
+        prefetch_tensormap(&maps.ss);
+        prefetch_tensormap(&maps.kr);
+        prefetch_tensormap(&maps.cv);
+        prefetch_tensormap(&maps.sv);
+        // each CTA's converters turn their own Q half into f16: a CTA-local barrier
+        mbar_arrive_expect_tx(&bars->q_ready, kKCh * 8192);
+        for (int c = 0; c < kKCh; ++c)
+          tma_load_2d(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64, &bars->q_ready,
+                      pol_q);
+      } else {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        if (even) mbar_arrive_expect_tx(&bars->q_ready, 2 * kKCh * 8192);
+        for (int c = 0; c < kKCh; ++c)
+          tma_load_2d_pair(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
+                           at_even(&bars->q_ready), pol_q);
+      }
     }
     int s_cnt = 0;
 #ifdef MLA_TC_TRACE
@@ -366,17 +444,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++s_cnt;
       return true;
     };
+    // FP8 cache: raw key chunks (codes + scales of this CTA's 128 tokens, or one page of
+    // bf16 RoPE keys) into the staging ring, for the converter warps
+    int m_cnt = 0;
+    auto load_raw_s = [&](bool rope, int c, int y0, int y1) -> bool {
+      constexpr int RS = Bars::RS;   // >= 1 (the bf16 cache never calls this)
+      const int st = m_cnt % RS;
+      bool r = true;
+      if (m_cnt >= RS) PROF(0, r = wait_bar(&bars->rs_free[st], ((m_cnt / RS) - 1) & 1, cx));
+      if (!r) return false;
+      uint8_t* dst = sm + Ly::OFF_RS + st * kRawS;
+      uint64_t* bar = &bars->rs_ready[st];
+      if (!rope) {
+        mbar_arrive_expect_tx(bar, kRawS);
+        tma_load_2d(dst, &maps.cs, c * 64, y0, bar, pol_s);
+        tma_load_2d(dst + 4096, &maps.cs, c * 64, y1, bar, pol_s);
+        tma_load_2d(dst + 8192, &maps.ss, kC + 2 * kR, y0, bar, pol_s);
+        tma_load_2d(dst + 8192 + 1024, &maps.ss, kC + 2 * kR, y1, bar, pol_s);
+      } else {
+        mbar_arrive_expect_tx(bar, 8192);
+        tma_load_2d(dst, &maps.kr, kC, y0, bar, pol_s);
+      }
+      ++m_cnt;
+      return true;
+    };
     // key chunks of every tile in order (the latent chunks have their own producer)
     bool ok = true;
     for (int k = 0; k < nt && ok; ++k) {
       const int ys0 = page_y(4 * k + 2 * (int)rank);
       const int ys1 = page_y(4 * k + 2 * (int)rank + 1);
-      for (int c = 0; c < kKCh && ok; ++c) {
-        if (leader) {
-          if (c == 4) TRACE(15, k);
-          ok = load_s_chunk(c, ys0, ys1);
+      if constexpr (F8) {
+        for (int c = 0; c < kKCh + 1 && ok; ++c) {   // 8 latent chunks, 2 RoPE half chunks
+          if (leader) ok = c < 8 ? load_raw_s(false, c, ys0, ys1) : load_raw_s(true, 0, c == 8 ? ys0 : ys1, 0);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+      } else {
+        for (int c = 0; c < kKCh && ok; ++c) {
+          if (leader) {
+            if (c == 4) TRACE(15, k);
+            ok = load_s_chunk(c, ys0, ys1);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
       }
     }
 #ifdef MLA_TC_TRACE
@@ -396,7 +505,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // their own issuing thread (warp 12): one thread cannot issue 2-SM MMAs as fast as the
     // tensor pipe retires them, two can.
     if (rank == 0 && lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(256, 128, 0, 0);
+      const uint32_t idS = F8 ? idesc_f16_f32(256, 128, 0, 0) : idesc_bf16_f32(256, 128, 0, 0);
       // operand descriptors; an operand's start moves by adding (byte offset >> 4)
       const uint64_t dS = smem_desc(smem_u32(sm + OFF_S), 16, 1024, kSw128);
       const uint64_t dQ = smem_desc(smem_u32(sm + OFF_Q), 16, 1024, kSw128);
@@ -406,7 +515,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       const long long prof_start = clock64();
 #endif
-      bool ok = wait_bar(&bars->q_ready, 0, cx);
+      // bf16: both CTAs' Q halves have landed; FP8: both have also been converted to f16
+      bool ok = wait_bar(F8 ? &bars->q_conv : &bars->q_ready, 0, cx);
       for (int t = 0; t < nt && ok; ++t) {
         TRACE(22, t);
         // TMEM buffer t % 2 is free once the softmax has read S^T(t-2)
@@ -454,7 +564,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ================================================================ P.V issuer (even CTA)
     // O^T += V^T(t) . P^T(t) for every tile once both CTAs' P^T halves are in place.
     if (rank == 0 && lane == 0) {
-      const uint32_t idPV = idesc_bf16_f32(256, 128, 1, 1);
+      const uint32_t idPV = F8 ? idesc_f16_f32(256, 128, 1, 1) : idesc_bf16_f32(256, 128, 1, 1);
       const uint64_t dV = smem_desc(smem_u32(sm + OFF_V), 4096, 1024, kSw128);
       const uint64_t dP = smem_desc(smem_u32(sm + OFF_P), 8192, 1024, kSw128);
       uint32_t v_st = 0, v_ph = 0;
@@ -549,40 +659,240 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    for (int t = 0; t < nt && ok; ++t) {
-      const bool last = t == nt - 1;
-      for (int v = 0; v < kVCh && ok; ++v, ++v_cnt) {
-        const int st = v_cnt % kNV;
-        // before a slot is reused on the last tile, the chunk that held it must be counted
-        if (last && v >= kNV) ok = finish_last(v - kNV);
-        if (!ok) break;
-        const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;   // whole warp
-        if (lane == 0) {
-          if (v_cnt >= kNV) PROF(0, ok = wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx));
-          if (ok) {
-            if (even) mbar_arrive_expect_tx(&bars->v_ready[st], 2 * 16384);
-            uint32_t bar;
-            if (last) {
-              mbar_arrive_expect_tx(&bars->v_landed[st], 16384);
-              bar = smem_u32(&bars->v_landed[st]);
-            } else {
-              bar = mapa(smem_u32(&bars->v_ready[st]), 0);
+    if constexpr (!F8) {
+      for (int t = 0; t < nt && ok; ++t) {
+        const bool last = t == nt - 1;
+        for (int v = 0; v < kVCh && ok; ++v, ++v_cnt) {
+          const int st = v_cnt % kNV;
+          // before a slot is reused on the last tile, the chunk that held it must be counted
+          if (last && v >= kNV) ok = finish_last(v - kNV);
+          if (!ok) break;
+          const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;   // whole warp
+          if (lane == 0) {
+            if (v_cnt >= kNV) PROF(0, ok = wait_bar(&bars->v_free[st], ((v_cnt / kNV) - 1) & 1, cx));
+            if (ok) {
+              if (even) mbar_arrive_expect_tx(&bars->v_ready[st], 2 * 16384);
+              uint32_t bar;
+              if (last) {
+                mbar_arrive_expect_tx(&bars->v_landed[st], 16384);
+                bar = smem_u32(&bars->v_landed[st]);
+              } else {
+                bar = mapa(smem_u32(&bars->v_ready[st]), 0);
+              }
+              for (int q4 = 0; q4 < 4; ++q4)
+                tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
+                                 (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
+              TRACE(19, v_cnt);
             }
-            for (int q4 = 0; q4 < 4; ++q4)
-              tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
-                               (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
-            TRACE(19, v_cnt);
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (last && ok)
+          for (int v = kVCh - kNV; v < kVCh && ok; ++v) ok = finish_last(v);
       }
-      if (last && ok)
-        for (int v = kVCh - kNV; v < kVCh && ok; ++v) ok = finish_last(v);
+    } else {
+      // FP8 cache: raw codes of this CTA's 256 d_c columns (4 boxes of 64) and the 4 scales
+      // of each of 32 tokens into the staging ring; the converter warp makes the f16 tile
+      int k_cnt = 0;
+      for (int t = 0; t < nt && ok; ++t) {
+        for (int v = 0; v < kVCh && ok; ++v) {
+          const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;   // whole warp
+          if (lane == 0) {
+            const int st = k_cnt % Ly::RV;
+            if (k_cnt >= Ly::RV) ok = wait_bar(&bars->rv_free[st], ((k_cnt / Ly::RV) - 1) & 1, cx);
+            if (ok) {
+              uint8_t* dst = sm + Ly::OFF_RV + st * kRawV;
+              uint64_t* bar = &bars->rv_ready[st];
+              mbar_arrive_expect_tx(bar, kRawV);
+              for (int q4 = 0; q4 < 4; ++q4)
+                tma_load_2d(dst + q4 * 2048, &maps.cv, (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64,
+                            y, bar, pol_v);
+              tma_load_2d(dst + 8192, &maps.sv, kC + 2 * kR, y, bar, pol_v);
+            }
+          }
+          ++k_cnt;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+      }
     }
 #ifdef MLA_TC_TRACE
     prof[7] = clock64() - prof_start;
     if (lane == 0) PROF_STORE(528);
 #endif
+  } else if (warp >= kCvtWarp0) {
+    // ================================================================ FP8 converters
+    // Dequantisation of the FP8 cache, 「Deepseek系列从v3到R易背面经版」 F8量化策略 (per-token
+    // 1x128 groups): value = code * scale of its group, produced here as f16 operand tiles in
+    // the MMA's swizzled layout. Warps 13-14 make the key tiles (and convert this CTA's Q half
+    // and the bf16 RoPE keys to f16 first), warp 15 the latent tiles for P.V, zeroing rows
+    // past the range so that P = 0 never meets stale data.
+    if constexpr (F8) {
+      const int ct = tid - kCvtWarp0 * 32;   // 0..95: warps 13-15
+      // codes (8 per item) x one scale -> 8 f16, stored at 16-byte unit u of row r of a
+      // 128-byte-swizzled tile
+      auto cvt8 = [](uint2 codes, uint32_t sc2) -> uint4 {
+        return make_uint4(mul_f16x2(e4m3x2_to_f16x2(codes.x), sc2),
+                          mul_f16x2(e4m3x2_to_f16x2(codes.x >> 16), sc2),
+                          mul_f16x2(e4m3x2_to_f16x2(codes.y), sc2),
+                          mul_f16x2(e4m3x2_to_f16x2(codes.y >> 16), sc2));
+      };
+      auto bf16x8_to_f16x8 = [](uint4 w) -> uint4 {
+        auto one = [](uint32_t x) {
+          return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+        };
+        return make_uint4(one(w.x), one(w.y), one(w.z), one(w.w));
+      };
+      auto scale2 = [](float sc) -> uint32_t {
+        const uint32_t h = pack_f16x2(sc, sc);
+        return h;
+      };
+      if (ct < 64) {
+        // ---- key tiles (warps 13, 14: 64 threads, named barriers 10 and 11)
+#ifdef MLA_TC_TRACE
+        long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const long long prof_start = clock64();
+#endif
+        bool ok = true;
+        if (ct == 0) ok = wait_bar(&bars->q_ready, 0, cx);
+        ok = bar_and(10, 64, ok);
+        if (ok) {
+          uint4* q = reinterpret_cast<uint4*>(sm + OFF_Q);
+          for (int x = ct; x < kKCh * 8192 / 16; x += 64) q[x] = bf16x8_to_f16x8(q[x]);
+          fence_proxy_async_smem();
+          bar_sync(11, 64);
+          if (ct == 0) arrive_even(&bars->q_conv, rank);
+        }
+        int n = 0, m = 0;   // key-tile count, raw key-chunk count
+        for (int t = 0; t < nt && ok; ++t) {
+          for (int c = 0; c < kKCh && ok; ++c, ++n) {
+            const int st = n % kNS;
+            uint8_t* dst = sm + OFF_S + st * 16384;
+            bool r = true;
+            if (ct == 0 && n >= kNS) PROF(0, r = wait_bar(&bars->s_free[st], ((n / kNS) - 1) & 1, cx));
+            r = bar_and(10, 64, r);
+            for (int h = 0; h < (c < 8 ? 1 : 2) && r; ++h, ++m) {
+              const int rs = m % Ly::RS;
+              if (ct == 0) PROF(1, r = wait_bar(&bars->rs_ready[rs], (m / Ly::RS) & 1, cx));
+              r = bar_and(10, 64, r);
+              if (!r) break;
+              const uint8_t* src = sm + Ly::OFF_RS + rs * kRawS;
+              // Thread = token row: 16-byte loads of the staging row start at a per-row
+              // rotation so the 64- and 128-byte row strides spread over all banks; the
+              // 128-byte swizzle of the tile does the same for the stores.
+              if (c < 8) {
+                // latent dims 64c .. 64c+63 of the CTA's 128 tokens, rows ct and ct + 64
+#pragma unroll
+                for (int r2 = 0; r2 < 2; ++r2) {
+                  const int rr = ct + 64 * r2;
+                  const uint32_t s2 = scale2(*reinterpret_cast<const float*>(src + 8192 + rr * 16 + (c >> 1) * 4));
+                  uint4 in[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    in[j] = *reinterpret_cast<const uint4*>(src + rr * 64 + (((j + rr) & 3) << 4));
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const int u0 = 2 * ((j + rr) & 3);
+                    *reinterpret_cast<uint4*>(dst + rr * 128 + ((u0 ^ (rr & 7)) << 4)) =
+                        cvt8(make_uint2(in[j].x, in[j].y), s2);
+                    *reinterpret_cast<uint4*>(dst + rr * 128 + (((u0 + 1) ^ (rr & 7)) << 4)) =
+                        cvt8(make_uint2(in[j].z, in[j].w), s2);
+                  }
+                }
+              } else {
+                // RoPE keys of page h of the CTA's two: bf16 -> f16, row 64h + ct
+                const int row = 64 * h + ct;
+                uint4 w[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  w[j] = *reinterpret_cast<const uint4*>(src + ct * 128 + (((j + ct) & 7) << 4));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int u = (j + ct) & 7;
+                  *reinterpret_cast<uint4*>(dst + row * 128 + ((u ^ (row & 7)) << 4)) = bf16x8_to_f16x8(w[j]);
+                }
+              }
+              bar_sync(11, 64);   // every thread has read the raw slot
+              if (ct == 0) mbar_arrive(&bars->rs_free[rs]);
+            }
+            ok = r;
+            if (!ok) break;
+            fence_proxy_async_smem();
+            bar_sync(11, 64);
+            if (ct == 0) arrive_even(&bars->s_ready[st], rank);
+          }
+        }
+#ifdef MLA_TC_TRACE
+        prof[7] = clock64() - prof_start;
+        if (ct == 0) PROF_STORE(544);
+#endif
+      } else {
+        // ---- latent tiles for P.V (warp 15)
+        const int cl = ct - 64;   // lane
+#ifdef MLA_TC_TRACE
+        long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const long long prof_start = clock64();
+#endif
+        bool ok = true;
+        int n = 0;   // latent-tile count (= raw latent-chunk count)
+        for (int t = 0; t < nt && ok; ++t) {
+          for (int v = 0; v < kVCh && ok; ++v, ++n) {
+            const int st = n % kNV, rv = n % Ly::RV;
+            if (cl == 0) {
+              if (n >= kNV) PROF(0, ok = wait_bar(&bars->v_free[st], ((n / kNV) - 1) & 1, cx));
+              if (ok) PROF(1, ok = wait_bar(&bars->rv_ready[rv], (n / Ly::RV) & 1, cx));
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const uint8_t* src = sm + Ly::OFF_RV + rv * kRawV;
+            uint8_t* dst = sm + OFF_V + st * 16384;
+            const int tok0 = lo + t * kTile + v * 32;
+#ifdef MLA_TC_TRACE
+            const long long pc0 = clock64();
+#endif
+            // Lane = token row (32 tokens per chunk); rows past the range get zeros. Loads of
+            // the 64-byte staging rows start at a per-row rotation to spread the banks.
+            const int rr = cl;
+            const bool valid = tok0 + rr < hi;
+            const float sca = *reinterpret_cast<const float*>(src + 8192 + rr * 16 + (int)rank * 4);
+            const float scb = *reinterpret_cast<const float*>(src + 8192 + rr * 16 + (2 + (int)rank) * 4);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint32_t s2 = scale2(q4 < 2 ? sca : scb);
+              uint4 in[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                in[j] = *reinterpret_cast<const uint4*>(src + q4 * 2048 + rr * 64 + (((j + rr) & 3) << 4));
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int u0 = 2 * ((j + rr) & 3);
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(dst + q4 * 4096 + rr * 128 + ((u0 ^ (rr & 7)) << 4)) =
+                    valid ? cvt8(make_uint2(in[j].x, in[j].y), s2) : z;
+                *reinterpret_cast<uint4*>(dst + q4 * 4096 + rr * 128 + (((u0 + 1) ^ (rr & 7)) << 4)) =
+                    valid ? cvt8(make_uint2(in[j].z, in[j].w), s2) : z;
+              }
+            }
+#ifdef MLA_TC_TRACE
+            const long long pc1 = clock64();
+            prof[2] += pc1 - pc0;
+#endif
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (cl == 0) {
+              mbar_arrive(&bars->rv_free[rv]);
+              arrive_even(&bars->v_ready[st], rank);
+            }
+#ifdef MLA_TC_TRACE
+            prof[3] += clock64() - pc1;
+#endif
+          }
+        }
+#ifdef MLA_TC_TRACE
+        prof[7] = clock64() - prof_start;
+        if (cl == 0) PROF_STORE(552);
+#endif
+      }
+    }
   } else if (warp == 3) {
     // ================================================================ exchange
     // Fetches the peer's P^T half, flag word and tile maxima once the peer has put them in
@@ -628,11 +938,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int par = t & 1, slot = t & (kXSlots - 1);
-      // ---- reference for tile t, from tile t-2's published maxima (both CTAs)
+      // ---- reference for tile t, from tile t-2's published maxima (both CTAs). One thread
+      // waits on each barrier; the others sleep in the named barrier, so no warp spins.
       bool ok1 = true;
+      if (t >= 2) {
+        if (stid == 0) ok1 = wait_bar(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
+        ok = bar_and(12, 256, ok1);
+        if (!ok) break;
+      }
       if (t >= 2 && stid < kH) {
         const int h = stid;
-        ok1 = wait_bar(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
         const float* rcv = fs + F_RCV + ((t - 2) & (kXSlots - 1)) * kRcvFloats;
         float cand = -CUDART_INF_F;
         if (flags[FL_PUB + par]) cand = fs[F_CMLOC + par * kH + h];
@@ -646,7 +961,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         fs[F_ALPHA + h] = alpha;
       }
-      if (ok1) ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
+      if (stid == 0) ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
       ok = bar_and(1, 256, ok1);
       if (!ok) break;
       if (stid == 0) TRACE(3, t);
@@ -680,14 +995,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bar_sync(3, 256);
         if (stid == 0) mbar_arrive_remote(mapa(smem_u32(&bars->x0_ready), peer));
         bool okx = true;
+        if (stid == 0) okx = wait_bar(&bars->x0_ready, 0, cx);
+        ok = bar_and(13, 256, okx);
+        if (!ok) break;
         if (stid < kH) {
           const int h = stid;
-          okx = wait_bar(&bars->x0_ready, 0, cx);
           fs[F_M + h] = fmaxf(my_max, __ldcg(x0_peer + h));
           fs[F_ALPHA + h] = 1.f;
         }
-        ok = bar_and(4, 256, okx);
-        if (!ok) break;
+        bar_sync(4, 256);
       }
       if (stid == 0) TRACE(4, t);
       // ---- weights p = 2^(s - M) in bf16 (32 heads at a time), the overshoot checks, and
@@ -714,18 +1030,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             float d = (valid ? s[4 * c4 + e] * prm.scale_log2 : -CUDART_INF_F) - m[e];
             over |= d > kLazy;
-            extreme |= d > kRange;
-            d = fminf(d, kRange);
+            extreme |= d > kRange<F8>;
+            d = fminf(d, kRange<F8>);
             p[e] = ex2(d);
           }
-          pk[16 * h2 + 2 * c4] = pack_bf16x2(p[0], p[1]);
-          pk[16 * h2 + 2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
+          pk[16 * h2 + 2 * c4] = F8 ? pack_f16x2(p[0], p[1]) : pack_bf16x2(p[0], p[1]);
+          pk[16 * h2 + 2 * c4 + 1] = F8 ? pack_f16x2(p[2], p[3]) : pack_bf16x2(p[2], p[3]);
         }
         float v[32];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          v[2 * c] = __uint_as_float(pk[16 * h2 + c] << 16);
-          v[2 * c + 1] = __uint_as_float(pk[16 * h2 + c] & 0xFFFF0000u);
+          v[2 * c] = p16_to_f32<F8>(pk[16 * h2 + c] & 0xFFFFu);
+          v[2 * c + 1] = p16_to_f32<F8>(pk[16 * h2 + c] >> 16);
         }
         const float lsum = warp_transpose_sum32(v, lane);
         if (rescale) l_w[h2] *= fs[F_ALPHA + 64 * g + 32 * h2 + lane];
@@ -746,7 +1062,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // P^T's buffer is free, and O is stable to rescale, once P.V of the previous tile is done
       bool ok3 = true;
-      if (t >= 1) ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
+      if (t >= 1 && stid == 0) ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
       bool any_over = false;
       if (bar_or(5, 256, over || !ok3)) {
         ok = bar_and(6, 256, ok3);
@@ -757,7 +1073,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const uint32_t w = pk[c >> 1];
-          const float pv = __uint_as_float((c & 1) ? (w & 0xFFFF0000u) : (w << 16));
+          const float pv = p16_to_f32<F8>((c & 1) ? (w >> 16) : (w & 0xFFFFu));
           const float mx = warp_max_f32(pv);
           if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
         }
@@ -821,7 +1137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       // ------------------------------------------------------------ epilogue
-      ok = wait_bar(&bars->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
+      if (stid == 0) ok = wait_bar(&bars->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
       ok = bar_and(7, 256, ok);
       if (ok) {
         tc_fence_after();
@@ -840,9 +1156,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(sum), peer_l_bar);
         }
         bool ok4 = true;
-        if (stid == 0) mbar_arrive_expect_tx(&bars->l_landed, kH * 4);
-        if (stid < kH) {
+        if (stid == 0) {
+          mbar_arrive_expect_tx(&bars->l_landed, kH * 4);
           ok4 = wait_bar(&bars->l_landed, 0, cx);
+        }
+        ok4 = bar_and(14, 256, ok4);
+        if (ok4 && stid < kH) {
           const int h = stid;
           const float mine = fs[F_LLOC + h], other = fs[F_LRCV + h];
           const float Lsum = rank == 0 ? mine + other : other + mine;
@@ -925,6 +1244,20 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte map over the FP8 pool, rows of `entry` bytes, box_bytes x box_rows boxes, no swizzle.
+static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t entry,
+                        uint32_t box_bytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)entry, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)entry};
+  cuuint32_t box[2] = {box_bytes, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int pick_splits(int B, int n_q, int max_seq_len, int num_splits, int num_sms) {
   if (num_splits > 0) return num_splits;
   const int units = B * n_q;
@@ -940,7 +1273,8 @@ static int pick_splits(int B, int n_q, int max_seq_len, int num_splits, int num_
 
 bool tc_supported(const Dims& d, int n_q) {
   return d.H == tc::kH && d.C == tc::kC && d.R == tc::kR && d.P == tc::kP &&
-         d.act_dtype == MLA_BF16 && d.cache_dtype == MLA_BF16 && n_q >= 1 && n_q <= 2;
+         d.act_dtype == MLA_BF16 && (d.cache_dtype == MLA_BF16 || d.cache_dtype == MLA_FP8_E4M3) &&
+         n_q >= 1 && n_q <= 2;
 }
 
 static size_t partial_bytes(const Dims& d, int B, int n_q, int S) {
@@ -964,16 +1298,33 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, sms);
-  CUtensorMap tmQ, tmK, tmV;
-  if (!tc::make_map(&tmQ, q_lat, (uint64_t)B * n_q * d.H, 64)) return cudaErrorInvalidValue;
-  if (!tc::make_map(&tmK, pool, (uint64_t)num_pages * d.P, 64)) return cudaErrorInvalidValue;
-  if (!tc::make_map(&tmV, pool, (uint64_t)num_pages * d.P, 32)) return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(tc::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
+  const bool f8 = d.cache_dtype == MLA_FP8_E4M3;
+  const uint64_t prow = (uint64_t)num_pages * d.P;
+  tc::Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (!tc::make_map(&maps.q, q_lat, (uint64_t)B * n_q * d.H, 64)) return cudaErrorInvalidValue;
+  if (f8) {
+    const uint32_t eb = (uint32_t)d.entry_bytes;   // 656: codes, bf16 RoPE keys, scales
+    if (!tc::make_map_u8(&maps.cs, pool, prow, eb, 64, 64) ||
+        !tc::make_map_u8(&maps.cv, pool, prow, eb, 64, 32) ||
+        !tc::make_map_u8(&maps.ss, pool, prow, eb, 16, 64) ||
+        !tc::make_map_u8(&maps.sv, pool, prow, eb, 16, 32) ||
+        !tc::make_map_u8(&maps.kr, pool, prow, eb, 128, 64))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!tc::make_map(&maps.k, pool, prow, 64)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&maps.v, pool, prow, 32)) return cudaErrorInvalidValue;
+  }
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[f8]) {
+    cudaError_t e = f8 ? cudaFuncSetAttribute(tc::decode_kernel<true>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              tc::kSmemBytes<true>)
+                       : cudaFuncSetAttribute(tc::decode_kernel<false>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              tc::kSmemBytes<false>);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done[f8] = true;
   }
   const size_t rows = (size_t)B * n_q * d.H;
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
@@ -998,7 +1349,10 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);
 #endif
   const unsigned grid = 2u * (unsigned)(B * n_q * S);
-  tc::decode_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(tmQ, tmK, tmV, prm);
+  if (f8)
+    tc::decode_kernel<true><<<grid, tc::Lay<true>::THREADS, tc::kSmemBytes<true>, stream>>>(maps, prm);
+  else
+    tc::decode_kernel<false><<<grid, tc::Lay<false>::THREADS, tc::kSmemBytes<false>, stream>>>(maps, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return e;
   return launch_combine(d.C, S, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, rows, stream);

@@ -25,6 +25,8 @@ SMALL_FP8 = W.small_v2(3, [129, 64, 70], n_q=2, cache="fp8", seed=12)
 SMALL_BF16_MTP = W.small_v2(3, [2, 100, 191], n_q=2, cache="bf16", seed=13)
 SMALL_BF16_LONG = W.small_v2(4, [700, 257, 1000, 64], n_q=1, cache="bf16", seed=14)
 SMALL_BF16_LONG_MTP = W.small_v2(3, [513, 256, 900], n_q=2, cache="bf16", seed=15)
+SMALL_FP8_LONG = W.small_v2(4, [700, 257, 1000, 64], n_q=1, cache="fp8", seed=17)
+SMALL_FP8_LONG_MTP = W.small_v2(3, [513, 256, 900], n_q=2, cache="fp8", seed=18)
 # 200 query rows: token tiles of the absorb kernels (128 / 64) with a ragged tail
 SMALL_BF16_T200 = W.small_v2(100, [3] * 100, n_q=2, cache="bf16", seed=16)
 TINY = W.config(1)
@@ -124,7 +126,8 @@ def _decode_only(wl, kernel, num_splits=0):
 
 @needs_cuda
 @pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP,
-                                SMALL_BF16_LONG, SMALL_BF16_LONG_MTP],
+                                SMALL_BF16_LONG, SMALL_BF16_LONG_MTP, SMALL_FP8_LONG,
+                                SMALL_FP8_LONG_MTP],
                          ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + f"-L{max(w.seq_lens)}")
 @pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
 def test_decode_latent_attention(wl, kernel):
@@ -134,8 +137,8 @@ def test_decode_latent_attention(wl, kernel):
 @needs_cuda
 @pytest.mark.parametrize("splits", [2, 3, 7])
 @pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
-def test_decode_splits_agree(splits, kernel):
-    wl = SMALL_BF16_LONG
+@pytest.mark.parametrize("wl", [SMALL_BF16_LONG, SMALL_FP8_LONG], ids=["bf16", "fp8"])
+def test_decode_splits_agree(splits, kernel, wl):
     base = _decode_only(wl, kernel, 1)
     other = _decode_only(wl, kernel, splits)
     a = base.step.o_lat.float().cpu().numpy()
@@ -150,13 +153,14 @@ def test_decode_splits_agree(splits, kernel):
 
 @needs_cuda
 def test_tensor_core_kernel_is_selected_for_v2_shapes():
-    for wl in (SMALL_BF16, SMALL_BF16_MTP):
+    for wl in (SMALL_BF16, SMALL_BF16_MTP, SMALL_FP8, SMALL_FP8_LONG):
         assert M.mla_decode_kernel(config_of(wl), wl.B, wl.n_q) == M.MLA_KERNEL_TC
     assert M.mla_decode_kernel(config_of(TINY), TINY.B, 1) == M.MLA_KERNEL_SIMT
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP, SMALL_BF16_LONG],
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP, SMALL_BF16_LONG,
+                                SMALL_FP8_LONG_MTP],
                          ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + f"-L{max(w.seq_lens)}")
 def test_decode_step_end_to_end(wl):
     """append -> absorb -> decode -> unabsorb against the non-absorbed oracle."""
