@@ -12,6 +12,8 @@ reads (sum_b L_b * 1152 B) per second of step time, inputs resident in HBM.
 L2 is flushed (a 2x-L2 buffer write) before every timed step, outside the
 step's events. `e2e` is the same metric through the public API with pinned
 HOST inputs copied in and the output copied back inside the timed region.
+`other_workloads` adds mla_decode timings of the ragged (128 x U[1024, 32768]),
+long-context (8 x 131072) and FP8 two-token (128 x 8192) workloads.
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 workload. With N > 1 each rank runs an independent replica (the path has no
 exchange step), so `scaling` is weak.
@@ -238,6 +240,68 @@ def run_reference(args, world, rank):
     return 0
 
 
+def _other_workloads(M, W, torch, dev, flush, peaks, steps: int = 5):
+    """mla_decode alone on the ragged, long-context and FP8 two-token workloads, device
+    resident, over a pool filled with seeded random latents (their values do not change the
+    work; parity on these workloads is checked by the full-size tests). L2 flushed before
+    each timed call."""
+    out = {}
+    g = torch.Generator(device=dev)
+    for n in (3, 4, 5):
+        wl = W.config(n)
+        g.manual_seed(7800 + n)
+        cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act)
+        eb = M.mla_cache_entry_bytes(cfg)
+        if wl.cache == "fp8":
+            pool = torch.randint(0, 0x76, (wl.num_pages, wl.P, eb), dtype=torch.uint8, device=dev,
+                                 generator=g)
+            scales = torch.full((wl.num_pages, wl.P, wl.C // 128), 2.0 ** -6, device=dev)
+            pool[:, :, wl.C + 2 * wl.R:] = scales.view(torch.uint8).reshape(wl.num_pages, wl.P, -1)
+            krope = torch.randn(wl.num_pages, wl.P, wl.R, device=dev, generator=g).to(torch.bfloat16)
+            pool[:, :, wl.C:wl.C + 2 * wl.R] = krope.view(torch.uint8).reshape(wl.num_pages, wl.P, -1)
+        else:
+            pool = torch.randn(wl.num_pages, wl.P, wl.C + wl.R, device=dev, generator=g).to(
+                torch.bfloat16).view(torch.uint8).reshape(wl.num_pages, wl.P, eb)
+        bt = torch.from_numpy(wl.block_table()).to(dev)
+        sl = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+        T = wl.B * wl.n_q
+        q = (torch.randn(T, wl.H, wl.C + wl.R, device=dev, generator=g) * 0.15).to(torch.bfloat16)
+        o = torch.empty(T, wl.H, wl.C, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(T, wl.H, dtype=torch.float32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        wsz = M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, wl.max_seq_len, 0)
+        ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+
+        def call():
+            M.mla_decode(cfg, q, pool, bt, sl, wl.n_q, wl.max_seq_len, o, lse, ws, 0,
+                         wl.num_pages, st)
+
+        for _ in range(3):
+            call()
+        ts = []
+        for k in range(steps):
+            flush.fill_(float(k))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        cache_bytes, qo_bytes, flops = _workload_sizes(wl)
+        gbs = (cache_bytes + qo_bytes) / (ms * 1e-3) / 1e9
+        tfl = flops / (ms * 1e-3) / 1e12
+        out[wl.name] = {
+            "decode_us": ms * 1e3, "gbs": gbs, "tflops": tfl,
+            "hbm_frac": gbs / peaks["hbm_gbs"], "tensor_frac": tfl / peaks["bf16_tflops"],
+            "kernel": {1: "simt", 2: "tcgen05"}.get(M.mla_decode_kernel(cfg, wl.B, wl.n_q)),
+            "status": int(st.item()),
+        }
+        del pool, q, o, lse, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local_rank):
     import torch
 
@@ -365,6 +429,8 @@ def run_ours(args, world, rank, local_rank):
         "clocks": clk,
         "wall_s_timed": wall,
     }
+    if not args.no_extra:
+        line["other_workloads"] = _other_workloads(M, W, torch, dev, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         v, sample, threads, t = _cpu_oracle_sample(wl, budget_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -385,6 +451,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds-per-step", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decode timings of the ragged, 128K and FP8 workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
