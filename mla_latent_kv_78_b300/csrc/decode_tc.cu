@@ -10,8 +10,11 @@
 //  * A CTA pair (cluster of 2) owns one (sequence, query row, split). Tiles are 256
 //    tokens = 4 pages. Scores are computed transposed, S^T[token][head] = K . Q^T, with a
 //    2-SM MMA (cta_group::2, M = 256 tokens, N = 128 heads): each CTA supplies its 128
-//    tokens' 576-d keys and HALF of Q (its 64 heads), so Q costs 72 KB of shared memory
-//    per SM instead of 144 KB, and every MMA runs at full rate (N = 128).
+//    tokens' 576-d keys and HALF of Q (its 64 heads), and every MMA runs at full rate
+//    (N = 128). With a bf16 cache the Q half is not resident: each [128 tokens x 64 dims]
+//    key chunk is staged together with the matching [64 heads x 64 dims] Q chunk (an L2
+//    hit after the first tile), which leaves shared memory for a 4-deep key ring, a 3-deep
+//    latent ring and two P^T buffers.
 //  * The output is accumulated transposed, O^T[d_c][head] = V^T . P^T, again 2-SM
 //    (M = 256 latent rows per MMA, two MMAs per K step): each CTA holds half of O^T,
 //    256 TMEM columns, which leaves room for a double-buffered S^T (2 x 128 columns).
@@ -81,16 +84,22 @@ constexpr int F_END = F_FLAG + 6;
 // converter warps write f16 operand tiles into the S and V rings.
 template <bool F8>
 struct Lay {
-  static constexpr int NS = F8 ? 2 : 3;     // S-phase ring: [128 tok x 64 dims] 16-bit = 16 KB
-  static constexpr int NV = F8 ? 2 : 4;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
+  // bf16: Q travels with every key chunk (a [64 heads x 64 dims] box read from L2 next to the
+  // [128 tokens x 64 dims] key box), which frees 72 KB for deeper rings and two P^T buffers.
+  // FP8: Q stays resident (the converters turn it into f16 once).
+  static constexpr bool QRES = F8;
+  static constexpr int SSTAGE = QRES ? 16384 : 16384 + 8192;   // S-phase stage bytes
+  static constexpr int NS = F8 ? 2 : 3;     // S-phase ring
+  static constexpr int NV = F8 ? 2 : 5;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
+  static constexpr int PB = F8 ? 1 : 2;     // P^T buffers [256 tok x 64 heads] = 32 KB each
   static constexpr int RS = F8 ? 3 : 0;     // raw key-chunk slots (kRawS bytes)
   static constexpr int RV = F8 ? 2 : 0;     // raw latent-chunk slots (kRawV bytes)
   static constexpr int THREADS = F8 ? 512 : 416;
   static constexpr int OFF_Q = 0;                        // 9 x [64 heads x 64 dims] (8 KB each)
-  static constexpr int OFF_S = OFF_Q + kKCh * 8192;
-  static constexpr int OFF_V = OFF_S + NS * 16384;
-  static constexpr int OFF_P = OFF_V + NV * 16384;       // [256 tok x 64 heads] = 32 KB
-  static constexpr int OFF_RS = OFF_P + 32768;
+  static constexpr int OFF_S = OFF_Q + (QRES ? kKCh * 8192 : 0);
+  static constexpr int OFF_V = OFF_S + NS * SSTAGE;
+  static constexpr int OFF_P = OFF_V + NV * 16384;
+  static constexpr int OFF_RS = OFF_P + PB * 32768;
   static constexpr int OFF_RV = OFF_RS + RS * kRawS;
   static constexpr int OFF_F = OFF_RV + RV * kRawV;      // fp32 scratch
   static constexpr int OFF_BAR = OFF_F + F_END * 4;
@@ -253,6 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   using Bars = BarsT<F8>;
   constexpr int kNS = Ly::NS, kNV = Ly::NV, kThreads = Ly::THREADS;
   constexpr int OFF_Q = Ly::OFF_Q, OFF_S = Ly::OFF_S, OFF_V = Ly::OFF_V, OFF_P = Ly::OFF_P;
+  constexpr int kSStage = Ly::SSTAGE, kPB = Ly::PB;
   constexpr int OFF_F = Ly::OFF_F, OFF_BAR = Ly::OFF_BAR;
   const CUtensorMap& tmQ = maps.q;
   const CUtensorMap& tmK = maps.k;
@@ -420,10 +430,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       } else {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
-        if (even) mbar_arrive_expect_tx(&bars->q_ready, 2 * kKCh * 8192);
-        for (int c = 0; c < kKCh; ++c)
-          tma_load_2d_pair(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64,
-                           at_even(&bars->q_ready), pol_q);
       }
     }
     int s_cnt = 0;
@@ -431,15 +437,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     const long long prof_start = clock64();
 #endif
+    const uint64_t pol_q = policy_evict_last();   // Q chunks are read again every tile
     auto load_s_chunk = [&](int c, int y0, int y1) -> bool {
       const int st = s_cnt % kNS;
       bool r = true;
       if (s_cnt >= kNS) PROF(0, r = wait_bar(&bars->s_free[st], ((s_cnt / kNS) - 1) & 1, cx));
       if (!r) return false;
-      if (even) mbar_arrive_expect_tx(&bars->s_ready[st], 2 * 16384);
+      if (even) mbar_arrive_expect_tx(&bars->s_ready[st], 2 * kSStage);
       const uint32_t bar = at_even(&bars->s_ready[st]);
-      tma_load_2d_pair(sm + OFF_S + st * 16384, &tmK, c * 64, y0, bar, pol_s);
-      tma_load_2d_pair(sm + OFF_S + st * 16384 + 8192, &tmK, c * 64, y1, bar, pol_s);
+      uint8_t* dst = sm + OFF_S + st * kSStage;
+      tma_load_2d_pair(dst, &tmK, c * 64, y0, bar, pol_s);
+      tma_load_2d_pair(dst + 8192, &tmK, c * 64, y1, bar, pol_s);
+      tma_load_2d_pair(dst + 16384, &tmQ, c * 64, row * kH + (int)rank * 64, bar, pol_q);
       TRACE(16, s_cnt);
       ++s_cnt;
       return true;
@@ -508,7 +517,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       const uint32_t idS = F8 ? idesc_f16_f32(256, 128, 0, 0) : idesc_bf16_f32(256, 128, 0, 0);
       // operand descriptors; an operand's start moves by adding (byte offset >> 4)
       const uint64_t dS = smem_desc(smem_u32(sm + OFF_S), 16, 1024, kSw128);
-      const uint64_t dQ = smem_desc(smem_u32(sm + OFF_Q), 16, 1024, kSw128);
+      // bf16: each stage holds its Q chunk after the key chunk; FP8: Q is resident
+      const uint64_t dQ = F8 ? smem_desc(smem_u32(sm + OFF_Q), 16, 1024, kSw128)
+                             : smem_desc(smem_u32(sm + OFF_S + 16384), 16, 1024, kSw128);
       uint32_t s_st = 0, s_ph = 0;
 #ifdef MLA_TC_TRACE
       int s_cnt = 0;
@@ -516,7 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       const long long prof_start = clock64();
 #endif
       // bf16: both CTAs' Q halves have landed; FP8: both have also been converted to f16
-      bool ok = wait_bar(F8 ? &bars->q_conv : &bars->q_ready, 0, cx);
+      bool ok = F8 ? wait_bar(&bars->q_conv, 0, cx) : true;
       for (int t = 0; t < nt && ok; ++t) {
         TRACE(22, t);
         // TMEM buffer t % 2 is free once the softmax has read S^T(t-2)
@@ -531,7 +542,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           TRACE(18, s_cnt);
           PROF(2, tc_fence_after());
           // K chunk c (128 tokens x 64 dims per CTA) . Q chunk c^T, four K=16 steps
-          const uint64_t a0 = dS + s_st * 1024u, b0 = dQ + (uint32_t)c * 512u;
+          const uint64_t a0 = dS + s_st * (uint32_t)(kSStage >> 4);
+          const uint64_t b0 = F8 ? dQ + (uint32_t)c * 512u : dQ + s_st * (uint32_t)(kSStage >> 4);
           PROF(1, {
             mma_bf16_pair(d, a0, b0, idS, c != 0);
             mma_bf16_pair(d, a0 + 2, b0 + 2, idS, 1);
@@ -588,7 +600,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           PROF(5, tc_fence_after());
           // this CTA's 2 x 128 latent rows x 32 tokens (V^T) . P^T rows v of tile t
           const uint64_t a0 = dV + v_st * 1024u;
-          const uint64_t b0 = dP + (uint32_t)v * 256u;
+          const uint64_t b0 = dP + (uint32_t)(t % kPB) * 2048u + (uint32_t)v * 256u;
           const uint32_t acc = (t | v) != 0;
           PROF(4, {
             mma_bf16_pair(tmem + 256, a0, b0, idPV, acc);
@@ -766,7 +778,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         for (int t = 0; t < nt && ok; ++t) {
           for (int c = 0; c < kKCh && ok; ++c, ++n) {
             const int st = n % kNS;
-            uint8_t* dst = sm + OFF_S + st * 16384;
+            uint8_t* dst = sm + OFF_S + st * kSStage;
             bool r = true;
             if (ct == 0 && n >= kNS) PROF(0, r = wait_bar(&bars->s_free[st], ((n / kNS) - 1) & 1, cx));
             r = bar_and(10, 64, r);
@@ -903,12 +915,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       for (int t = 0; t < nt && ok; ++t) {
         const int par = t & 1, slot = t & (kXSlots - 1);
         ok = wait_bar(&bars->x_ready[par], (t >> 1) & 1, cx);
-        // the single P^T buffer is free once P.V of the previous tile has read it
-        if (ok && t >= 1) ok = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
+        // P^T buffer t % kPB is free once P.V of tile t - kPB has read it
+        if (ok && t >= kPB) ok = wait_bar(&bars->o_done[(t - kPB) & 1], ((t - kPB) >> 1) & 1, cx);
         if (!ok) break;
         TRACE(8, t);
         const uint8_t* src = x_slot(peer, slot);
-        bulk_g2s(sm + OFF_P + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
+        bulk_g2s(sm + OFF_P + (t % kPB) * 32768 + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
         bulk_g2s(fs + F_RCV + slot * kRcvFloats, src + kXPBytes, kXBytes - kXPBytes,
                  &bars->p_landed[par]);
         ok = wait_bar(&bars->p_landed[par], (t >> 1) & 1, cx);
@@ -1018,7 +1030,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         if (h2 == 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) arrive_even(&bars->s_empty[par], rank);
+          // (the loads are complete; the arrival publishes nothing, so it need not wait for
+          // this thread's outstanding P^T stores to the exchange ring)
+          if (lane == 0) {
+            if (rank == 0)
+              mbar_arrive(&bars->s_empty[par]);
+            else
+              mbar_arrive_remote_relaxed(mapa(smem_u32(&bars->s_empty[par]), 0));
+          }
           if (stid == 0) TRACE(12, t);
         }
 #pragma unroll
@@ -1060,9 +1079,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_global();
       }
-      // P^T's buffer is free, and O is stable to rescale, once P.V of the previous tile is done
+      // P^T's buffer is free once P.V of tile t - kPB is done; O is stable to rescale once P.V
+      // of the previous tile is
       bool ok3 = true;
-      if (t >= 1 && stid == 0) ok3 = wait_bar(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, cx);
+      {
+        const int wt = rescale ? t - 1 : t - kPB;   // (a rescale needs t >= 2)
+        if (wt >= 0 && stid == 0) ok3 = wait_bar(&bars->o_done[wt & 1], (wt >> 1) & 1, cx);
+      }
       bool any_over = false;
       if (bar_or(5, 256, over || !ok3)) {
         ok = bar_and(6, 256, ok3);
@@ -1117,7 +1140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       // ---- this CTA's own head half of P^T, rows of its tokens
       if (g == (int)rank) {
         const int k = (int)rank * 128 + i;
-        uint8_t* dst = sm + OFF_P + k * 128;
+        uint8_t* dst = sm + OFF_P + (t % kPB) * 32768 + k * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =

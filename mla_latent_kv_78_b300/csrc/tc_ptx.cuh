@@ -33,6 +33,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // Arrive on a barrier in another CTA of the cluster (address from mapa).
+// Arrive on a barrier in another CTA without release semantics: for signals that publish no
+// memory writes (e.g. "this thread has finished reading TMEM", after tcgen05.wait::ld), so
+// the arrival need not wait for the thread's earlier stores to become visible.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
