@@ -56,7 +56,7 @@ constexpr int kXSlots = 4;                      // exchange slots per CTA: tile 
 constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
 constexpr uint32_t kXHdrBytes = 16;             // flag word (1: the tile's maxima follow) + pad
 constexpr uint32_t kXBytes = kXPBytes + kXHdrBytes + kH * 4;   // + that tile's per-head maxima
-constexpr size_t kXUnitBytes = 2 * kXSlots * (size_t)kXBytes + 2 * kH * 4;  // per (seq, row, split)
+constexpr size_t kXUnitBytes = 2 * kXSlots * (size_t)kXBytes;   // per (seq, row, split)
 constexpr float kLazy = 8.f;    // log2 units a score may exceed the reference before it moves
 // Larger excesses are clamped and flagged (MLA_DEV_SCORE_RANGE): bf16 P holds 2^96, f16 P
 // (FP8 cache) 2^15.
@@ -74,7 +74,8 @@ constexpr int F_ALPHA = F_M + 128;   // [128]
 constexpr int F_LLOC = F_ALPHA + 128;  // [128]
 constexpr int F_LRCV = F_LLOC + 128;   // [128]
 constexpr int F_INV = F_LRCV + 128;    // [128]
-constexpr int F_FLAG = F_INV + 128;    // ints, see FL_*
+constexpr int F_X0 = F_INV + 128;     // [128] the peer's tile-0 per-head maxima
+constexpr int F_FLAG = F_X0 + 128;    // ints, see FL_*
 constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for this tile
 constexpr int FL_ABORT = 2;    // a bounded wait gave up
 constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
@@ -317,15 +318,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     return;
   }
 
-  // exchange area of this unit: [rank][slot] {P^T 16 KB, flag word, maxima 512 B}, then [rank]
-  // tile-0 maxima
+  // exchange area of this unit: [rank][slot] {P^T 16 KB, flag word, maxima 512 B}
   uint8_t* xunit = prm.xws + (size_t)unit * kXUnitBytes;
   auto x_slot = [&](uint32_t r, int slot) {
     return xunit + (size_t)(r * kXSlots + slot) * kXBytes;
   };
-  float* x0_mine = reinterpret_cast<float*>(xunit + 2 * kXSlots * (size_t)kXBytes + rank * kH * 4);
-  const float* x0_peer =
-      reinterpret_cast<const float*>(xunit + 2 * kXSlots * (size_t)kXBytes + peer * kH * 4);
 
   // ---- set-up
   if (tid == 0) TRACE(11, 0);
@@ -645,10 +642,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     const long long prof_start = clock64();
 #endif
+    // Chunks of the last tile that hold rows past the range (a suffix from v_part on) land on
+    // this CTA's own barrier first; the others go straight to the even CTA's barrier.
+    const int base_last = (nt - 1) * kVCh;   // chunk count before the last tile
+    int v_part = kVCh;
+    for (int v = kVCh - 1; v >= 0; --v)
+      if (lo + (nt - 1) * kTile + v * 32 + 32 > hi) v_part = v;
+    auto landing = [&](int v) { return v >= v_part; };
     auto finish_last = [&](int v) -> bool {   // zero + count chunk v of the last tile
-      const int base = (nt - 1) * kVCh;       // chunk count before the last tile
-      const int st = (base + v) % kNV;
-      const int first = (st - base % kNV + kNV) % kNV;   // the last tile's first chunk in slot st
+      const int st = (base_last + v) % kNV;
+      // the first landing chunk in slot st, and so the phase of v_landed[st] for chunk v
+      const int first = v_part + ((st - (base_last + v_part)) % kNV + kNV) % kNV;
       bool r = true;
       if (lane == 0) r = wait_bar(&bars->v_landed[st], ((v - first) / kNV) & 1, cx);
       if (!__shfl_sync(0xffffffffu, r, 0)) return false;
@@ -677,7 +681,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         for (int v = 0; v < kVCh && ok; ++v, ++v_cnt) {
           const int st = v_cnt % kNV;
           // before a slot is reused on the last tile, the chunk that held it must be counted
-          if (last && v >= kNV) ok = finish_last(v - kNV);
+          if (last && v >= kNV && landing(v - kNV)) ok = finish_last(v - kNV);
           if (!ok) break;
           const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;   // whole warp
           if (lane == 0) {
@@ -685,7 +689,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
             if (ok) {
               if (even) mbar_arrive_expect_tx(&bars->v_ready[st], 2 * 16384);
               uint32_t bar;
-              if (last) {
+              if (last && landing(v)) {
                 mbar_arrive_expect_tx(&bars->v_landed[st], 16384);
                 bar = smem_u32(&bars->v_landed[st]);
               } else {
@@ -700,7 +704,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
         if (last && ok)
-          for (int v = kVCh - kNV; v < kVCh && ok; ++v) ok = finish_last(v);
+          for (int v = max(kVCh - kNV, 0); v < kVCh && ok; ++v)
+            if (landing(v)) ok = finish_last(v);
       }
     } else {
       // FP8 cache: raw codes of this CTA's 256 d_c columns (4 boxes of 64) and the 4 scales
@@ -996,23 +1001,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           }
         }
         bar_sync(2, 256);
+        // this CTA's per-head maxima go straight into the peer's shared memory (st.async,
+        // counted on the peer's x0_ready), the peer's arrive the same way
         float my_max = -CUDART_INF_F;
         if (stid < kH) {
           const int h = stid, gg = h >> 6, cc = h & 63;
 #pragma unroll
           for (int q = 0; q < 4; ++q) my_max = fmaxf(my_max, fs[F_COL + (gg * 4 + q) * 64 + cc]);
-          x0_mine[h] = my_max;
-          __threadfence();
+          st_async_b32(mapa(smem_u32(fs + F_X0 + h), peer), __float_as_uint(my_max),
+                       mapa(smem_u32(&bars->x0_ready), peer));
         }
-        bar_sync(3, 256);
-        if (stid == 0) mbar_arrive_remote(mapa(smem_u32(&bars->x0_ready), peer));
         bool okx = true;
-        if (stid == 0) okx = wait_bar(&bars->x0_ready, 0, cx);
+        if (stid == 0) {
+          mbar_arrive_expect_tx(&bars->x0_ready, kH * 4);
+          okx = wait_bar(&bars->x0_ready, 0, cx);
+        }
         ok = bar_and(13, 256, okx);
         if (!ok) break;
         if (stid < kH) {
           const int h = stid;
-          fs[F_M + h] = fmaxf(my_max, __ldcg(x0_peer + h));
+          fs[F_M + h] = fmaxf(my_max, fs[F_X0 + h]);
           fs[F_ALPHA + h] = 1.f;
         }
         bar_sync(4, 256);
