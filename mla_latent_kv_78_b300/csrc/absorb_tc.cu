@@ -50,39 +50,24 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int
   return true;
 }
 
-// cos/sin of pos * theta without fp64: the angle is carried as a float pair (exact product of
-// the integer position with theta_hi via FMA, plus pos * theta_lo), reduced by 2*pi with a
-// three-part Cody-Waite split (6.28125 + 0.0019350051879882812 + 3.0199160e-07; the first two
-// products are exact for |n| < 2^15, i.e. positions up to ~2e5), then evaluated with sincosf.
-__device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float* c, float* s) {
-  const float p = (float)pos;
-  const float a_hi = p * th_hi;
-  const float a_lo = fmaf(p, th_hi, -a_hi) + p * th_lo;
-  const float n = rintf(a_hi * 0.15915493667125702f);
-  float r = fmaf(-n, 6.28125f, a_hi);
-  r = fmaf(-n, 0.0019350051879882812f, r);
-  r = fmaf(-n, 3.019916050561733e-07f, r);
-  r += a_lo;
-  sincosf(r, s, c);
-}
-
 // ------------------------------------------------------------------ absorb
-// D[token][c] = q_c[token] . W_UK[i][:, c]: M = 128 tokens (TMEM lane = token), N = 2 x 256
-// latent columns, K = 128. A = q_c tile, 2 boxes [128 t x 64 d] (K-major);
-// B = W_UK[i] as 8 boxes [128 d x 64 c] (MN-major: latent columns contiguous).
+// D[token][c] = q_c[token] . W_UK[i][:, c] for one half (256) of the latent columns per CTA:
+// M = 128 tokens (TMEM lane = token), N = 256, K = 128. A = q_c tile, 2 boxes [128 t x 64 d]
+// (K-major); B = the half of W_UK[i] as 4 boxes [128 d x 64 c] (MN-major). Two CTAs per head
+// (and two per SM) keep enough weight bytes in flight; the first also rotates q^R.
 constexpr int kAbsNT = 128;
-constexpr int kAbsSmem = 2 * 16384 + 8 * 16384 + 64 + 1024;
+constexpr int kAbsSmem = 2 * 16384 + 4 * 16384 + 64 + 1024;
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, 2)
     absorb_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
                      const AbsorbParams p) {
   extern __shared__ __align__(1024) uint8_t raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = sm;                 // q_c
-  uint8_t* sB = sm + 2 * 16384;     // W_UK[i]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 8 * 16384);   // [0] loads, [1] mma
+  uint8_t* sB = sm + 2 * 16384;     // this CTA's half of W_UK[i]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 4 * 16384);   // [0] loads, [1] mma
   uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
-  const int i = blockIdx.x, t0 = blockIdx.y * kAbsNT;
+  const int i = blockIdx.x, half = blockIdx.y, t0 = blockIdx.z * kAbsNT;
   const int nt = min(kAbsNT, p.T - t0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -91,7 +76,7 @@ __global__ void __launch_bounds__(128, 1)
     fence_mbarrier_init_cluster();
   }
   if (warp == 0) {
-    tmem_alloc(slot, 512);
+    tmem_alloc(slot, 256);
     tmem_relinquish();
   }
   __syncthreads();
@@ -99,27 +84,27 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = *slot;
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(&bars[0], 10 * 16384);
+    mbar_arrive_expect_tx(&bars[0], 6 * 16384);
     for (int kb = 0; kb < 2; ++kb) tma_load_3d(sA + kb * 16384, &tmQ, kb * 64, i, t0, &bars[0], pol);
-    for (int j = 0; j < 8; ++j) tma_load_2d(sB + j * 16384, &tmW, j * 64, i * kD, &bars[0], pol);
+    for (int j = 0; j < 4; ++j)
+      tma_load_2d(sB + j * 16384, &tmW, (4 * half + j) * 64, i * kD, &bars[0], pol);
     if (wait_bounded(&bars[0], 0, p.status)) {
       tc_fence_after();
       const uint32_t id = idesc_bf16_f32(128, 256, 0, 1);
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-      for (int n = 0; n < 2; ++n)
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSw128);
-          const uint64_t b = smem_desc(b0 + n * 4 * 16384 + kk * 2048, 16384, 1024, kSw128);
-          mma_bf16(tmem + n * 256, a, b, id, kk > 0);
-        }
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t a = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSw128);
+        const uint64_t b = smem_desc(b0 + kk * 2048, 16384, 1024, kSw128);
+        mma_bf16(tmem, a, b, id, kk > 0);
+      }
     }
     mma_commit(&bars[1]);
   }
-  // this thread's token: RoPE part while the MMAs run
+  // this thread's token: RoPE part while the MMAs run (first half's CTA)
   const int t = warp * 32 + lane;
   const bool valid = t < nt;
   const size_t row = ((size_t)(t0 + t) * p.H + i);
-  if (valid) {
+  if (valid && half == 0) {
     const int pos = p.pos[t0 + t];
     const uint4* src = reinterpret_cast<const uint4*>(p.q_r + row * kR);
     uint4* dst = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + kC);
@@ -142,9 +127,9 @@ __global__ void __launch_bounds__(128, 1)
   wait_bounded(&bars[1], 0, p.status);
   tc_fence_after();
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  uint4* out = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR));
+  uint4* out = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + half * 256);
 #pragma unroll 1
-  for (int cc = 0; cc < kC / 32; ++cc) {
+  for (int cc = 0; cc < 256 / 32; ++cc) {
     float v[32];
     tmem_ld32(lane_base + cc * 32, v);
     tmem_ld_wait();
@@ -157,7 +142,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ------------------------------------------------------------------ unabsorb
@@ -265,7 +250,7 @@ cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, co
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(d.H, (T + tca::kAbsNT - 1) / tca::kAbsNT);
+  dim3 grid(d.H, 2, (T + tca::kAbsNT - 1) / tca::kAbsNT);
   tca::absorb_tc_kernel<<<grid, 128, tca::kAbsSmem, stream>>>(tmW, tmQ, p);
   return cudaGetLastError();
 }

@@ -4,13 +4,44 @@
 // is cached beside it. 「Deepseek系列从v3到R易背面经版」 F8量化策略: activations are
 // quantised per token in 1x128 groups, E4M3.
 //
-// One warp per token. The page/slot mapping is integer-exact; RoPE runs in fp64
-// and is rounded once to the cache type; the FP8 scale and the per-element
-// division are IEEE fp32 (__fdiv_rn), so the integer codes match a CPU encoder
-// that takes the same fp32 decisions.
+// One warp per token. The page/slot mapping is integer-exact; RoPE frequencies come from the
+// host in fp64; the rotation runs in fp64 for an fp32 cache and in fp32 with a double-float
+// angle reduction for bf16 / FP8 caches (both far below one ulp of the stored type), rounded
+// once; the FP8 scale and the per-element division are IEEE fp32 (__fdiv_rn), so the integer
+// codes match a CPU encoder that takes the same fp32 decisions.
 #include "mla_internal.cuh"
 
 namespace mla {
+
+// rotated pair k of one token: (x0, x1) -> (x0 c - x1 s, x0 s + x1 c). bf16 and FP8 caches
+// keep k^R in bf16, so fp32 with a double-float angle reduction is exact to well below one
+// bf16 ulp; the fp32 cache uses fp64 (fp32 accuracy is what it stores).
+template <int CACHE>
+__device__ __forceinline__ void rope_pair(const RopeTable& rt, int pos, int k, int R, double base,
+                                          float x0, float x1, float* y0, float* y1) {
+  if constexpr (CACHE == MLA_F32) {
+    double cs, sn;
+    if (k < kMaxRopePairs) {
+      sincos((double)pos * rt.th[k], &sn, &cs);
+    } else {
+      rope_cos_sin(pos, k, R, base, &cs, &sn);
+    }
+    *y0 = (float)((double)x0 * cs - (double)x1 * sn);
+    *y1 = (float)((double)x0 * sn + (double)x1 * cs);
+  } else {
+    float cs, sn;
+    if (k < kMaxRopePairs) {
+      rope_cs(pos, rt.hi[k], rt.lo[k], &cs, &sn);
+      *y0 = x0 * cs - x1 * sn;
+      *y1 = x0 * sn + x1 * cs;
+    } else {
+      double c2, s2;
+      rope_cos_sin(pos, k, R, base, &c2, &s2);
+      *y0 = (float)((double)x0 * c2 - (double)x1 * s2);
+      *y1 = (float)((double)x0 * s2 + (double)x1 * c2);
+    }
+  }
+}
 
 template <typename In, int CACHE>
 __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restrict__ c_kv,
@@ -20,10 +51,12 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restric
                                                      const int32_t* __restrict__ bt, int batch,
                                                      int maxp, int num_pages,
                                                      uint8_t* __restrict__ pool,
-                                                     int32_t* status) {
+                                                     int32_t* status, const RopeTable rt) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
+  const In* src_c = c_kv + (size_t)t * d.C;
+  const In* src_r = k_r + (size_t)t * d.R;
   const int b = seq_idx[t];
   const int p = pos[t];
   if (b < 0 || b >= batch || p < 0 || p / d.P >= maxp) {
@@ -36,19 +69,24 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restric
     return;
   }
   uint8_t* dst = pool + ((size_t)page * d.P + (p % d.P)) * (size_t)d.entry_bytes;
-  const In* src_c = c_kv + (size_t)t * d.C;
-  const In* src_r = k_r + (size_t)t * d.R;
   const double base = (double)d.rope_base;
 
   if constexpr (CACHE != MLA_FP8_E4M3) {
     In* out = reinterpret_cast<In*>(dst);
-    for (int k = lane; k < d.C; k += 32) out[k] = src_c[k];
+    // the latent row: 16-byte vectors when the row and both ends are 16-byte aligned
+    const size_t row_bytes = (size_t)d.C * sizeof(In);
+    if ((row_bytes & 15) == 0 && ((reinterpret_cast<uintptr_t>(src_c) | reinterpret_cast<uintptr_t>(out)) & 15) == 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src_c);
+      uint4* o4 = reinterpret_cast<uint4*>(out);
+      for (int k = lane; k < (int)(row_bytes / 16); k += 32) o4[k] = s4[k];
+    } else {
+      for (int k = lane; k < d.C; k += 32) out[k] = src_c[k];
+    }
     for (int k = lane; k < d.R / 2; k += 32) {
-      double cs, sn;
-      rope_cos_sin(p, k, d.R, base, &cs, &sn);
-      const double x0 = (double)ld_act(src_r, 2 * k), x1 = (double)ld_act(src_r, 2 * k + 1);
-      st_act(out, d.C + 2 * k, (float)(x0 * cs - x1 * sn));
-      st_act(out, d.C + 2 * k + 1, (float)(x0 * sn + x1 * cs));
+      float y0, y1;
+      rope_pair<CACHE>(rt, p, k, d.R, base, ld_act(src_r, 2 * k), ld_act(src_r, 2 * k + 1), &y0, &y1);
+      st_act(out, d.C + 2 * k, y0);
+      st_act(out, d.C + 2 * k + 1, y1);
     }
   } else {
     uint8_t* codes = dst;
@@ -73,11 +111,10 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restric
       if (lane == 0) scales[g] = s;
     }
     for (int k = lane; k < d.R / 2; k += 32) {
-      double cs, sn;
-      rope_cos_sin(p, k, d.R, base, &cs, &sn);
-      const double x0 = (double)ld_act(src_r, 2 * k), x1 = (double)ld_act(src_r, 2 * k + 1);
-      kr[2 * k] = __float2bfloat16_rn((float)(x0 * cs - x1 * sn));
-      kr[2 * k + 1] = __float2bfloat16_rn((float)(x0 * sn + x1 * cs));
+      float y0, y1;
+      rope_pair<CACHE>(rt, p, k, d.R, base, ld_act(src_r, 2 * k), ld_act(src_r, 2 * k + 1), &y0, &y1);
+      kr[2 * k] = __float2bfloat16_rn(y0);
+      kr[2 * k + 1] = __float2bfloat16_rn(y1);
     }
   }
 }
@@ -88,21 +125,23 @@ cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, cons
   const int threads = 128;
   const int blocks = (T * 32 + threads - 1) / threads;
   uint8_t* out = static_cast<uint8_t*>(pool);
+  RopeTable rt;
+  fill_rope_table(&rt, d.R, (double)d.rope_base);
   switch (d.cache_dtype) {
     case MLA_F32:
       append_kernel<float, MLA_F32><<<blocks, threads, 0, stream>>>(
           d, (const float*)c_kv, (const float*)k_r, seq_idx, pos, T, bt, batch, maxp, num_pages,
-          out, status);
+          out, status, rt);
       break;
     case MLA_BF16:
       append_kernel<__nv_bfloat16, MLA_BF16><<<blocks, threads, 0, stream>>>(
           d, (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_r, seq_idx, pos, T, bt, batch,
-          maxp, num_pages, out, status);
+          maxp, num_pages, out, status, rt);
       break;
     default:
       append_kernel<__nv_bfloat16, MLA_FP8_E4M3><<<blocks, threads, 0, stream>>>(
           d, (const __nv_bfloat16*)c_kv, (const __nv_bfloat16*)k_r, seq_idx, pos, T, bt, batch,
-          maxp, num_pages, out, status);
+          maxp, num_pages, out, status, rt);
       break;
   }
   return cudaGetLastError();

@@ -42,6 +42,39 @@ __device__ __forceinline__ void rope_cos_sin(int pos, int k, int R, double base,
   sincos((double)pos * theta, s, c);
 }
 
+// RoPE frequencies theta_k = base^(-2k/R), computed on the host in fp64 and passed as a
+// float pair (hi + lo) and as a double.
+constexpr int kMaxRopePairs = 64;
+struct RopeTable {
+  float hi[kMaxRopePairs], lo[kMaxRopePairs];
+  double th[kMaxRopePairs];
+};
+
+inline void fill_rope_table(RopeTable* t, int R, double base) {
+  for (int k = 0; k < R / 2 && k < kMaxRopePairs; ++k) {
+    const double th = pow(base, -2.0 * (double)k / (double)R);
+    t->th[k] = th;
+    t->hi[k] = (float)th;
+    t->lo[k] = (float)(th - (double)t->hi[k]);
+  }
+}
+
+// cos/sin of pos * theta without fp64: the angle is carried as a float pair (exact product of
+// the integer position with theta_hi via FMA, plus pos * theta_lo), reduced by 2*pi with a
+// three-part Cody-Waite split (6.28125 + 0.0019350051879882812 + 3.0199160e-07; the first two
+// products are exact for |n| < 2^15, i.e. positions up to ~2e5), then evaluated with sincosf.
+__device__ __forceinline__ void rope_cs(int pos, float th_hi, float th_lo, float* c, float* s) {
+  const float p = (float)pos;
+  const float a_hi = p * th_hi;
+  const float a_lo = fmaf(p, th_hi, -a_hi) + p * th_lo;
+  const float n = rintf(a_hi * 0.15915493667125702f);
+  float r = fmaf(-n, 6.28125f, a_hi);
+  r = fmaf(-n, 0.0019350051879882812f, r);
+  r = fmaf(-n, 3.019916050561733e-07f, r);
+  r += a_lo;
+  sincosf(r, s, c);
+}
+
 // E4M3 encode of one fp32 value: round to nearest even, saturate to +-448.
 __device__ __forceinline__ uint8_t e4m3_encode(float x) {
   __nv_fp8_storage_t v = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
