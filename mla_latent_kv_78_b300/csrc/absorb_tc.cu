@@ -4,13 +4,14 @@
 // 「一文通透DeepSeek-V2」 §2.2.1 (last paragraph): W^{UK} is absorbed into the query side and
 // W^{UV} into the output side. Per head i these are small GEMMs whose cost is reading the
 // head's 128 KB weight block once:
-//   absorb:   q_lat[t][i][0:512]  = q_c[t][i][:] . W_UK[i]      (D = W_UK[i]^T . q_c^T: M = 512 latent
-//             rows in four 128-row tiles, N = tokens, K = 128; W_UK[i] is the MN-major A operand)
-//             q_lat[t][i][512:576] = RoPE_pos[t](q_r[t][i])
+//   absorb:   q_lat[t][i][0:512]  = q_c[t][i][:] . W_UK[i]      (D = q_c . W_UK[i] per half of
+//             the latent columns: M = 128 tokens, N = 256, K = 128; W_UK[i] is the MN-major B
+//             operand), q_lat[t][i][512:576] = RoPE_pos[t](q_r[t][i])
 //   unabsorb: o[t][i][0:128]      = W_UV[i] . o_lat[t][i][:]    (D = W_UV[i] . o_lat^T: M = 128,
 //             N = tokens, K = 512)
-// Operands arrive by TMA (128-byte swizzle), the MMAs are tcgen05 kind::f16 with fp32 TMEM
-// accumulators, and the epilogue reads TMEM lane = output column.
+// Operands arrive by TMA (128-byte swizzle) and the MMAs are tcgen05 kind::f16 with fp32 TMEM
+// accumulators. The absorb epilogue (TMEM lane = token) stages q_lat rows in shared memory for
+// TMA stores; the unabsorb epilogue (TMEM lane = output column) stores straight from registers.
 #include "mla_internal.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
@@ -60,7 +61,7 @@ constexpr int kAbsSmem = 2 * 16384 + 4 * 16384 + 64 + 1024;
 
 __global__ void __launch_bounds__(128, 2)
     absorb_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmQ,
-                     const AbsorbParams p) {
+                     const __grid_constant__ CUtensorMap tmL, const AbsorbParams p) {
   extern __shared__ __align__(1024) uint8_t raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = sm;                 // q_c
@@ -82,12 +83,25 @@ __global__ void __launch_bounds__(128, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
+  const int t = warp * 32 + lane;   // this thread's token (TMEM lane) in the tile
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
     mbar_arrive_expect_tx(&bars[0], 6 * 16384);
     for (int kb = 0; kb < 2; ++kb) tma_load_3d(sA + kb * 16384, &tmQ, kb * 64, i, t0, &bars[0], pol);
     for (int j = 0; j < 4; ++j)
       tma_load_2d(sB + j * 16384, &tmW, (4 * half + j) * 64, i * kD, &bars[0], pol);
+  }
+  // the first half's CTA also rotates q^R: fetch this token's row while the operands land
+  uint4 xr[kR / 8];
+  int pos = 0;
+  if (half == 0) {
+    const bool valid = t < nt;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q_r + ((size_t)(t0 + t) * p.H + i) * kR);
+#pragma unroll
+    for (int q = 0; q < kR / 8; ++q) xr[q] = valid ? src[q] : make_uint4(0, 0, 0, 0);
+    pos = valid ? p.pos[t0 + t] : 0;
+  }
+  if (threadIdx.x == 0) {
     if (wait_bounded(&bars[0], 0, p.status)) {
       tc_fence_after();
       const uint32_t id = idesc_bf16_f32(128, 256, 0, 1);
@@ -100,17 +114,17 @@ __global__ void __launch_bounds__(128, 2)
     }
     mma_commit(&bars[1]);
   }
-  // this thread's token: RoPE part while the MMAs run (first half's CTA)
-  const int t = warp * 32 + lane;
-  const bool valid = t < nt;
-  const size_t row = ((size_t)(t0 + t) * p.H + i);
-  if (valid && half == 0) {
-    const int pos = p.pos[t0 + t];
-    const uint4* src = reinterpret_cast<const uint4*>(p.q_r + row * kR);
-    uint4* dst = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + kC);
-#pragma unroll
+  wait_bounded(&bars[1], 0, p.status);
+  tc_fence_after();
+  // The MMAs have read both operand buffers: each thread writes its token's row into them as
+  // 128-byte-swizzled boxes [128 tokens x 64 columns] (the W half's buffer takes the 256 latent
+  // columns, q_c's the 64 rotated ones), and TMA stores whole 128-byte row segments of q_lat.
+  const uint32_t rsw = (uint32_t)(t & 7);
+  if (half == 0) {
+    uint8_t* rowp = sA + t * 128;
+#pragma unroll 1
     for (int q = 0; q < kR / 8; ++q) {
-      const uint4 x = src[q];
+      const uint4 x = xr[q];
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
       uint32_t o[4];
 #pragma unroll
@@ -121,34 +135,43 @@ __global__ void __launch_bounds__(128, 2)
         const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
         o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
       }
-      dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(rowp + ((uint32_t)q ^ rsw) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
-  wait_bounded(&bars[1], 0, p.status);
-  tc_fence_after();
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  uint4* out = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + half * 256);
 #pragma unroll 1
-  for (int cc = 0; cc < 256 / 32; ++cc) {
-    float v[32];
-    tmem_ld32(lane_base + cc * 32, v);
+  for (int cc = 0; cc < 256 / 64; ++cc) {
+    float v[64];
+    tmem_ld32(lane_base + cc * 64, v);
+    tmem_ld32(lane_base + cc * 64 + 32, v + 32);
     tmem_ld_wait();
-    if (valid) {
+    uint8_t* rowp = sB + cc * 16384 + t * 128;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        out[cc * 4 + q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                     pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    for (int q = 0; q < 8; ++q) {
+      *reinterpret_cast<uint4*>(rowp + ((uint32_t)q ^ rsw) * 16) =
+          make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                     pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     }
   }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < 4; ++j) tma_store_3d(&tmL, sB + j * 16384, half * 256 + j * 64, i, t0);
+    if (half == 0) tma_store_3d(&tmL, sA, kC, i, t0);
+    bulk_commit_group();
+    bulk_wait_read_all();
+  }
+  __syncwarp();
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ------------------------------------------------------------------ unabsorb
 // smem: A = W_UV[i] as 8 boxes [128 r x 64 c] (16 KB) | B = o_lat tile as 8 boxes [64 t x 64 c]
+// (8 KB). Box pair j (64 latent columns) has its own barrier, so the MMAs of K-slice j start
+// as soon as it lands while later slices are still in flight.
 constexpr int kUnNT = 64;
-constexpr int kUnSmem = 8 * 16384 + 8 * 8192 + 64 + 1024;
+constexpr int kUnSmem = 8 * 16384 + 8 * 8192 + 128 + 1024;
 
 __global__ void __launch_bounds__(128, 1)
     unabsorb_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmO,
@@ -157,14 +180,13 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = sm;
   uint8_t* sB = sm + 8 * 16384;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 8 * 8192);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 8 * 8192);   // [0..7] slices, [8] mma
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 9);
   const int i = blockIdx.x, t0 = blockIdx.y * kUnNT;
   const int nt = min(kUnNT, p.T - t0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int j = 0; j < 9; ++j) mbar_init(&bars[j], 1);
     fence_mbarrier_init_cluster();
   }
   if (warp == 0) {
@@ -176,35 +198,35 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = *slot;
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(&bars[0], 8 * 16384 + 8 * 8192);
-    for (int j = 0; j < 8; ++j) tma_load_2d(sA + j * 16384, &tmW, j * 64, i * kD, &bars[0], pol);
-    for (int j = 0; j < 8; ++j) tma_load_3d(sB + j * 8192, &tmO, j * 64, i, t0, &bars[0], pol);
-    if (wait_bounded(&bars[0], 0, p.status)) {
+    for (int j = 0; j < 8; ++j) {
+      mbar_arrive_expect_tx(&bars[j], 16384 + 8192);
+      tma_load_2d(sA + j * 16384, &tmW, j * 64, i * kD, &bars[j], pol);
+      tma_load_3d(sB + j * 8192, &tmO, j * 64, i, t0, &bars[j], pol);
+    }
+    const uint32_t id = idesc_bf16_f32(128, kUnNT, 0, 0);
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+    for (int j = 0; j < 8; ++j) {
+      if (!wait_bounded(&bars[j], 0, p.status)) break;
       tc_fence_after();
-      const uint32_t id = idesc_bf16_f32(128, kUnNT, 0, 0);
-      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-      for (int kk = 0; kk < 32; ++kk) {
-        const uint64_t a = smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSw128);
-        const uint64_t b = smem_desc(b0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSw128);
-        mma_bf16(tmem, a, b, id, kk > 0);
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t a = smem_desc(a0 + j * 16384 + k * 32, 16, 1024, kSw128);
+        const uint64_t b = smem_desc(b0 + j * 8192 + k * 32, 16, 1024, kSw128);
+        mma_bf16(tmem, a, b, id, (j | k) != 0);
       }
     }
-    mma_commit(&bars[1]);
+    mma_commit(&bars[8]);
   }
-  wait_bounded(&bars[1], 0, p.status);
+  wait_bounded(&bars[8], 0, p.status);
   tc_fence_after();
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
   const int r = warp * 32 + lane;
-  for (int cc = 0; cc < kUnNT / 32; ++cc) {
-    float v[32];
-    tmem_ld32(lane_base + cc * 32, v);
-    tmem_ld_wait();
+  float v[kUnNT];
+  tmem_ld32(lane_base, v);
+  tmem_ld32(lane_base + 32, v + 32);
+  tmem_ld_wait();
 #pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      const int t = cc * 32 + x;
-      if (t < nt) p.o[((size_t)(t0 + t) * p.H + i) * kD + r] = v[x];
-    }
-  }
+  for (int t = 0; t < kUnNT; ++t)
+    if (t < nt) p.o[((size_t)(t0 + t) * p.H + i) * kD + r] = v[t];
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 64);
@@ -218,12 +240,18 @@ bool absorb_tc_supported(const Dims& d) {
 
 cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, const int32_t* pos,
                              int T, const void* w_uk, void* q_lat, cudaStream_t stream) {
-  CUtensorMap tmW, tmQ;
+  CUtensorMap tmW, tmQ, tmL;
   {
     const uint64_t dims[2] = {(uint64_t)tca::kC, (uint64_t)d.H * tca::kD};
     const uint64_t st[1] = {(uint64_t)tca::kC * 2};
     const uint32_t box[2] = {64, 128};
     if (!encode_bf16_map(&tmW, w_uk, 2, dims, st, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)(tca::kC + tca::kR), (uint64_t)d.H, (uint64_t)T};
+    const uint64_t st[2] = {(uint64_t)(tca::kC + tca::kR) * 2, (uint64_t)d.H * (tca::kC + tca::kR) * 2};
+    const uint32_t box[3] = {64, 1, tca::kAbsNT};
+    if (!encode_bf16_map(&tmL, q_lat, 3, dims, st, box)) return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[3] = {(uint64_t)tca::kD, (uint64_t)d.H, (uint64_t)T};
@@ -251,7 +279,7 @@ cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, co
     attr = true;
   }
   dim3 grid(d.H, 2, (T + tca::kAbsNT - 1) / tca::kAbsNT);
-  tca::absorb_tc_kernel<<<grid, 128, tca::kAbsSmem, stream>>>(tmW, tmQ, p);
+  tca::absorb_tc_kernel<<<grid, 128, tca::kAbsSmem, stream>>>(tmW, tmQ, tmL, p);
   return cudaGetLastError();
 }
 

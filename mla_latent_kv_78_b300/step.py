@@ -95,7 +95,8 @@ class DecodeStep:
     # -- the step as one CUDA graph ----------------------------------------
     def capture(self, c_kv_new, k_r_new, q_c, q_r, timing: bool = False) -> None:
         """Record append -> absorb -> decode -> unabsorb over these input tensors as one CUDA
-        graph, so a step costs one graph launch instead of four host-side library calls.
+        graph, so a step costs one graph launch instead of four host-side library calls. In the
+        graph the append and the absorption are independent branches that may overlap.
 
         The graph keeps the inputs' device addresses: write each step's inputs into the same
         tensors (copy_) before replay(). One eager step runs first, outside the capture, so
@@ -113,11 +114,18 @@ class DecodeStep:
         ev = ([torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
               if timing else None)
         graph = torch.cuda.CUDAGraph()
+        fork = torch.cuda.Stream(device=dev)
         with torch.cuda.graph(graph):
+            main = torch.cuda.current_stream(dev)
             if ev:
                 ev[0].record()
-            self.append(c_kv_new, k_r_new)
+            # the cache append and the query absorption touch disjoint buffers: they run side
+            # by side, and the decode waits for both
+            fork.wait_stream(main)
+            with torch.cuda.stream(fork):
+                self.append(c_kv_new, k_r_new)
             self.absorb(q_c, q_r)
+            main.wait_stream(fork)
             if ev:
                 ev[1].record()
             self.decode()
