@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(128, 2)
   tc_fence_after();
   const uint32_t tmem = *slot;
   const int t = warp * 32 + lane;   // this thread's token (TMEM lane) in the tile
+  griddep_launch_dependents();   // the decode may start its set-up while this grid finishes
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
     mbar_arrive_expect_tx(&bars[0], 6 * 16384);
@@ -196,6 +197,9 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
+  // launched programmatically after the decode: the set-up above overlaps its tail, the inputs
+  // are read only once it has completed
+  griddep_wait();
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
     for (int j = 0; j < 8; ++j) {
@@ -311,8 +315,9 @@ cudaError_t launch_unabsorb_tc(const Dims& d, const void* o_lat, int T, const vo
     attr = true;
   }
   dim3 grid(d.H, (T + tca::kUnNT - 1) / tca::kUnNT);
-  tca::unabsorb_tc_kernel<<<grid, 128, tca::kUnSmem, stream>>>(tmW, tmO, p);
-  return cudaGetLastError();
+  cudaError_t e = launch_programmatic(tca::unabsorb_tc_kernel, grid, dim3(128), tca::kUnSmem, stream,
+                                      tmW, tmO, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace mla

@@ -285,39 +285,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   const int split = unit % prm.S;
   const int row = unit / prm.S;           // b * n_q + j
   const int b = row / prm.n_q, j = row % prm.n_q;
-  const int L = prm.seq_lens[b];
-  const bool bad_len = (L < prm.n_q || L > prm.max_seq_len);
-  const int visible = bad_len ? 0 : L - prm.n_q + j + 1;
-  int chunk = (visible + prm.S - 1) / prm.S;
-  chunk = (chunk + kTile - 1) / kTile * kTile;
-  const int lo = min(visible, split * chunk);
-  const int hi = min(visible, lo + chunk);
-  const int nt = (hi - lo + kTile - 1) / kTile;
-  const int valid_pages = (hi + kP - 1) / kP;   // pages holding tokens < hi
-
-  if (nt == 0) {
-    // nothing visible in this range: zero output, lse = -inf
-    if (bad_len && tid == 0 && rank == 0 && split == 0) flag_status(prm.status, MLA_DEV_BAD_SEQLEN);
-    for (int idx = tid; idx < kH * 256; idx += kThreads) {
-      const int h = idx >> 8, q = idx & 255;
-      const int dc = (q >> 7) * 256 + rank * 128 + (q & 127);
-      const size_t o = (size_t)row * kH + h;
-      if (prm.S == 1)
-        prm.o_lat[o * kC + dc] = __float2bfloat16_rn(0.f);
-      else
-        prm.ws_o[(o * prm.S + split) * kC + dc] = 0.f;
-    }
-    if (rank == 0 && tid < kH) {
-      const size_t o = (size_t)row * kH + tid;
-      if (prm.S == 1) {
-        if (prm.lse) prm.lse[o] = -CUDART_INF_F;
-      } else {
-        prm.ws_lse[o * prm.S + split] = -CUDART_INF_F;
-      }
-    }
-    return;
-  }
-
   // exchange area of this unit: [rank][slot] {P^T 16 KB, flag word, maxima 512 B}
   uint8_t* xunit = prm.xws + (size_t)unit * kXUnitBytes;
   auto x_slot = [&](uint32_t r, int slot) {
@@ -374,6 +341,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status};
+  // Everything above touches only this pair's own shared memory and TMEM, so with a
+  // programmatic launch it overlaps the tail of the preceding kernel on the stream; every
+  // read of the inputs comes after that kernel has completed.
+  griddep_launch_dependents();
+  griddep_wait();
+  const int L = prm.seq_lens[b];
+  const bool bad_len = (L < prm.n_q || L > prm.max_seq_len);
+  const int visible = bad_len ? 0 : L - prm.n_q + j + 1;
+  int chunk = (visible + prm.S - 1) / prm.S;
+  chunk = (chunk + kTile - 1) / kTile * kTile;
+  const int lo = min(visible, split * chunk);
+  const int hi = min(visible, lo + chunk);
+  const int nt = (hi - lo + kTile - 1) / kTile;
+  const int valid_pages = (hi + kP - 1) / kP;   // pages holding tokens < hi
 
   // Page ids of this unit's range, read by a whole producer warp 32 pages at a time (lane j
   // holds page 32*batch + j of the range) one batch ahead of use, so no TMA issue waits on a
@@ -401,7 +382,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     return pg < 0 ? prm.num_pages * kP : pg * kP;
   };
 
-  if (warp == 0) {
+  if (nt == 0) {
+    // nothing visible in this range: zero output, lse = -inf
+    if (bad_len && tid == 0 && rank == 0 && split == 0) flag_status(prm.status, MLA_DEV_BAD_SEQLEN);
+    for (int idx = tid; idx < kH * 256; idx += kThreads) {
+      const int h = idx >> 8, q = idx & 255;
+      const int dc = (q >> 7) * 256 + rank * 128 + (q & 127);
+      const size_t o = (size_t)row * kH + h;
+      if (prm.S == 1)
+        prm.o_lat[o * kC + dc] = __float2bfloat16_rn(0.f);
+      else
+        prm.ws_o[(o * prm.S + split) * kC + dc] = 0.f;
+    }
+    if (rank == 0 && tid < kH) {
+      const size_t o = (size_t)row * kH + tid;
+      if (prm.S == 1) {
+        if (prm.lse) prm.lse[o] = -CUDART_INF_F;
+      } else {
+        prm.ws_lse[o * prm.S + split] = -CUDART_INF_F;
+      }
+    }
+  } else if (warp == 0) {
     // ================================================================ TMA producer
     // Q once, then every tile's key chunks in order (lane 0 issues; the warp keeps page ids)
     pid_cur = fetch_pid(0);
@@ -1380,11 +1381,11 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);
 #endif
   const unsigned grid = 2u * (unsigned)(B * n_q * S);
-  if (f8)
-    tc::decode_kernel<true><<<grid, tc::Lay<true>::THREADS, tc::kSmemBytes<true>, stream>>>(maps, prm);
-  else
-    tc::decode_kernel<false><<<grid, tc::Lay<false>::THREADS, tc::kSmemBytes<false>, stream>>>(maps, prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = f8 ? launch_programmatic(tc::decode_kernel<true>, dim3(grid), dim3(tc::Lay<true>::THREADS),
+                                           tc::kSmemBytes<true>, stream, maps, prm)
+                     : launch_programmatic(tc::decode_kernel<false>, dim3(grid), dim3(tc::Lay<false>::THREADS),
+                                           tc::kSmemBytes<false>, stream, maps, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return e;
   return launch_combine(d.C, S, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, rows, stream);
 }

@@ -5,6 +5,24 @@
 
 namespace mla {
 
+// Launch with programmatic stream serialization: the kernel may begin while the preceding
+// kernel on `stream` is still running, so it must read no input before griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, const int32_t* seq_idx,
                           const int32_t* pos, int T, const int32_t* bt, int batch, int maxp,
                           int num_pages, void* pool, int32_t* status, cudaStream_t stream);

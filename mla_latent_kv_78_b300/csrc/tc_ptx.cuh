@@ -32,7 +32,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// Arrive on a barrier in another CTA of the cluster (address from mapa).
 // Arrive on a barrier in another CTA without release semantics: for signals that publish no
 // memory writes (e.g. "this thread has finished reading TMEM", after tcgen05.wait::ld), so
 // the arrival need not wait for the thread's earlier stores to become visible.
@@ -41,6 +40,8 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr
                : "memory");
 }
 
+// Arrive on a barrier in another CTA of the cluster (address from mapa), releasing this
+// thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
@@ -210,6 +211,16 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start before the preceding kernel on its stream has finished; griddep_wait() blocks until
+// that kernel has completed and its writes are visible. griddep_launch_dependents() lets the
+// next such kernel start launching (it still waits for this one's completion before reading).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
