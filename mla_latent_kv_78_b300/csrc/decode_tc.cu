@@ -52,11 +52,10 @@ constexpr int kVCh = kTile / 32;     // 8 latent chunks per tile
 constexpr int kPvWarp = 12;             // the P.V issuer
 constexpr int kCvtWarp0 = 13;           // FP8 cache: warps 13-15 convert codes to f16 tiles
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
-constexpr int kXSlots = 4;                      // exchange slots per CTA: tile t uses t % 4
-constexpr uint32_t kXPBytes = 128 * 128;        // P^T rows one CTA sends per tile (16 KB)
-constexpr uint32_t kXHdrBytes = 16;             // flag word (1: the tile's maxima follow) + pad
-constexpr uint32_t kXBytes = kXPBytes + kXHdrBytes + kH * 4;   // + that tile's per-head maxima
-constexpr size_t kXUnitBytes = 2 * kXSlots * (size_t)kXBytes;   // per (seq, row, split)
+constexpr int kXSlots = 4;    // slots for the peer's published tile maxima: tile t uses t % 4
+// Bytes the peer stores into this CTA's shared memory per tile (st.async, counted on
+// p_landed): its 128 token rows of this CTA's head half of P^T, and its per-head tile maxima.
+constexpr uint32_t kXBytes = 128 * 128 + kH * 4;
 constexpr float kLazy = 8.f;    // log2 units a score may exceed the reference before it moves
 // Larger excesses are clamped and flagged (MLA_DEV_SCORE_RANGE): bf16 P holds 2^96, f16 P
 // (FP8 cache) 2^15.
@@ -65,11 +64,10 @@ constexpr float kRange = F8 ? 15.f : 96.f;
 constexpr int kRawS = 8192 + 2048;   // FP8 key chunk: [128 tok x 64 codes] + [128 tok x 4 scales]
 constexpr int kRawV = 8192 + 512;    // FP8 latent chunk: 4 x [32 tok x 64 codes] + [32 tok x 4 scales]
 
-constexpr int kRcvFloats = (int)(kXBytes - kXPBytes) / 4;   // 132: flag word, pad, 128 maxima
 constexpr int F_COL = 0;       // [8 warps][64]   column max / column sum partials
 constexpr int F_CMLOC = 512;   // [2][128] this CTA's published per-head tile maxima
-constexpr int F_RCV = 768;     // [4][132] the peer's flag word + per-head tile maxima, by slot
-constexpr int F_M = F_RCV + kXSlots * kRcvFloats;   // [128] reference (log2 units), same in both CTAs
+constexpr int F_RCV = 768;     // [4][128] the peer's per-head tile maxima by slot (-inf: none)
+constexpr int F_M = F_RCV + kXSlots * kH;   // [128] reference (log2 units), same in both CTAs
 constexpr int F_ALPHA = F_M + 128;   // [128]
 constexpr int F_LLOC = F_ALPHA + 128;  // [128]
 constexpr int F_LRCV = F_LLOC + 128;   // [128]
@@ -118,8 +116,7 @@ struct BarsT {
   uint64_t rs_ready[RS], rs_free[RS], rv_ready[RV], rv_free[RV];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_landed[2], p_ready[2], o_done[2];
-  uint64_t x_ready[2];   // the peer has put P^T(t) and its maxima of tile t in global memory
-  uint64_t x0_ready;     // the peer has put its tile-0 maxima in global memory
+  uint64_t x0_ready;     // the peer's tile-0 maxima have landed
   uint64_t l_landed;
   uint64_t teardown;
   uint32_t tmem_base;
@@ -150,7 +147,6 @@ struct Params {
   float* lse;
   float* ws_o;
   float* ws_lse;
-  uint8_t* xws;          // exchange area, kXUnitBytes per unit
   int32_t* status;
 #ifdef MLA_TC_TRACE
   unsigned long long* trace;
@@ -285,12 +281,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   const int split = unit % prm.S;
   const int row = unit / prm.S;           // b * n_q + j
   const int b = row / prm.n_q, j = row % prm.n_q;
-  // exchange area of this unit: [rank][slot] {P^T 16 KB, flag word, maxima 512 B}
-  uint8_t* xunit = prm.xws + (size_t)unit * kXUnitBytes;
-  auto x_slot = [&](uint32_t r, int slot) {
-    return xunit + (size_t)(r * kXSlots + slot) * kXBytes;
-  };
-
   // ---- set-up
   if (tid == 0) TRACE(11, 0);
   if (tid == 0) {
@@ -323,7 +313,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       mbar_init(&bars->p_landed[s], 8);
       mbar_init(&bars->p_ready[s], 2);
       mbar_init(&bars->o_done[s], 1);
-      mbar_init(&bars->x_ready[s], 1);
     }
     mbar_init(&bars->x0_ready, 1);
     mbar_init(&bars->l_landed, 1);
@@ -912,26 +901,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       }
     }
   } else if (warp == 3) {
-    // ================================================================ exchange
-    // Fetches the peer's P^T half, flag word and tile maxima once the peer has put them in
-    // global memory, into this CTA's P^T buffer of that tile's parity (after PV of the tile
-    // two back has finished reading it); reports the buffer complete to the even CTA.
+    // ================================================================ P^T relay
+    // This CTA's P^T buffer of tile t is complete once its own softmax warps have written their
+    // rows and the peer's rows and maxima have landed (p_landed); the relay makes the peer's
+    // stores visible to the tensor core and reports the buffer to the even CTA's P.V issuer.
     if (lane == 0) {
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
-        const int par = t & 1, slot = t & (kXSlots - 1);
-        ok = wait_bar(&bars->x_ready[par], (t >> 1) & 1, cx);
-        // P^T buffer t % kPB is free once P.V of tile t - kPB has read it
-        if (ok && t >= kPB) ok = wait_bar(&bars->o_done[(t - kPB) & 1], ((t - kPB) >> 1) & 1, cx);
-        if (!ok) break;
-        TRACE(8, t);
-        const uint8_t* src = x_slot(peer, slot);
-        bulk_g2s(sm + OFF_P + (t % kPB) * 32768 + peer * kXPBytes, src, kXPBytes, &bars->p_landed[par]);
-        bulk_g2s(fs + F_RCV + slot * kRcvFloats, src + kXPBytes, kXBytes - kXPBytes,
-                 &bars->p_landed[par]);
+        const int par = t & 1;
         ok = wait_bar(&bars->p_landed[par], (t >> 1) & 1, cx);
         TRACE(7, t);
-        if (ok) arrive_even(&bars->p_ready[par], rank);
+        if (ok) {
+          fence_proxy_async_smem();
+          arrive_even(&bars->p_ready[par], rank);
+        }
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -952,10 +935,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     const int stid = tid - 128;        // 0..255
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
     const float* Mg = fs + F_M + 64 * g;
+    const uint32_t peer_rcv = mapa(smem_u32(fs + F_RCV), peer);
+    uint32_t peer_landed = 0;
     float l_w[2] = {0.f, 0.f};   // sums of P of this warp's tokens for heads 64g + 32 h2 + lane
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int par = t & 1, slot = t & (kXSlots - 1);
+      peer_landed = mapa(smem_u32(&bars->p_landed[par]), peer);
       // ---- reference for tile t, from tile t-2's published maxima (both CTAs). One thread
       // waits on each barrier; the others sleep in the named barrier, so no warp spins.
       bool ok1 = true;
@@ -966,10 +952,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       }
       if (t >= 2 && stid < kH) {
         const int h = stid;
-        const float* rcv = fs + F_RCV + ((t - 2) & (kXSlots - 1)) * kRcvFloats;
-        float cand = -CUDART_INF_F;
-        if (flags[FL_PUB + par]) cand = fs[F_CMLOC + par * kH + h];
-        if (__float_as_uint(rcv[0]) != 0u) cand = fmaxf(cand, rcv[4 + h]);
+        const float* rcv = fs + F_RCV + ((t - 2) & (kXSlots - 1)) * kH;
+        float cand = rcv[h];
+        if (flags[FL_PUB + par]) cand = fmaxf(cand, fs[F_CMLOC + par * kH + h]);
         const float mo = fs[F_M + h];
         float alpha = 1.f;
         if (cand > mo + kLazy) {
@@ -1077,19 +1062,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       }
       if (extreme) flag_status(prm.status, MLA_DEV_SCORE_RANGE);
       if (stid == 0) TRACE(14, t);
-      // ---- the peer's head half of P^T goes out first (same swizzled bytes as in shared
-      // memory); the slot was last read four tiles ago
-      const uint32_t sw_off = (uint32_t)((i & 7) * 16);
-      if (g != (int)rank) {
-        uint8_t* dst = x_slot(rank, slot) + i * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        fence_proxy_async_global();
-      }
-      // P^T's buffer is free once P.V of tile t - kPB is done; O is stable to rescale once P.V
-      // of the previous tile is
+      // P^T's buffer (in both CTAs) is free once P.V of tile t - kPB is done; O is stable to
+      // rescale once P.V of the previous tile is
       bool ok3 = true;
       {
         const int wt = rescale ? t - 1 : t - kPB;   // (a rescale needs t >= 2)
@@ -1117,17 +1091,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           for (int q = 0; q < 4; ++q) pmax = fmaxf(pmax, fs[F_COL + (gg * 4 + q) * 64 + cc]);
           const float my_max = pmax > 0.f ? fs[F_M + h] + log2f(pmax) : -CUDART_INF_F;
           fs[F_CMLOC + par * kH + h] = my_max;
-          reinterpret_cast<float*>(x_slot(rank, slot) + kXPBytes + kXHdrBytes)[h] = my_max;
-          fence_proxy_async_global();
+          st_async_b32(peer_rcv + (uint32_t)(slot * kH + h) * 4u, __float_as_uint(my_max), peer_landed);
         }
         bar_sync(3, 256);
+      } else if (stid < kH) {
+        // nothing published: the peer's slot reads -inf
+        st_async_b32(peer_rcv + (uint32_t)(slot * kH + stid) * 4u, __float_as_uint(-CUDART_INF_F),
+                     peer_landed);
       }
       if (stid == 0) {
         flags[FL_PUB + par] = any_over ? 1 : 0;
         flags[FL_RESCALE + par] = 0;   // every thread has read it (barrier 5)
-        *reinterpret_cast<uint32_t*>(x_slot(rank, slot) + kXPBytes) = any_over ? 1u : 0u;
-        fence_proxy_async_global();
-        mbar_arrive_remote(mapa(smem_u32(&bars->x_ready[par]), peer));
         TRACE(5, t);
       }
       tc_fence_after();
@@ -1146,21 +1120,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           }
         tmem_st_wait();
       }
-      // ---- this CTA's own head half of P^T, rows of its tokens
-      if (g == (int)rank) {
-        const int k = (int)rank * 128 + i;
-        uint8_t* dst = sm + OFF_P + (t % kPB) * 32768 + k * 128;
+      // ---- P^T rows of this CTA's tokens: its own head half into its buffer, the peer's half
+      // straight into the peer's buffer (same offsets, 128-byte swizzle)
+      {
+        const uint32_t sw_off = (uint32_t)((i & 7) * 16);
+        const uint32_t off = (uint32_t)(OFF_P + (t % kPB) * 32768 + ((int)rank * 128 + i) * 128);
+        if (g == (int)rank) {
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(dst + ((cc * 16) ^ sw_off)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        fence_proxy_async_smem();
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4*>(sm + off + ((cc * 16) ^ sw_off)) =
+                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          fence_proxy_async_smem();
+        } else {
+          const uint32_t dst = mapa(smem_u32(sm + off), peer);
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            st_async_v4_b32(dst + ((cc * 16) ^ sw_off),
+                            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]),
+                            peer_landed);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (sw == 0) {
-          mbar_arrive_expect_tx(&bars->p_landed[par], kXBytes);
+          mbar_arrive_expect_tx(&bars->p_landed[par], kXBytes);   // the peer's rows + maxima
           TRACE(6, t);
         } else {
           mbar_arrive(&bars->p_landed[par]);
@@ -1319,7 +1303,7 @@ size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int nu
                           int num_sms) {
   const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, num_sms);
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
-  return part + (size_t)B * n_q * S * tc::kXUnitBytes;
+  return part;
 }
 
 cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool, const int32_t* bt,
@@ -1360,7 +1344,7 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   }
   const size_t rows = (size_t)B * n_q * d.H;
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
-  if (ws_bytes < part + (size_t)B * n_q * S * tc::kXUnitBytes) return cudaErrorInvalidValue;
+  if (ws_bytes < part) return cudaErrorInvalidValue;
   tc::Params prm;
   prm.bt = bt;
   prm.maxp = maxp;
@@ -1375,7 +1359,6 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.lse = lse;
   prm.ws_o = S > 1 ? static_cast<float*>(ws) : nullptr;
   prm.ws_lse = S > 1 ? static_cast<float*>(ws) + rows * S * d.C : nullptr;
-  prm.xws = static_cast<uint8_t*>(ws) + part;
   prm.status = status;
 #ifdef MLA_TC_TRACE
   prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);

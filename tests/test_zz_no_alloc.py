@@ -60,10 +60,10 @@ def test_noalloc_matches_decode_on_consecutive_calls(kernel):
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     wl = W.small_v2(2, [64, 64], n_q=1, cache="bf16", seed=23)
     cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act)
-    batch = 2048   # the tensor-core exchange area alone then exceeds the fixed scratch
-    assert M.mla_decode_workspace_size(cfg, batch, 1, 4096) > L.NOALLOC_SCRATCH_BYTES
+    batch, splits = 64, 4   # fp32 split partials: 64 x 128 heads x 4 x 513 x 4 B = 67 MB
+    assert M.mla_decode_workspace_size(cfg, batch, 1, 4096, splits) > L.NOALLOC_SCRATCH_BYTES
     lib = M.lib()
-    rc = lib.mla_decode_noalloc(ctypes.byref(cfg), 16, 16, 16, 64, 64, 16, batch, 1, 4096, 0,
+    rc = lib.mla_decode_noalloc(ctypes.byref(cfg), 16, 16, 16, 64, 64, 16, batch, 1, 4096, splits,
                                 16, None, None, None)
     assert rc == L.MLA_ERR_SCRATCH_LIMIT
     assert "scratch" in M.mla_status_string(rc)
