@@ -88,8 +88,8 @@ struct Lay {
   // FP8: Q stays resident (the converters turn it into f16 once).
   static constexpr bool QRES = F8;
   static constexpr int SSTAGE = QRES ? 16384 : 16384 + 8192;   // S-phase stage bytes
-  static constexpr int NS = F8 ? 2 : 3;     // S-phase ring
-  static constexpr int NV = F8 ? 2 : 5;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
+  static constexpr int NS = F8 ? 2 : 4;     // S-phase ring
+  static constexpr int NV = F8 ? 2 : 3;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
   static constexpr int PB = F8 ? 1 : 2;     // P^T buffers [256 tok x 64 heads] = 32 KB each
   static constexpr int RS = F8 ? 3 : 0;     // raw key-chunk slots (kRawS bytes)
   static constexpr int RV = F8 ? 2 : 0;     // raw latent-chunk slots (kRawV bytes)
@@ -221,13 +221,18 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) 
   return v[0];
 }
 
+// Bounded wait by one thread, polling (a suspended thread resumed measurably later than a
+// polling one). kCluster: the arrivals carry data written by the other CTA's threads, so the
+// acquire is at cluster scope; otherwise at CTA scope.
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& cx) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto test = [&]() { return kCluster ? mbar_test_cluster(a, parity) : mbar_test_cta(a, parity); };
+  if (test()) return true;
   const long long t0 = clock64();
   while (true) {
     if (*cx.abort_flag) return false;
-    if (mbar_try_wait(a, parity)) return true;
+    if (test()) return true;
     if (clock64() - t0 > kTimeout) {
       *cx.abort_flag = 1;
       flag_status(cx.status, MLA_DEV_TIMEOUT);
@@ -514,7 +519,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       const long long prof_start = clock64();
 #endif
       // bf16: both CTAs' Q halves have landed; FP8: both have also been converted to f16
-      bool ok = F8 ? wait_bar(&bars->q_conv, 0, cx) : true;
+      bool ok = F8 ? wait_bar<true>(&bars->q_conv, 0, cx) : true;
       for (int t = 0; t < nt && ok; ++t) {
         TRACE(22, t);
         // TMEM buffer t % 2 is free once the softmax has read S^T(t-2)
@@ -524,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         const uint32_t d = tmem + (uint32_t)(t & 1) * 128u;
         for (int c = 0; c < kKCh && ok; ++c) {
           TRACE(17, s_cnt);
-          PROF(0, ok = wait_bar(&bars->s_ready[s_st], s_ph, cx));
+          PROF(0, ok = wait_bar<F8>(&bars->s_ready[s_st], s_ph, cx));
           if (!ok) break;
           TRACE(18, s_cnt);
           PROF(2, tc_fence_after());
@@ -575,13 +580,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
         TRACE(23, t);
-        PROF(6, ok = wait_bar(&bars->p_ready[t & 1], (t >> 1) & 1, cx));
+        PROF(6, ok = wait_bar<true>(&bars->p_ready[t & 1], (t >> 1) & 1, cx));
         if (!ok) break;
         TRACE(1, t);
         tc_fence_after();
         for (int v = 0; v < kVCh && ok; ++v) {
           TRACE(20, v_cnt);
-          PROF(3, ok = wait_bar(&bars->v_ready[v_st], v_ph, cx));
+          PROF(3, ok = wait_bar<F8>(&bars->v_ready[v_st], v_ph, cx));
           if (!ok) break;
           TRACE(21, v_cnt);
           PROF(5, tc_fence_after());
@@ -909,7 +914,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
         const int par = t & 1;
-        ok = wait_bar(&bars->p_landed[par], (t >> 1) & 1, cx);
+        ok = wait_bar<true>(&bars->p_landed[par], (t >> 1) & 1, cx);
         TRACE(7, t);
         if (ok) {
           fence_proxy_async_smem();
@@ -946,7 +951,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       // waits on each barrier; the others sleep in the named barrier, so no warp spins.
       bool ok1 = true;
       if (t >= 2) {
-        if (stid == 0) ok1 = wait_bar(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
+        if (stid == 0) ok1 = wait_bar<true>(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
         ok = bar_and(12, 256, ok1);
         if (!ok) break;
       }
@@ -1000,7 +1005,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         bool okx = true;
         if (stid == 0) {
           mbar_arrive_expect_tx(&bars->x0_ready, kH * 4);
-          okx = wait_bar(&bars->x0_ready, 0, cx);
+          okx = wait_bar<true>(&bars->x0_ready, 0, cx);
         }
         ok = bar_and(13, 256, okx);
         if (!ok) break;
@@ -1174,7 +1179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         bool ok4 = true;
         if (stid == 0) {
           mbar_arrive_expect_tx(&bars->l_landed, kH * 4);
-          ok4 = wait_bar(&bars->l_landed, 0, cx);
+          ok4 = wait_bar<true>(&bars->l_landed, 0, cx);
         }
         ok4 = bar_and(14, 256, ok4);
         if (ok4 && stid < kH) {
