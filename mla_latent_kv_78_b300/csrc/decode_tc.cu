@@ -77,7 +77,8 @@ constexpr int F_FLAG = F_X0 + 128;    // ints, see FL_*
 constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for this tile
 constexpr int FL_ABORT = 2;    // a bounded wait gave up
 constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
-constexpr int F_END = F_FLAG + 6;
+constexpr int FL_TICKET = 5;   // FP8 converters: the next job allowed to acquire its slots
+constexpr int F_END = F_FLAG + 8;   // (even: the barriers that follow need 8-byte alignment)
 // Shared-memory layout. bf16 cache: keys and latents arrive by TMA in their MMA layout.
 // FP8 cache: raw codes and scales arrive by TMA in staging rings (RS, RV slots) and the
 // converter warps write f16 operand tiles into the S and V rings.
@@ -124,6 +125,7 @@ struct BarsT {
 template <bool F8>
 constexpr int kSmemBytes = Lay<F8>::OFF_BAR + (int)sizeof(BarsT<F8>) + 1024;   // + alignment slack
 static_assert(kSmemBytes<false> <= 232448 && kSmemBytes<true> <= 232448, "shared memory");
+static_assert(Lay<false>::OFF_BAR % 8 == 0 && Lay<true>::OFF_BAR % 8 == 0, "mbarrier alignment");
 
 // Tensor maps of one launch (bf16 cache: q, k, v; FP8 cache: q and the raw maps).
 struct Maps {
@@ -735,13 +737,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     // ================================================================ FP8 converters
     // Dequantisation of the FP8 cache, 「Deepseek系列从v3到R易背面经版」 F8量化策略 (per-token
     // 1x128 groups): value = code * scale of its group, produced here as f16 operand tiles in
-    // the MMA's swizzled layout. Warps 13-14 make the key tiles (and convert this CTA's Q half
-    // and the bf16 RoPE keys to f16 first), warp 15 the latent tiles for P.V, zeroing rows
-    // past the range so that P = 0 never meets stale data.
+    // the MMA's swizzled layout. The three warps first turn this CTA's Q half into f16, then
+    // share the key chunks of every tile in order (9 per tile, the ninth being the bf16 RoPE
+    // keys): warp w takes every third chunk and converts it alone. Chunks acquire their slots
+    // (the staging chunk and the free operand slot) strictly in order, through a ticket: a
+    // barrier is then never waited on more than one phase ahead of the phase it is in, which
+    // its parity test could not tell from the phase before; the conversions themselves
+    // overlap. The latent chunks for P.V are converted by the softmax warps.
     if constexpr (F8) {
-      const int ct = tid - kCvtWarp0 * 32;   // 0..95: warps 13-15
-      // codes (8 per item) x one scale -> 8 f16, stored at 16-byte unit u of row r of a
-      // 128-byte-swizzled tile
+      const int cw = warp - kCvtWarp0;      // 0..2
+      const int ct = tid - kCvtWarp0 * 32;   // 0..95
+      // codes (8 per item) x one scale -> 8 f16
       auto cvt8 = [](uint2 codes, uint32_t sc2) -> uint4 {
         return make_uint4(mul_f16x2(e4m3x2_to_f16x2(codes.x), sc2),
                           mul_f16x2(e4m3x2_to_f16x2(codes.x >> 16), sc2),
@@ -754,156 +760,106 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         };
         return make_uint4(one(w.x), one(w.y), one(w.z), one(w.w));
       };
-      auto scale2 = [](float sc) -> uint32_t {
-        const uint32_t h = pack_f16x2(sc, sc);
-        return h;
-      };
-      if (ct < 64) {
-        // ---- key tiles (warps 13, 14: 64 threads, named barriers 10 and 11)
+      auto scale2 = [](float sc) -> uint32_t { return pack_f16x2(sc, sc); };
 #ifdef MLA_TC_TRACE
-        long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        const long long prof_start = clock64();
+      long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      const long long prof_start = clock64();
 #endif
-        bool ok = true;
-        if (ct == 0) ok = wait_bar(&bars->q_ready, 0, cx);
-        ok = bar_and(10, 64, ok);
-        if (ok) {
-          uint4* q = reinterpret_cast<uint4*>(sm + OFF_Q);
-          for (int x = ct; x < kKCh * 8192 / 16; x += 64) q[x] = bf16x8_to_f16x8(q[x]);
-          fence_proxy_async_smem();
-          bar_sync(11, 64);
-          if (ct == 0) arrive_even(&bars->q_conv, rank);
-        }
-        int n = 0, m = 0;   // key-tile count, raw key-chunk count
-        for (int t = 0; t < nt && ok; ++t) {
-          for (int c = 0; c < kKCh && ok; ++c, ++n) {
-            const int st = n % kNS;
-            uint8_t* dst = sm + OFF_S + st * kSStage;
-            bool r = true;
-            if (ct == 0 && n >= kNS) PROF(0, r = wait_bar(&bars->s_free[st], ((n / kNS) - 1) & 1, cx));
-            r = bar_and(10, 64, r);
-            for (int h = 0; h < (c < 8 ? 1 : 2) && r; ++h, ++m) {
-              const int rs = m % Ly::RS;
-              if (ct == 0) PROF(1, r = wait_bar(&bars->rs_ready[rs], (m / Ly::RS) & 1, cx));
-              r = bar_and(10, 64, r);
-              if (!r) break;
-              const uint8_t* src = sm + Ly::OFF_RS + rs * kRawS;
-              // Thread = token row: 16-byte loads of the staging row start at a per-row
-              // rotation so the 64- and 128-byte row strides spread over all banks; the
-              // 128-byte swizzle of the tile does the same for the stores.
-              if (c < 8) {
-                // latent dims 64c .. 64c+63 of the CTA's 128 tokens, rows ct and ct + 64
-#pragma unroll
-                for (int r2 = 0; r2 < 2; ++r2) {
-                  const int rr = ct + 64 * r2;
-                  const uint32_t s2 = scale2(*reinterpret_cast<const float*>(src + 8192 + rr * 16 + (c >> 1) * 4));
-                  uint4 in[4];
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    in[j] = *reinterpret_cast<const uint4*>(src + rr * 64 + (((j + rr) & 3) << 4));
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const int u0 = 2 * ((j + rr) & 3);
-                    *reinterpret_cast<uint4*>(dst + rr * 128 + ((u0 ^ (rr & 7)) << 4)) =
-                        cvt8(make_uint2(in[j].x, in[j].y), s2);
-                    *reinterpret_cast<uint4*>(dst + rr * 128 + (((u0 + 1) ^ (rr & 7)) << 4)) =
-                        cvt8(make_uint2(in[j].z, in[j].w), s2);
-                  }
-                }
-              } else {
-                // RoPE keys of page h of the CTA's two: bf16 -> f16, row 64h + ct
-                const int row = 64 * h + ct;
-                uint4 w[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  w[j] = *reinterpret_cast<const uint4*>(src + ct * 128 + (((j + ct) & 7) << 4));
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const int u = (j + ct) & 7;
-                  *reinterpret_cast<uint4*>(dst + row * 128 + ((u ^ (row & 7)) << 4)) = bf16x8_to_f16x8(w[j]);
-                }
-              }
-              bar_sync(11, 64);   // every thread has read the raw slot
-              if (ct == 0) mbar_arrive(&bars->rs_free[rs]);
-            }
-            ok = r;
-            if (!ok) break;
-            fence_proxy_async_smem();
-            bar_sync(11, 64);
-            if (ct == 0) arrive_even(&bars->s_ready[st], rank);
-          }
-        }
-#ifdef MLA_TC_TRACE
-        prof[7] = clock64() - prof_start;
-        if (ct == 0) PROF_STORE(544);
-#endif
-      } else {
-        // ---- latent tiles for P.V (warp 15)
-        const int cl = ct - 64;   // lane
-#ifdef MLA_TC_TRACE
-        long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        const long long prof_start = clock64();
-#endif
-        bool ok = true;
-        int n = 0;   // latent-tile count (= raw latent-chunk count)
-        for (int t = 0; t < nt && ok; ++t) {
-          for (int v = 0; v < kVCh && ok; ++v, ++n) {
-            const int st = n % kNV, rv = n % Ly::RV;
-            if (cl == 0) {
-              if (n >= kNV) PROF(0, ok = wait_bar(&bars->v_free[st], ((n / kNV) - 1) & 1, cx));
-              if (ok) PROF(1, ok = wait_bar(&bars->rv_ready[rv], (n / Ly::RV) & 1, cx));
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            const uint8_t* src = sm + Ly::OFF_RV + rv * kRawV;
-            uint8_t* dst = sm + OFF_V + st * 16384;
-            const int tok0 = lo + t * kTile + v * 32;
-#ifdef MLA_TC_TRACE
-            const long long pc0 = clock64();
-#endif
-            // Lane = token row (32 tokens per chunk); rows past the range get zeros. Loads of
-            // the 64-byte staging rows start at a per-row rotation to spread the banks.
-            const int rr = cl;
-            const bool valid = tok0 + rr < hi;
-            const float sca = *reinterpret_cast<const float*>(src + 8192 + rr * 16 + (int)rank * 4);
-            const float scb = *reinterpret_cast<const float*>(src + 8192 + rr * 16 + (2 + (int)rank) * 4);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const uint32_t s2 = scale2(q4 < 2 ? sca : scb);
-              uint4 in[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                in[j] = *reinterpret_cast<const uint4*>(src + q4 * 2048 + rr * 64 + (((j + rr) & 3) << 4));
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int u0 = 2 * ((j + rr) & 3);
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(dst + q4 * 4096 + rr * 128 + ((u0 ^ (rr & 7)) << 4)) =
-                    valid ? cvt8(make_uint2(in[j].x, in[j].y), s2) : z;
-                *reinterpret_cast<uint4*>(dst + q4 * 4096 + rr * 128 + (((u0 + 1) ^ (rr & 7)) << 4)) =
-                    valid ? cvt8(make_uint2(in[j].z, in[j].w), s2) : z;
-              }
-            }
-#ifdef MLA_TC_TRACE
-            const long long pc1 = clock64();
-            prof[2] += pc1 - pc0;
-#endif
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (cl == 0) {
-              mbar_arrive(&bars->rv_free[rv]);
-              arrive_even(&bars->v_ready[st], rank);
-            }
-#ifdef MLA_TC_TRACE
-            prof[3] += clock64() - pc1;
-#endif
-          }
-        }
-#ifdef MLA_TC_TRACE
-        prof[7] = clock64() - prof_start;
-        if (cl == 0) PROF_STORE(552);
-#endif
+      bool ok = true;
+      if (ct == 0) ok = wait_bar(&bars->q_ready, 0, cx);
+      ok = bar_and(10, 96, ok);
+      if (ok) {
+        uint4* q = reinterpret_cast<uint4*>(sm + OFF_Q);
+        for (int x = ct; x < kKCh * 8192 / 16; x += 96) q[x] = bf16x8_to_f16x8(q[x]);
+        fence_proxy_async_smem();
+        bar_sync(11, 96);
+        if (ct == 0) arrive_even(&bars->q_conv, rank);
       }
+      // lane 0: wait until job J is next to acquire its slots
+      volatile int* ticket = &flags[FL_TICKET];
+      auto my_turn = [&](int J) -> bool {
+        const long long t0 = clock64();
+        while (*ticket != J) {
+          if (*cx.abort_flag) return false;
+          if (clock64() - t0 > kTimeout) {
+            *cx.abort_flag = 1;
+            flag_status(cx.status, MLA_DEV_TIMEOUT);
+            return false;
+          }
+        }
+        return true;
+      };
+      auto pass_turn = [&](int J) {
+        __threadfence_block();
+        *ticket = J + 1;
+      };
+      // Key chunk job n (tile n / 9, chunk n % 9), raw key chunks m .. m (+1 for the RoPE keys).
+      auto key_job = [&](int J, int n) -> bool {
+        const int c = n % kKCh;
+        const int m = (n / kKCh) * (kKCh + 1) + c;   // 10 raw key chunks per tile
+        const int st = n % kNS;
+        uint8_t* dst = sm + OFF_S + st * kSStage;
+        bool r = true;
+        if (lane == 0) {
+          r = my_turn(J);
+          if (r && n >= kNS) PROF(0, r = wait_bar(&bars->s_free[st], ((n / kNS) - 1) & 1, cx));
+          for (int h = 0; h < (c < 8 ? 1 : 2) && r; ++h)
+            PROF(1, r = wait_bar(&bars->rs_ready[(m + h) % Ly::RS], ((m + h) / Ly::RS) & 1, cx));
+          if (r) pass_turn(J);
+        }
+        if (!__shfl_sync(0xffffffffu, r, 0)) return false;
+        if (c < 8) {
+          // latent dims 64c .. 64c+63 of the CTA's 128 tokens; lane = rows lane + 32k.
+          // 16-byte loads of the 64-byte staging rows start at a per-row rotation and the
+          // tile's 128-byte swizzle spreads the stores over all banks.
+          const uint8_t* src = sm + Ly::OFF_RS + (m % Ly::RS) * kRawS;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = lane + 32 * k;
+            const uint32_t s2 = scale2(*reinterpret_cast<const float*>(src + 8192 + rr * 16 + (c >> 1) * 4));
+            uint4 in[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              in[j] = *reinterpret_cast<const uint4*>(src + rr * 64 + (((j + rr) & 3) << 4));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int u0 = 2 * ((j + rr) & 3);
+              *reinterpret_cast<uint4*>(dst + rr * 128 + ((u0 ^ (rr & 7)) << 4)) =
+                  cvt8(make_uint2(in[j].x, in[j].y), s2);
+              *reinterpret_cast<uint4*>(dst + rr * 128 + (((u0 + 1) ^ (rr & 7)) << 4)) =
+                  cvt8(make_uint2(in[j].z, in[j].w), s2);
+            }
+          }
+        } else {
+          // RoPE keys, bf16 -> f16: rows 0-63 from the first page's staging slot, 64-127 from
+          // the second's
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = lane + 32 * k;
+            const uint8_t* src = sm + Ly::OFF_RS + ((m + (k >> 1)) % Ly::RS) * kRawS + (rr & 63) * 128;
+            uint4 w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(src + (((j + rr) & 7) << 4));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int u = (j + rr) & 7;
+              *reinterpret_cast<uint4*>(dst + rr * 128 + ((u ^ (rr & 7)) << 4)) = bf16x8_to_f16x8(w[j]);
+            }
+          }
+        }
+        __syncwarp();   // every lane has read the staging slot(s)
+        if (lane == 0)
+          for (int h = 0; h < (c < 8 ? 1 : 2); ++h) mbar_arrive(&bars->rs_free[(m + h) % Ly::RS]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) arrive_even(&bars->s_ready[st], rank);
+        return true;
+      };
+      for (int n = cw; n < nt * kKCh && ok; n += 3) ok = key_job(n, n);
+#ifdef MLA_TC_TRACE
+      prof[7] = clock64() - prof_start;
+      if (lane == 0) PROF_STORE(544 + 8 * (cw & 1));
+#endif
     }
   } else if (warp == 3) {
     // ================================================================ P^T relay
@@ -1154,6 +1110,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         } else {
           mbar_arrive(&bars->p_landed[par]);
         }
+      }
+      if constexpr (F8) {
+        // ---- FP8 cache: this tile's latent chunks for P.V, dequantised by the 256 softmax
+        // threads (chunk = 32 tokens x this CTA's 256 d_c columns; thread = token rr, 32 codes
+        // of sub-tile q4 = part / 2). Rows past the range become zeros, so that P = 0 never
+        // meets stale data.
+        const int rr = stid & 31, part = stid >> 5, q4 = part >> 1, half = part & 1;
+#pragma unroll 1
+        for (int v = 0; v < kVCh && ok; ++v) {
+          const int n = t * kVCh + v;
+          const int st = n % kNV, rv = n % Ly::RV;
+          bool r = true;
+          if (stid == 0) {
+            if (n >= kNV) r = wait_bar(&bars->v_free[st], ((n / kNV) - 1) & 1, cx);
+            if (r) r = wait_bar(&bars->rv_ready[rv], (n / Ly::RV) & 1, cx);
+          }
+          ok = bar_and(15, 256, r);
+          if (!ok) break;
+          const uint8_t* src = sm + Ly::OFF_RV + rv * kRawV;
+          uint8_t* dst = sm + OFF_V + st * 16384 + q4 * 4096 + rr * 128;
+          const bool valid = lo + t * kTile + v * 32 + rr < hi;
+          const float sc = *reinterpret_cast<const float*>(src + 8192 + rr * 16 +
+                                                           ((q4 < 2 ? 0 : 2) + (int)rank) * 4);
+          const uint32_t s2 = pack_f16x2(sc, sc);
+          const uint4* in = reinterpret_cast<const uint4*>(src + q4 * 2048 + rr * 64 + half * 32);
+          const uint4 a0 = in[0], a1 = in[1];
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t u = (uint32_t)(half * 4 + k) ^ (uint32_t)(rr & 7);
+            const uint4 o = make_uint4(mul_f16x2(e4m3x2_to_f16x2(w[2 * k]), s2),
+                                       mul_f16x2(e4m3x2_to_f16x2(w[2 * k] >> 16), s2),
+                                       mul_f16x2(e4m3x2_to_f16x2(w[2 * k + 1]), s2),
+                                       mul_f16x2(e4m3x2_to_f16x2(w[2 * k + 1] >> 16), s2));
+            *reinterpret_cast<uint4*>(dst + u * 16) = valid ? o : z;
+          }
+          fence_proxy_async_smem();
+          bar_sync(15, 256);
+          if (stid == 0) {
+            mbar_arrive(&bars->rv_free[rv]);
+            arrive_even(&bars->v_ready[st], rank);
+          }
+        }
+        if (!ok) break;
       }
     }
     if (ok) {
