@@ -858,7 +858,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       for (int n = cw; n < nt * kKCh && ok; n += 3) ok = key_job(n, n);
 #ifdef MLA_TC_TRACE
       prof[7] = clock64() - prof_start;
-      if (lane == 0) PROF_STORE(544 + 8 * (cw & 1));
+      if (lane == 0) PROF_STORE(544 + 8 * cw);
 #endif
     }
   } else if (warp == 3) {
@@ -899,6 +899,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     const uint32_t peer_rcv = mapa(smem_u32(fs + F_RCV), peer);
     uint32_t peer_landed = 0;
     float l_w[2] = {0.f, 0.f};   // sums of P of this warp's tokens for heads 64g + 32 h2 + lane
+#ifdef MLA_TC_TRACE
+    long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const long long prof_start = clock64();
+#endif
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int par = t & 1, slot = t & (kXSlots - 1);
@@ -1117,14 +1121,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         // of sub-tile q4 = part / 2). Rows past the range become zeros, so that P = 0 never
         // meets stale data.
         const int rr = stid & 31, part = stid >> 5, q4 = part >> 1, half = part & 1;
+#ifdef MLA_TC_TRACE
+        const long long pv0 = clock64();
+#endif
 #pragma unroll 1
         for (int v = 0; v < kVCh && ok; ++v) {
           const int n = t * kVCh + v;
           const int st = n % kNV, rv = n % Ly::RV;
           bool r = true;
           if (stid == 0) {
-            if (n >= kNV) r = wait_bar(&bars->v_free[st], ((n / kNV) - 1) & 1, cx);
-            if (r) r = wait_bar(&bars->rv_ready[rv], (n / Ly::RV) & 1, cx);
+            if (n >= kNV) PROF(0, r = wait_bar(&bars->v_free[st], ((n / kNV) - 1) & 1, cx));
+            if (r) PROF(1, r = wait_bar(&bars->rv_ready[rv], (n / Ly::RV) & 1, cx));
           }
           ok = bar_and(15, 256, r);
           if (!ok) break;
@@ -1154,9 +1161,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
             arrive_even(&bars->v_ready[st], rank);
           }
         }
+#ifdef MLA_TC_TRACE
+        prof[2] += clock64() - pv0;
+#endif
         if (!ok) break;
       }
     }
+#ifdef MLA_TC_TRACE
+    prof[7] = clock64() - prof_start;
+    if (stid == 0) PROF_STORE(568);
+#endif
     if (ok) {
       // ------------------------------------------------------------ epilogue
       if (stid == 0) ok = wait_bar(&bars->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
