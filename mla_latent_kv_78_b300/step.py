@@ -93,16 +93,21 @@ class DecodeStep:
         return self.o
 
     # -- the step as one CUDA graph ----------------------------------------
-    def capture(self, c_kv_new, k_r_new, q_c, q_r, timing: bool = False) -> None:
+    def capture(self, c_kv_new, k_r_new, q_c, q_r, timing: bool = False,
+                time_decode: bool = False) -> None:
         """Record append -> absorb -> decode -> unabsorb over these input tensors as one CUDA
         graph, so a step costs one graph launch instead of four host-side library calls. In the
-        graph the append and the absorption are independent branches that may overlap.
+        graph the append and the absorption are independent branches that may overlap, and the
+        decode and unabsorb kernels are programmatic launches that set up while their
+        predecessor finishes.
 
         The graph keeps the inputs' device addresses: write each step's inputs into the same
         tensors (copy_) before replay(). One eager step runs first, outside the capture, so
         the library's one-time per-process set-up never happens inside it. With timing=True
-        the graph also records events around the whole step and around mla_decode; read them
-        with step_ms() / decode_ms() after the replay has finished.
+        the graph records events at its start and end (read with step_ms()). time_decode=True
+        also records events around mla_decode (decode_ms()); an event between two kernels
+        turns their programmatic edge into a full dependency, so that graph is for timing the
+        decode alone, not the step.
         """
         dev = self.device
         side = torch.cuda.Stream(device=dev)
@@ -111,6 +116,7 @@ class DecodeStep:
             self.step(c_kv_new, k_r_new, q_c, q_r)
         torch.cuda.current_stream(dev).wait_stream(side)
         torch.cuda.synchronize(dev)
+        timing = timing or time_decode
         ev = ([torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
               if timing else None)
         graph = torch.cuda.CUDAGraph()
@@ -126,10 +132,10 @@ class DecodeStep:
                 self.append(c_kv_new, k_r_new)
             self.absorb(q_c, q_r)
             main.wait_stream(fork)
-            if ev:
+            if time_decode:
                 ev[1].record()
             self.decode()
-            if ev:
+            if time_decode:
                 ev[2].record()
             self.unabsorb()
             if ev:
