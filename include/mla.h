@@ -142,9 +142,9 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
                  int32_t num_tokens, const void* w_uk, void* q_lat, void* stream);
 
 /*
- * Workspace bytes mla_decode needs for these sizes (0 when the chosen kernel needs none:
- * the CUDA-core kernel without splits). The tensor-core kernel always needs some (its CTA
- * pairs exchange data through it).
+ * Workspace bytes mla_decode needs for these sizes: fp32 split partials when the rows are
+ * split over several CTA pairs (num_splits, or the automatic choice, above 1), and with an FP8
+ * cache an f16 copy of q_lat for the tensor-core kernel; 0 when neither applies.
  * num_splits as for mla_decode; max_seq_len bounds every seq_lens[b].
  */
 size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n_q,
