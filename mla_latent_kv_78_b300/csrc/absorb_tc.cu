@@ -92,15 +92,29 @@ __global__ void __launch_bounds__(128, 2)
     for (int j = 0; j < 4; ++j)
       tma_load_2d(sB + j * 16384, &tmW, (4 * half + j) * 64, i * kD, &bars[0], pol);
   }
-  // the first half's CTA also rotates q^R: fetch this token's row while the operands land
-  uint4 xr[kR / 8];
-  int pos = 0;
-  if (half == 0) {
-    const bool valid = t < nt;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q_r + ((size_t)(t0 + t) * p.H + i) * kR);
+  // the first half's CTA also rotates q^R while the operands land (a rolled loop: four
+  // sin/cos pairs of code per iteration), straight into q_lat's last 64 columns
+  const uint32_t rsw = (uint32_t)(t & 7);
+  if (half == 0 && t < nt) {
+    const size_t row = (size_t)(t0 + t) * p.H + i;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q_r + row * kR);
+    uint4* dst = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + kC);
+    const int pos = p.pos[t0 + t];
+#pragma unroll 1
+    for (int q = 0; q < kR / 8; ++q) {
+      const uint4 x = src[q];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o[4];
 #pragma unroll
-    for (int q = 0; q < kR / 8; ++q) xr[q] = valid ? src[q] : make_uint4(0, 0, 0, 0);
-    pos = valid ? p.pos[t0 + t] : 0;
+      for (int e = 0; e < 4; ++e) {
+        const int k = q * 4 + e;
+        float c, s;
+        rope_cs(pos, p.theta_hi[k], p.theta_lo[k], &c, &s);
+        const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
+        o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+      }
+      dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
   if (threadIdx.x == 0) {
     if (wait_bounded(&bars[0], 0, p.status)) {
@@ -117,28 +131,9 @@ __global__ void __launch_bounds__(128, 2)
   }
   wait_bounded(&bars[1], 0, p.status);
   tc_fence_after();
-  // The MMAs have read both operand buffers: each thread writes its token's row into them as
-  // 128-byte-swizzled boxes [128 tokens x 64 columns] (the W half's buffer takes the 256 latent
-  // columns, q_c's the 64 rotated ones), and TMA stores whole 128-byte row segments of q_lat.
-  const uint32_t rsw = (uint32_t)(t & 7);
-  if (half == 0) {
-    uint8_t* rowp = sA + t * 128;
-#pragma unroll 1
-    for (int q = 0; q < kR / 8; ++q) {
-      const uint4 x = xr[q];
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k = q * 4 + e;
-        float c, s;
-        rope_cs(pos, p.theta_hi[k], p.theta_lo[k], &c, &s);
-        const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
-        o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
-      }
-      *reinterpret_cast<uint4*>(rowp + ((uint32_t)q ^ rsw) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
+  // The MMAs have read the W half's buffer: each thread writes its token's row of each
+  // 64-column box into it (128-byte swizzle), and as soon as a box is complete one thread
+  // sends it to q_lat with a TMA store (whole 128-byte row segments) while the next is staged.
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
   for (int cc = 0; cc < 256 / 64; ++cc) {
@@ -153,17 +148,16 @@ __global__ void __launch_bounds__(128, 2)
           make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tma_store_3d(&tmL, sB + cc * 16384, half * 256 + cc * 64, i, t0);
+      bulk_commit_group();
+    }
   }
-  fence_proxy_async_smem();
   tc_fence_before();
+  if (threadIdx.x == 0) bulk_wait_read_all();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int j = 0; j < 4; ++j) tma_store_3d(&tmL, sB + j * 16384, half * 256 + j * 64, i, t0);
-    if (half == 0) tma_store_3d(&tmL, sA, kC, i, t0);
-    bulk_commit_group();
-    bulk_wait_read_all();
-  }
-  __syncwarp();
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
