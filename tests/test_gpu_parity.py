@@ -233,3 +233,29 @@ def test_empty_batch_and_empty_token_lists_are_noops():
     assert lib.mla_append_cache(cfg, None, None, None, None, 0, None, 1, 1, 1, None, None, None) == 0
     assert lib.mla_unabsorb(cfg, None, 0, None, None, None) == 0
     assert z.numel() == 0
+
+
+@needs_cuda
+def test_score_beyond_the_weight_range_is_flagged():
+    """The tensor-core decode clamps weights at 2^96 (bf16 P) above its running reference and
+    reports MLA_DEV_SCORE_RANGE: one cached token whose score jumps far above tile 0's scores
+    (raw score 30 * 40 = 1200, i.e. ~125 in log2 units after the 1/sqrt(192) scale) trips it.
+    One split, so that the token falls in a later tile than the one that sets the reference;
+    the same workload at ordinary scale leaves the status clear."""
+    wl = SMALL_BF16_LONG
+    case = Case(wl, num_splits=1)
+    case.run_step()
+    assert case.step.status() == 0
+    assert M.mla_decode_kernel(case.cfg, wl.B, wl.n_q) == M.MLA_KERNEL_TC
+    # token 600 of sequence 0 (tile 2): latent column 0 set to 40 in the bf16 pool entry
+    pos = 600
+    page = int(case.bt_np[0, pos // wl.P])
+    entry = case.step.pool[page, pos % wl.P].view(torch.bfloat16)
+    entry[0] = 40.0
+    q = case.step.q_lat.clone()
+    q[0, :, :] = 0
+    q[0, :, 0] = 30.0
+    case.step.dev_status.zero_()
+    case.step.decode(q)
+    torch.cuda.synchronize()
+    assert case.step.status() & M.MLA_DEV_SCORE_RANGE
