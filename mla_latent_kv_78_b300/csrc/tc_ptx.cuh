@@ -107,31 +107,6 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-// 16-byte asynchronous store into another CTA's shared memory; completes tx bytes
-// on that CTA's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
-                                            float d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(cluster_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Non-tensor bulk copy global -> this CTA's shared memory (16-byte aligned, size % 16 == 0),
-// completing `bytes` of tx on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -144,11 +119,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
-}
-
-// Bulk prefetch of [gaddr, gaddr + bytes) into L2 (bytes a multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void* gaddr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gaddr), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
