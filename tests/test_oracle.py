@@ -362,3 +362,97 @@ def test_page_slot_mapping():
     pg, sl = O.page_slots(np.array([0, 0, 1, 1, 1]), np.array([0, 17, 15, 16, 40]), bt, 16)
     np.testing.assert_array_equal(pg, [5, 2, 0, 4, 1])
     np.testing.assert_array_equal(sl, [0, 1, 15, 0, 8])
+
+
+# ---------------------------------------------------------------- storage rounding
+def _torch_bf16(x_f32: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 -> fp64 through torch's own conversion (an implementation independent of
+    the oracle's bit arithmetic)."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def test_round_bf16_matches_an_independent_rounding():
+    """round_bf16 is round-to-nearest-even from fp32 to bf16, the rounding every bf16 value of
+    the cache and of the activations goes through. Checked against torch's converter on random
+    fp32 values over a wide exponent range, both signs."""
+    g = _rng(40)
+    x = (g.standard_normal(200_000) * np.exp2(g.integers(-60, 60, 200_000))).astype(np.float32)
+    np.testing.assert_array_equal(O.round_bf16(x.astype(np.float64)), _torch_bf16(x))
+
+
+def test_round_bf16_ties_go_to_even():
+    """Exact halfway cases: the fp32 value's 16 dropped bits are exactly 0x8000. bf16 keeps 7
+    stored mantissa bits, so 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 (keeps the even 1),
+    and 1 + 3 * 2^-8 halfway between 1 + 2^-7 and 1 + 2^-6 (keeps the even 1 + 2^-6). One ulp
+    of fp32 to either side of a tie is not a tie. Worked by hand, then the same constructed
+    ties checked against torch over many exponents and mantissas."""
+    assert O.round_bf16(np.array([1 + 2.0 ** -8]))[0] == 1.0
+    assert O.round_bf16(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
+    assert O.round_bf16(np.array([-(1 + 2.0 ** -8)]))[0] == -1.0
+    assert O.round_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -23]))[0] == 1 + 2.0 ** -7
+    assert O.round_bf16(np.array([1 + 2.0 ** -8 - 2.0 ** -23]))[0] == 1.0
+    # a value that fp64 -> fp32 rounding moves onto a tie is rounded as the fp32 value says
+    assert O.round_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -40]))[0] == 1.0
+    g = _rng(41)
+    hi = g.integers(0, 1 << 16, 50_000, dtype=np.uint64) & np.uint64(0x7F7F)   # finite, any mantissa parity
+    bits = ((hi << np.uint64(16)) | np.uint64(0x8000)).astype(np.uint32)
+    ties = bits.view(np.float32)
+    got = O.round_bf16(ties.astype(np.float64))
+    np.testing.assert_array_equal(got, _torch_bf16(ties))
+    # every tie went to the neighbour whose last kept bit is 0
+    kept = (got.astype(np.float32).view(np.uint32) >> np.uint32(16)) & np.uint32(1)
+    assert not kept[np.abs(got) > 0].any()
+
+
+def test_cache_entries_hand_worked():
+    """What the cache holds for a token (「一文通透DeepSeek-V2」 §2.2.2: k^R_t = RoPE(W^{KR}h_t)
+    is cached, rotated at the token's own position, beside c^{KV}_t), worked by hand for
+    R = 4, base 10000 (theta_0 = 1, theta_1 = 0.01) at positions 0, 1 and 100.
+
+    bf16 and fp32 caches: c is the stored value of c^{KV}; k^R = (x0 cos a0 - x1 sin a0,
+    x0 sin a0 + x1 cos a0, x2 cos a1 - x3 sin a1, x2 sin a1 + x3 cos a1) with a0 = pos,
+    a1 = 0.01 pos, then rounded to the cache's storage type."""
+    c = np.array([[0.5, -1.25, 3.0, 0.0]] * 3)
+    k = np.array([[1.0, 2.0, -0.5, 0.25]] * 3)
+    pos = np.array([0, 1, 100])
+    expect = []
+    for p in pos:
+        a0, a1 = float(p), 0.01 * float(p)
+        expect.append([1.0 * math.cos(a0) - 2.0 * math.sin(a0), 1.0 * math.sin(a0) + 2.0 * math.cos(a0),
+                       -0.5 * math.cos(a1) - 0.25 * math.sin(a1), -0.5 * math.sin(a1) + 0.25 * math.cos(a1)])
+    expect = np.array(expect)
+    bf = O.cache_entries(c, k, pos, "bf16", 10000.0)
+    np.testing.assert_array_equal(bf["c"], c)                       # exact in bf16
+    np.testing.assert_array_equal(bf["k_r"], _torch_bf16(expect.astype(np.float32)))
+    np.testing.assert_array_equal(bf["k_r"][0], [1.0, 2.0, -0.5, 0.25])   # position 0: identity
+    f32 = O.cache_entries(c, k, pos, "f32", 10000.0)
+    np.testing.assert_allclose(f32["k_r"], expect, rtol=2.0 ** -23, atol=0)
+    assert f32["k_r"].dtype == np.float64 and np.all(f32["k_r"] == f32["k_r"].astype(np.float32))
+
+
+def test_cache_entries_fp8_group_hand_worked():
+    """One 1x128 group quantised by hand (「Deepseek系列从v3到R易背面经版」 F8量化策略).
+
+    Group x = (1, -2, 0.5, 3, 0, ..., 0): amax = 3, scale = 3/448. x / scale = 149.33, -298.67,
+    74.67, 448, 0. E4M3 spacing is 16 on [128, 256), 32 on [256, 448], 8 on [64, 128):
+    149.33 -> 144 = 1.125 * 2^7 (code 0 1110 001 = 0x71); -298.67 -> -288 = -1.125 * 2^8
+    (1 1111 001 = 0xF9); 74.67 -> 72 = 1.125 * 2^6 (0 1101 001 = 0x69); 448 = 1.75 * 2^8
+    (0 1111 110 = 0x7E). The cache then reads code value * scale. The second group is all
+    zeros: scale 1, every code 0. k^R stays bf16."""
+    C = 256
+    c = np.zeros((1, C))
+    c[0, :4] = [1.0, -2.0, 0.5, 3.0]
+    k = np.array([[1.0, 2.0, -0.5, 0.25]])
+    e = O.cache_entries(c, k, np.array([0]), "fp8", 10000.0)
+    scale = np.float32(3.0) / np.float32(448.0)
+    np.testing.assert_array_equal(e["scales"][0], [scale, np.float32(1.0)])
+    codes = np.zeros(C, dtype=np.uint8)
+    codes[:4] = [0x71, 0xF9, 0x69, 0x7E]
+    np.testing.assert_array_equal(e["codes"][0], codes)
+    want = np.zeros(C)
+    want[:4] = np.array([144.0, -288.0, 72.0, 448.0]) * float(scale)
+    np.testing.assert_array_equal(e["c"][0], want)
+    np.testing.assert_array_equal(e["k_r"][0], [1.0, 2.0, -0.5, 0.25])
