@@ -62,11 +62,6 @@ extern "C" {
 #define MLA_DEV_INDEX_OUT_OF_RANGE 1  /* page id / sequence id / position outside its table */
 #define MLA_DEV_BAD_SEQLEN 2          /* seq_lens[b] < n_q or > max_seq_len */
 #define MLA_DEV_TIMEOUT 4             /* a bounded barrier wait gave up; outputs invalid */
-#define MLA_DEV_SCORE_RANGE 8         /* tensor-core decode: a scaled score exceeded the
-                                         running maximum of its head (over the tiles two or
-                                         more before its own) by more than 66.5, a weight
-                                         ratio above 2^96; those weights were clamped and the
-                                         row's output is approximate */
 
 /* ---- element types ----------------------------------------------------- */
 #define MLA_F32 0
@@ -78,10 +73,13 @@ extern "C" {
 #define MLA_KERNEL_SIMT 1   /* generic CUDA-core kernel, any shape */
 #define MLA_KERNEL_TC 2     /* tcgen05/TMEM kernel: n_heads=128, d_latent=512, d_rope=64,
                                page_size=64, bf16 act, bf16 or FP8 cache, n_q in {1,2}.
-                               With an FP8 cache the operands are f16 (codes * scales,
-                               queries and softmax weights), so latents and absorbed
-                               queries must lie within f16 range (|x| < 65504); values
-                               below 2^-14 keep f16's subnormal precision only */
+                               Operands are bf16 (an FP8 cache is dequantised as
+                               code * scale in fp32, rounded once to bf16), accumulation
+                               fp32. The softmax is exact for any spread of finite scores:
+                               a unit whose scores jump beyond the kernel's running
+                               reference by more than 2^96 is computed again with the
+                               exact per-head maxima as the reference. Non-finite inputs
+                               give non-finite outputs. */
 
 typedef struct mla_config {
   int32_t n_heads;      /* H  = n_h                                               */
@@ -142,9 +140,9 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
                  int32_t num_tokens, const void* w_uk, void* q_lat, void* stream);
 
 /*
- * Workspace bytes mla_decode needs for these sizes: fp32 split partials when the rows are
- * split over several CTA pairs (num_splits, or the automatic choice, above 1), and with an FP8
- * cache an f16 copy of q_lat for the tensor-core kernel; 0 when neither applies.
+ * Workspace bytes mla_decode needs for these sizes: the fp32 split partials (one [C] output
+ * and one log-sum-exp per query row, head and split) when the rows are split over several
+ * ranges (num_splits, or the automatic choice, above 1); 0 otherwise.
  * num_splits as for mla_decode; max_seq_len bounds every seq_lens[b].
  */
 size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n_q,
@@ -206,7 +204,8 @@ int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, c
  *   - If mla_decode_workspace_size() for these sizes exceeds MLA_NOALLOC_SCRATCH_BYTES the call
  *     returns MLA_ERR_SCRATCH_LIMIT and launches nothing.
  *   - The first call on a device looks up the scratch's device address on that device (with
- *     it current); make that first call before any stream capture.
+ *     it current); make that first call before any stream capture. The lookup is repeated
+ *     when the device's context has changed since (after cudaDeviceReset).
  *   - Every call on a device shares the one array and leaves its contents behind. Nothing in it
  *     needs to start at zero (each call writes what it later reads), but calls whose work
  *     overlaps on the GPU (different streams, or different host threads) race on it: keep them

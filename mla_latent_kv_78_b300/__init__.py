@@ -9,7 +9,6 @@ from ._lib import (  # noqa: F401
     MLA_BF16,
     MLA_DEV_BAD_SEQLEN,
     MLA_DEV_INDEX_OUT_OF_RANGE,
-    MLA_DEV_SCORE_RANGE,
     MLA_DEV_TIMEOUT,
     MLA_F32,
     MLA_FP8_E4M3,

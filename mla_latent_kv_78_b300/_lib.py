@@ -29,7 +29,6 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 MLA_DEV_INDEX_OUT_OF_RANGE = 1
 MLA_DEV_BAD_SEQLEN = 2
 MLA_DEV_TIMEOUT = 4
-MLA_DEV_SCORE_RANGE = 8
 
 MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC = 0, 1, 2

@@ -269,12 +269,10 @@ cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, co
     p.theta_hi[k] = (float)th;
     p.theta_lo[k] = (float)(th - (double)p.theta_hi[k]);
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tca::absorb_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tca::kAbsSmem);
+  static std::atomic<bool> attr[kMaxDevices];
+  {
+    cudaError_t e = set_smem_limit_once(tca::absorb_tc_kernel, tca::kAbsSmem, attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   dim3 grid(d.H, 2, (T + tca::kAbsNT - 1) / tca::kAbsNT);
   tca::absorb_tc_kernel<<<grid, 128, tca::kAbsSmem, stream>>>(tmW, tmQ, tmL, p);
@@ -301,12 +299,10 @@ cudaError_t launch_unabsorb_tc(const Dims& d, const void* o_lat, int T, const vo
   p.H = d.H;
   p.o = o;
   p.status = nullptr;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tca::unabsorb_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tca::kUnSmem);
+  static std::atomic<bool> attr[kMaxDevices];
+  {
+    cudaError_t e = set_smem_limit_once(tca::unabsorb_tc_kernel, tca::kUnSmem, attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   dim3 grid(d.H, (T + tca::kUnNT - 1) / tca::kUnNT);
   cudaError_t e = launch_programmatic(tca::unabsorb_tc_kernel, grid, dim3(128), tca::kUnSmem, stream,

@@ -4,9 +4,11 @@
 // more device memory: an inference server's plugin interface whose memory pool is managed
 // elsewhere, a process that must not let a library call into cudaMalloc (which may block on the
 // device or fail under memory pressure in the middle of a decode loop), or a caller from a
-// runtime with no CUDA allocator binding at all. For them the decode's scratch (the CTA pairs'
-// exchange area and, with split-KV, the partial results) lives in a fixed array that is part of
-// this library's device image: every GPU that loads the library holds it until the process exits.
+// runtime with no CUDA allocator binding at all. For them the decode's scratch (the split-KV
+// partial outputs and log-sum-exps, which the decode needs only when it spreads a query row over
+// several CTA pairs) lives in a fixed array that is part of this library's device image: every
+// GPU that loads the library holds it until the process exits.
+#include <cuda.h>
 #include <mutex>
 
 #include "mla_internal.cuh"
@@ -14,27 +16,57 @@
 namespace {
 
 constexpr size_t kScratchBytes = MLA_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDev = 64;
 
-// The scratch itself. Host code never touches it by name: its device address is looked up once
-// per device below.
+// The scratch itself. Host code never touches it by name: its device address is looked up per
+// device below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// Device address of the scratch on the current device (looked up on this device's first call).
+// The driver's cuCtxGetCurrent, reached through the runtime (no link to libcuda needed).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+std::mutex g_setup_mu;
+struct ScratchEntry {
+  CUcontext ctx;   // the context the address belongs to
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxDev] = {};
+
+// Device address of the scratch in the current device's context. It is looked up on the first
+// call in a context and again whenever the context has changed since (a device reset tears
+// down the context the cached address belonged to).
 int scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MLA_ERR_CUDA;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return MLA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry& e = g_scratch[dev];
+  if (!ctx || !e.addr || e.ctx != ctx) {
+    // (the lookup also makes the device's primary context current if none was yet)
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) return MLA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    const cudaError_t rc = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (rc != cudaSuccess || !p) return MLA_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return MLA_ERR_CUDA;
+    e.ctx = ctx;
+    e.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = e.addr;
   return MLA_OK;
 }
 

@@ -18,12 +18,14 @@
 //  * The output is accumulated transposed, O^T[d_c][head] = V^T . P^T, again 2-SM
 //    (M = 256 latent rows per MMA, two MMAs per K step): each CTA holds half of O^T,
 //    256 TMEM columns, which leaves room for a double-buffered S^T (2 x 128 columns).
-//  * P^T is split by head: the CTA that computed a token's scores keeps its own head
-//    half and sends the other half (16 KB per tile) to the peer through a 4-slot exchange
-//    ring in global memory (normally L2), with a flag word and, rarely, the tile's maxima.
-//    Both CTAs take identical online-softmax decisions from the same data: the reference
-//    maximum of a head moves only when a tile's published maximum exceeds it by more than
-//    2^8, two tiles later, so the common tile needs no cross-thread reduction.
+//  * P^T is split by head: the CTA that computed a token's scores keeps its own head half and
+//    stores the other half (16 KB per tile) straight into the peer's shared memory (st.async),
+//    with the tile's per-head maxima when it publishes them. Both CTAs take identical
+//    online-softmax decisions from the same data: the reference maximum of a head moves only
+//    when a tile's published maximum exceeds it by more than 2^8, two tiles later, so the
+//    common tile needs no cross-thread reduction. A unit in which a weight ran beyond the
+//    range this lag leaves (2^96) is computed again with the exact maxima, so the result is
+//    exact for any spread of scores.
 //  * The key tile is read from HBM once, as [128 tokens x 64 dims] chunks for S^T; the
 //    latent part is read a second time, about a tile later, as [32 tokens x 256 d_c]
 //    chunks for O^T, normally from L2.
@@ -31,8 +33,8 @@
 //    retires them (~85 cycles per instruction against 64), two can.
 //  * Warp roles: w0 key-chunk TMA producer (+Q), w1 S^T issuer (even CTA) + TMEM owner,
 //    w2 latent-chunk producer (+ zeroing of rows past the range on the last tile),
-//    w3 exchange, w4..w11 softmax / epilogue (thread = TMEM lane; warps 4-7 heads 0-63,
-//    8-11 heads 64-127), w12 P.V issuer (even CTA).
+//    w3 P^T relay, w4..w11 softmax / epilogue (thread = TMEM lane; warps 4-7 heads 0-63,
+//    8-11 heads 64-127), w12 P.V issuer (even CTA); FP8 cache: w13..w15 convert the codes.
 //  * Every wait is bounded; a timeout sets MLA_DEV_TIMEOUT and every role winds down.
 #include <math_constants.h>
 #include <string.h>
@@ -50,17 +52,17 @@ constexpr int kTile = 256;           // tokens per tile (4 pages)
 constexpr int kKCh = kCR / 64;       // 9 dim chunks per tile
 constexpr int kVCh = kTile / 32;     // 8 latent chunks per tile
 constexpr int kPvWarp = 12;             // the P.V issuer
-constexpr int kCvtWarp0 = 13;           // FP8 cache: warps 13-15 convert codes to f16 tiles
+constexpr int kCvtWarp0 = 13;           // FP8 cache: warps 13-15 convert codes to bf16 tiles
 constexpr long long kTimeout = 4000000000LL;   // clock cycles (~2 s)
 constexpr int kXSlots = 4;    // slots for the peer's published tile maxima: tile t uses t % 4
 // Bytes the peer stores into this CTA's shared memory per tile (st.async, counted on
 // p_landed): its 128 token rows of this CTA's head half of P^T, and its per-head tile maxima.
 constexpr uint32_t kXBytes = 128 * 128 + kH * 4;
 constexpr float kLazy = 8.f;    // log2 units a score may exceed the reference before it moves
-// Larger excesses are clamped and flagged (MLA_DEV_SCORE_RANGE): bf16 P holds 2^96, f16 P
-// (FP8 cache) 2^15.
-template <bool F8>
-constexpr float kRange = F8 ? 15.f : 96.f;
+// Weights above 2^kRange relative to the lagging reference are clamped (P and the fp32 sums
+// would otherwise run out of range); a unit in which that happened runs again exactly (two
+// more passes: the exact per-head maxima, then the softmax with them as the reference).
+constexpr float kRange = 96.f;
 constexpr int kRawS = 8192 + 2048;   // FP8 key chunk: [128 tok x 64 codes] + [128 tok x 4 scales]
 constexpr int kRawV = 8192 + 512;    // FP8 latent chunk: 4 x [32 tok x 64 codes] + [32 tok x 4 scales]
 
@@ -78,15 +80,19 @@ constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for th
 constexpr int FL_ABORT = 2;    // a bounded wait gave up
 constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
 constexpr int FL_TICKET = 5;   // FP8 converters: the next job allowed to acquire its slots
-constexpr int F_END = F_FLAG + 8;   // (even: the barriers that follow need 8-byte alignment)
+constexpr int FL_CLAMP = 6;    // this pass clamped a weight of this CTA's tokens (see kRange)
+constexpr int FL_REPLAY = 7;   // the unit runs again exactly (set in both CTAs alike)
+constexpr int FL_PEER_CLAMP = 8;   // the peer's FL_CLAMP, received with its epilogue sums
+constexpr int FL_PEER_ABORT = 9;   // the peer's FL_ABORT at the end of a pass
+constexpr int F_END = F_FLAG + 10;   // (even: the barriers that follow need 8-byte alignment)
 // Shared-memory layout. bf16 cache: keys and latents arrive by TMA in their MMA layout.
 // FP8 cache: raw codes and scales arrive by TMA in staging rings (RS, RV slots) and the
-// converter warps write f16 operand tiles into the S and V rings.
+// converter warps write bf16 operand tiles into the S and V rings.
 template <bool F8>
 struct Lay {
   // bf16: Q travels with every key chunk (a [64 heads x 64 dims] box read from L2 next to the
   // [128 tokens x 64 dims] key box), which frees 72 KB for deeper rings and two P^T buffers.
-  // FP8: Q stays resident (the converters turn it into f16 once).
+  // FP8: Q stays resident.
   static constexpr bool QRES = F8;
   static constexpr int SSTAGE = QRES ? 16384 : 16384 + 8192;   // S-phase stage bytes
   static constexpr int NS = F8 ? 2 : 4;     // S-phase ring
@@ -111,7 +117,7 @@ struct BarsT {
   static constexpr int RS = Lay<F8>::RS > 0 ? Lay<F8>::RS : 1;
   static constexpr int RV = Lay<F8>::RV > 0 ? Lay<F8>::RV : 1;
   uint64_t q_ready;
-  uint64_t q_conv;       // FP8: both CTAs' Q halves converted to f16 (even CTA, 2 arrivals)
+  uint64_t q_conv;       // FP8: both CTAs' resident Q halves have landed (even CTA, 2 arrivals)
   uint64_t s_ready[NS], s_free[NS];
   uint64_t v_landed[NV], v_ready[NV], v_free[NV];
   uint64_t rs_ready[RS], rs_free[RS], rv_ready[RV], rv_free[RV];
@@ -197,14 +203,8 @@ __device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_
 #define PROF_STORE(base) ((void)0)
 #endif
 
-// One 16-bit weight (bf16, or f16 with an FP8 cache) -> fp32, exactly.
-template <bool F8>
-__device__ __forceinline__ float p16_to_f32(uint32_t h) {
-  if constexpr (F8)
-    return f16_to_f32(h);
-  else
-    return __uint_as_float(h << 16);
-}
+// One bf16 weight -> fp32, exactly.
+__device__ __forceinline__ float p16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 // Sum over the warp's 32 lanes of each of 32 values per lane; lane j returns the sum of
 // value j. Halving exchange: at each step a lane keeps one half of its values, sends the
@@ -259,38 +259,11 @@ __device__ __forceinline__ void arrive_even(uint64_t* bar, uint32_t rank) {
     mbar_arrive_remote(mapa(smem_u32(bar), 0));
 }
 
+// Barrier set-up of one pass (one thread of each CTA).
 template <bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
-    decode_kernel(const __grid_constant__ Maps maps, const Params prm) {
+__device__ __forceinline__ void init_barriers(BarsT<F8>* bars) {
+  constexpr int kNS = Lay<F8>::NS, kNV = Lay<F8>::NV;
   using Ly = Lay<F8>;
-  using Bars = BarsT<F8>;
-  constexpr int kNS = Ly::NS, kNV = Ly::NV, kThreads = Ly::THREADS;
-  constexpr int OFF_Q = Ly::OFF_Q, OFF_S = Ly::OFF_S, OFF_V = Ly::OFF_V, OFF_P = Ly::OFF_P;
-  constexpr int kSStage = Ly::SSTAGE, kPB = Ly::PB;
-  constexpr int OFF_F = Ly::OFF_F, OFF_BAR = Ly::OFF_BAR;
-  const CUtensorMap& tmQ = maps.q;
-  const CUtensorMap& tmK = maps.k;
-  const CUtensorMap& tmV = maps.v;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
-  float* fs = reinterpret_cast<float*>(sm + OFF_F);
-  int* flags = reinterpret_cast<int*>(fs + F_FLAG);
-  Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t peer = rank ^ 1u;
-
-  // ---- which (sequence, query row, split) this pair owns
-  const int unit = blockIdx.x >> 1;
-  const int split = unit % prm.S;
-  const int row = unit / prm.S;           // b * n_q + j
-  const int b = row / prm.n_q, j = row % prm.n_q;
-  // ---- set-up
-  if (tid == 0) TRACE(11, 0);
-  if (tid == 0) {
     // *_ready live in the even CTA: one arrival (its producer registers both CTAs' bytes)
     // plus the bytes of both CTAs' loads, which signal it directly
     // (FP8 cache: each CTA's converter warps arrive once on the even CTA's s_ready / v_ready
@@ -325,23 +298,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     mbar_init(&bars->l_landed, 1);
     mbar_init(&bars->teardown, 2);   // both issuing threads' last commits
     fence_mbarrier_init_cluster();
-  }
-  if (tid < kH) fs[F_M + tid] = -CUDART_INF_F;
-  if (tid < F_END - F_FLAG) flags[tid] = 0;
-  if (warp == 1) {
-    tmem_alloc_pair(&bars->tmem_base, 512);
-    tmem_relinquish_pair();
-  }
-  __syncthreads();
-  cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
+}
+
+// One pass over this pair's unit. mode 0 is the ordinary pass; modes 1 and 2 run only when
+// mode 0 had to clamp a weight (see kRange): 1 computes the scores alone, for the exact
+// per-head maxima, 2 is the ordinary pass with those maxima as the reference.
+template <bool F8>
+__device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm, uint8_t* sm, const int mode) {
+  using Ly = Lay<F8>;
+  using Bars = BarsT<F8>;
+  constexpr int kNS = Ly::NS, kNV = Ly::NV, kThreads = Ly::THREADS;
+  constexpr int OFF_Q = Ly::OFF_Q, OFF_S = Ly::OFF_S, OFF_V = Ly::OFF_V, OFF_P = Ly::OFF_P;
+  constexpr int kSStage = Ly::SSTAGE, kPB = Ly::PB;
+  constexpr int OFF_F = Ly::OFF_F, OFF_BAR = Ly::OFF_BAR;
+  const CUtensorMap& tmQ = maps.q;
+  const CUtensorMap& tmK = maps.k;
+  const CUtensorMap& tmV = maps.v;
+  float* fs = reinterpret_cast<float*>(sm + OFF_F);
+  int* flags = reinterpret_cast<int*>(fs + F_FLAG);
+  Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+
+  // ---- which (sequence, query row, split) this pair owns
+  const int unit = blockIdx.x >> 1;
+  const int split = unit % prm.S;
+  const int row = unit / prm.S;           // b * n_q + j
+  const int b = row / prm.n_q, j = row % prm.n_q;
   Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status};
-  // Everything above touches only this pair's own shared memory and TMEM, so with a
-  // programmatic launch it overlaps the tail of the preceding kernel on the stream; every
-  // read of the inputs comes after that kernel has completed.
-  griddep_launch_dependents();
-  griddep_wait();
+  const uint32_t tmem = bars->tmem_base;
   const int L = prm.seq_lens[b];
   const bool bad_len = (L < prm.n_q || L > prm.max_seq_len);
   const int visible = bad_len ? 0 : L - prm.n_q + j + 1;
@@ -409,22 +397,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     auto at_even = [&](uint64_t* bar) { return mapa(smem_u32(bar), 0); };
     if (leader) {
       prefetch_tensormap(&tmQ);
-      const uint64_t pol_q = policy_evict_last();
       if constexpr (F8) {
         prefetch_tensormap(&maps.cs);
         prefetch_tensormap(&maps.ss);
         prefetch_tensormap(&maps.kr);
         prefetch_tensormap(&maps.cv);
         prefetch_tensormap(&maps.sv);
-        // each CTA's converters turn their own Q half into f16: a CTA-local barrier
+        // each CTA's resident Q half: a CTA-local barrier, relayed to the even CTA's q_conv
         mbar_arrive_expect_tx(&bars->q_ready, kKCh * 8192);
-        for (int c = 0; c < kKCh; ++c)
-          tma_load_2d(sm + OFF_Q + c * 8192, &tmQ, c * 64, row * kH + (int)rank * 64, &bars->q_ready,
-                      pol_q);
       } else {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
       }
+    }
+    if constexpr (F8) {
+      // one box per lane: TMA loads issued by one thread complete one after another, which
+      // the FP8 cache's many small boxes (codes, scales, RoPE keys) feel most
+      __syncwarp();
+      if (lane < kKCh)
+        tma_load_2d(sm + OFF_Q + lane * 8192, &tmQ, lane * 64, row * kH + (int)rank * 64, &bars->q_ready,
+                    policy_evict_last());
     }
     int s_cnt = 0;
 #ifdef MLA_TC_TRACE
@@ -450,26 +442,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     // FP8 cache: raw key chunks (codes + scales of this CTA's 128 tokens, or one page of
     // bf16 RoPE keys) into the staging ring, for the converter warps
     int m_cnt = 0;
-    auto load_raw_s = [&](bool rope, int c, int y0, int y1) -> bool {
+    auto load_raw_s = [&](bool rope, int c, int y0, int y1) -> bool {   // whole warp
       constexpr int RS = Bars::RS;   // >= 1 (the bf16 cache never calls this)
       const int st = m_cnt % RS;
+      const int q = lane - 4 * (m_cnt & 7);   // the chunk's boxes, one lane each
       bool r = true;
-      if (m_cnt >= RS) PROF(0, r = wait_bar(&bars->rs_free[st], ((m_cnt / RS) - 1) & 1, cx));
-      if (!r) return false;
-      uint8_t* dst = sm + Ly::OFF_RS + st * kRawS;
-      uint64_t* bar = &bars->rs_ready[st];
-      if (!rope) {
-        mbar_arrive_expect_tx(bar, kRawS);
-        tma_load_2d(dst, &maps.cs, c * 64, y0, bar, pol_s);
-        tma_load_2d(dst + 4096, &maps.cs, c * 64, y1, bar, pol_s);
-        tma_load_2d(dst + 8192, &maps.ss, kC + 2 * kR, y0, bar, pol_s);
-        tma_load_2d(dst + 8192 + 1024, &maps.ss, kC + 2 * kR, y1, bar, pol_s);
-      } else {
-        mbar_arrive_expect_tx(bar, 8192);
-        tma_load_2d(dst, &maps.kr, kC, y0, bar, pol_s);
+      if (q >= 0 && q < (rope ? 1 : 4)) {
+        if (m_cnt >= RS) PROF(0, r = wait_bar(&bars->rs_free[st], ((m_cnt / RS) - 1) & 1, cx));
+        if (r) {
+          uint8_t* dst = sm + Ly::OFF_RS + st * kRawS;
+          uint64_t* bar = &bars->rs_ready[st];
+          if (q == 0) mbar_arrive_expect_tx(bar, rope ? 8192 : kRawS);
+          if (rope)
+            tma_load_2d(dst, &maps.kr, kC, y0, bar, pol_s);
+          else if (q < 2)
+            tma_load_2d(dst + q * 4096, &maps.cs, c * 64, q ? y1 : y0, bar, pol_s);
+          else
+            tma_load_2d(dst + 8192 + (q - 2) * 1024, &maps.ss, kC + 2 * kR, q == 3 ? y1 : y0, bar, pol_s);
+        }
       }
       ++m_cnt;
-      return true;
+      return __all_sync(0xffffffffu, r);
     };
     // key chunks of every tile in order (the latent chunks have their own producer)
     bool ok = true;
@@ -478,8 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       const int ys1 = page_y(4 * k + 2 * (int)rank + 1);
       if constexpr (F8) {
         for (int c = 0; c < kKCh + 1 && ok; ++c) {   // 8 latent chunks, 2 RoPE half chunks
-          if (leader) ok = c < 8 ? load_raw_s(false, c, ys0, ys1) : load_raw_s(true, 0, c == 8 ? ys0 : ys1, 0);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = c < 8 ? load_raw_s(false, c, ys0, ys1) : load_raw_s(true, 0, c == 8 ? ys0 : ys1, 0);
         }
       } else {
         for (int c = 0; c < kKCh && ok; ++c) {
@@ -508,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     // their own issuing thread (warp 12): one thread cannot issue 2-SM MMAs as fast as the
     // tensor pipe retires them, two can.
     if (rank == 0 && lane == 0) {
-      const uint32_t idS = F8 ? idesc_f16_f32(256, 128, 0, 0) : idesc_bf16_f32(256, 128, 0, 0);
+      const uint32_t idS = idesc_bf16_f32(256, 128, 0, 0);
       // operand descriptors; an operand's start moves by adding (byte offset >> 4)
       const uint64_t dS = smem_desc(smem_u32(sm + OFF_S), 16, 1024, kSw128);
       // bf16: each stage holds its Q chunk after the key chunk; FP8: Q is resident
@@ -520,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       const long long prof_start = clock64();
 #endif
-      // bf16: both CTAs' Q halves have landed; FP8: both have also been converted to f16
+      // bf16: Q travels with the key chunks; FP8: both CTAs' resident Q halves have landed
       bool ok = F8 ? wait_bar<true>(&bars->q_conv, 0, cx) : true;
       for (int t = 0; t < nt && ok; ++t) {
         TRACE(22, t);
@@ -570,7 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     // ================================================================ P.V issuer (even CTA)
     // O^T += V^T(t) . P^T(t) for every tile once both CTAs' P^T halves are in place.
     if (rank == 0 && lane == 0) {
-      const uint32_t idPV = F8 ? idesc_f16_f32(256, 128, 1, 1) : idesc_bf16_f32(256, 128, 1, 1);
+      const uint32_t idPV = idesc_bf16_f32(256, 128, 1, 1);
       const uint64_t dV = smem_desc(smem_u32(sm + OFF_V), 4096, 1024, kSw128);
       const uint64_t dP = smem_desc(smem_u32(sm + OFF_P), 8192, 1024, kSw128);
       uint32_t v_st = 0, v_ph = 0;
@@ -580,7 +572,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       const long long prof_start = clock64();
 #endif
       bool ok = true;
-      for (int t = 0; t < nt && ok; ++t) {
+      const int nt_pv = mode == 1 ? 0 : nt;   // the scores-only pass issues no P.V
+      for (int t = 0; t < nt_pv && ok; ++t) {
         TRACE(23, t);
         PROF(6, ok = wait_bar<true>(&bars->p_ready[t & 1], (t >> 1) & 1, cx));
         if (!ok) break;
@@ -622,7 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       mma_commit_pair(&bars->teardown, 0x1);
       wait_drain(&bars->teardown, 0);
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 && mode != 1) {
     // ================================================================ latent-chunk producer
     // Loads each tile's latent rows (this CTA's 256 d_c columns, 32 tokens per chunk) in the
     // MMA issuer's order. On the last tile the rows past the range may hold anything (P is 0
@@ -711,21 +704,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       for (int t = 0; t < nt && ok; ++t) {
         for (int v = 0; v < kVCh && ok; ++v) {
           const int y = page_y(4 * t + (v >> 1)) + (v & 1) * 32;   // whole warp
-          if (lane == 0) {
+          const int q = lane - 5 * (k_cnt % 6);   // four code boxes and the scales, one lane each
+          bool r = true;
+          if (q >= 0 && q < 5) {
             const int st = k_cnt % Ly::RV;
-            if (k_cnt >= Ly::RV) ok = wait_bar(&bars->rv_free[st], ((k_cnt / Ly::RV) - 1) & 1, cx);
-            if (ok) {
+            if (k_cnt >= Ly::RV) r = wait_bar(&bars->rv_free[st], ((k_cnt / Ly::RV) - 1) & 1, cx);
+            if (r) {
               uint8_t* dst = sm + Ly::OFF_RV + st * kRawV;
               uint64_t* bar = &bars->rv_ready[st];
-              mbar_arrive_expect_tx(bar, kRawV);
-              for (int q4 = 0; q4 < 4; ++q4)
-                tma_load_2d(dst + q4 * 2048, &maps.cv, (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64,
-                            y, bar, pol_v);
-              tma_load_2d(dst + 8192, &maps.sv, kC + 2 * kR, y, bar, pol_v);
+              if (q == 0) mbar_arrive_expect_tx(bar, kRawV);
+              if (q < 4)
+                tma_load_2d(dst + q * 2048, &maps.cv, (q >> 1) * 256 + (int)rank * 128 + (q & 1) * 64, y,
+                            bar, pol_v);
+              else
+                tma_load_2d(dst + 8192, &maps.sv, kC + 2 * kR, y, bar, pol_v);
             }
           }
           ++k_cnt;
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = __all_sync(0xffffffffu, r);
         }
       }
     }
@@ -736,10 +732,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   } else if (warp >= kCvtWarp0) {
     // ================================================================ FP8 converters
     // Dequantisation of the FP8 cache, 「Deepseek系列从v3到R易背面经版」 F8量化策略 (per-token
-    // 1x128 groups): value = code * scale of its group, produced here as f16 operand tiles in
-    // the MMA's swizzled layout. The three warps first turn this CTA's Q half into f16, then
+    // 1x128 groups): value = code * scale of its group, taken in fp32 and rounded once to bf16,
+    // produced here as bf16 operand tiles in the MMA's swizzled layout (bf16 keeps fp32's
+    // exponent range, so no scale or value is limited to a narrower range). The three warps
     // share the key chunks of every tile in order (9 per tile, the ninth being the bf16 RoPE
-    // keys): warp w takes every third chunk and converts it alone. Chunks acquire their slots
+    // keys, copied into the swizzled layout): warp w takes every third chunk alone. Chunks acquire their slots
     // (the staging chunk and the free operand slot) strictly in order, through a ticket: a
     // barrier is then never waited on more than one phase ahead of the phase it is in, which
     // its parity test could not tell from the phase before; the conversions themselves
@@ -747,20 +744,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     if constexpr (F8) {
       const int cw = warp - kCvtWarp0;      // 0..2
       const int ct = tid - kCvtWarp0 * 32;   // 0..95
-      // codes (8 per item) x one scale -> 8 f16
-      auto cvt8 = [](uint2 codes, uint32_t sc2) -> uint4 {
-        return make_uint4(mul_f16x2(e4m3x2_to_f16x2(codes.x), sc2),
-                          mul_f16x2(e4m3x2_to_f16x2(codes.x >> 16), sc2),
-                          mul_f16x2(e4m3x2_to_f16x2(codes.y), sc2),
-                          mul_f16x2(e4m3x2_to_f16x2(codes.y >> 16), sc2));
+      // codes (8 per item) x one fp32 scale -> 8 bf16
+      auto cvt8 = [](uint2 codes, float sc) -> uint4 {
+        return make_uint4(e4m3x2_scaled_bf16x2(codes.x, sc), e4m3x2_scaled_bf16x2(codes.x >> 16, sc),
+                          e4m3x2_scaled_bf16x2(codes.y, sc), e4m3x2_scaled_bf16x2(codes.y >> 16, sc));
       };
-      auto bf16x8_to_f16x8 = [](uint4 w) -> uint4 {
-        auto one = [](uint32_t x) {
-          return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-        };
-        return make_uint4(one(w.x), one(w.y), one(w.z), one(w.w));
-      };
-      auto scale2 = [](float sc) -> uint32_t { return pack_f16x2(sc, sc); };
 #ifdef MLA_TC_TRACE
       long long prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       const long long prof_start = clock64();
@@ -768,13 +756,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       bool ok = true;
       if (ct == 0) ok = wait_bar(&bars->q_ready, 0, cx);
       ok = bar_and(10, 96, ok);
-      if (ok) {
-        uint4* q = reinterpret_cast<uint4*>(sm + OFF_Q);
-        for (int x = ct; x < kKCh * 8192 / 16; x += 96) q[x] = bf16x8_to_f16x8(q[x]);
-        fence_proxy_async_smem();
-        bar_sync(11, 96);
-        if (ct == 0) arrive_even(&bars->q_conv, rank);
-      }
+      // Q needs no conversion (bf16 already): report this CTA's half as landed
+      if (ok && ct == 0) arrive_even(&bars->q_conv, rank);
       // lane 0: wait until job J is next to acquire its slots
       volatile int* ticket = &flags[FL_TICKET];
       auto my_turn = [&](int J) -> bool {
@@ -816,7 +799,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int rr = lane + 32 * k;
-            const uint32_t s2 = scale2(*reinterpret_cast<const float*>(src + 8192 + rr * 16 + (c >> 1) * 4));
+            const float s2 = *reinterpret_cast<const float*>(src + 8192 + rr * 16 + (c >> 1) * 4);
             uint4 in[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -843,7 +826,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int u = (j + rr) & 7;
-              *reinterpret_cast<uint4*>(dst + rr * 128 + ((u ^ (rr & 7)) << 4)) = bf16x8_to_f16x8(w[j]);
+              *reinterpret_cast<uint4*>(dst + rr * 128 + ((u ^ (rr & 7)) << 4)) = w[j];
             }
           }
         }
@@ -861,7 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       if (lane == 0) PROF_STORE(544 + 8 * cw);
 #endif
     }
-  } else if (warp == 3) {
+  } else if (warp == 3 && mode != 1) {
     // ================================================================ P^T relay
     // This CTA's P^T buffer of tile t is complete once its own softmax warps have written their
     // rows and the peer's rows and maxima have landed (p_landed); the relay makes the peer's
@@ -904,6 +887,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     const long long prof_start = clock64();
 #endif
     bool ok = true;
+    if (mode == 1) {
+      // ---- scores only: the exact per-head maxima of this range. Lane j of each warp keeps
+      // the running maxima of heads 64g + j and 64g + 32 + j over the warp's tokens; the
+      // warps, then the two CTAs, combine them into F_M, which the next pass uses as its
+      // reference from the first tile on.
+      float run[2] = {-CUDART_INF_F, -CUDART_INF_F};
+      for (int t = 0; t < nt; ++t) {
+        const int par = t & 1;
+        bool ok1 = true;
+        if (stid == 0) ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
+        ok = bar_and(1, 256, ok1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t s_addr = lane_addr + par * 128 + 64 * g;
+        const bool valid = lo + t * kTile + (int)rank * 128 + i < hi;
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float sv[32];
+          tmem_ld32(s_addr + 32 * h2, sv);
+          tmem_ld_wait();
+          if (h2 == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0)
+                mbar_arrive(&bars->s_empty[par]);
+              else
+                mbar_arrive_remote_relaxed(mapa(smem_u32(&bars->s_empty[par]), 0));
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float mx = warp_max_f32(valid ? sv[c] * prm.scale_log2 : -CUDART_INF_F);
+            if (lane == c) run[h2] = fmaxf(run[h2], mx);
+          }
+        }
+      }
+      if (ok) {
+        fs[F_COL + sw * 64 + lane] = run[0];
+        fs[F_COL + sw * 64 + 32 + lane] = run[1];
+        bar_sync(2, 256);
+        float my_max = -CUDART_INF_F;
+        if (stid < kH) {
+          const int h = stid, gg = h >> 6, cc = h & 63;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) my_max = fmaxf(my_max, fs[F_COL + (gg * 4 + q) * 64 + cc]);
+          st_async_b32(mapa(smem_u32(fs + F_X0 + h), peer), __float_as_uint(my_max),
+                       mapa(smem_u32(&bars->x0_ready), peer));
+        }
+        bool okx = true;
+        if (stid == 0) {
+          mbar_arrive_expect_tx(&bars->x0_ready, kH * 4);
+          okx = wait_bar<true>(&bars->x0_ready, 0, cx);
+        }
+        ok = bar_and(13, 256, okx);
+        if (ok && stid < kH) fs[F_M + stid] = fmaxf(my_max, fs[F_X0 + stid]);
+      }
+    } else {
     for (int t = 0; t < nt; ++t) {
       const int par = t & 1, slot = t & (kXSlots - 1);
       peer_landed = mapa(smem_u32(&bars->p_landed[par]), peer);
@@ -938,7 +979,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
       const uint32_t s_addr = lane_addr + par * 128 + 64 * g;
       const int tok = lo + t * kTile + (int)rank * 128 + i;
       const bool valid = tok < hi;
-      if (t == 0) {
+      if (t == 0 && mode == 0) {
         // ---- the first reference: per-head maxima over both CTAs' tokens of tile 0
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -1008,24 +1049,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           for (int e = 0; e < 4; ++e) {
             float d = (valid ? s[4 * c4 + e] * prm.scale_log2 : -CUDART_INF_F) - m[e];
             over |= d > kLazy;
-            extreme |= d > kRange<F8>;
-            d = fminf(d, kRange<F8>);
+            extreme |= d > kRange;
+            d = fminf(d, kRange);
             p[e] = ex2(d);
           }
-          pk[16 * h2 + 2 * c4] = F8 ? pack_f16x2(p[0], p[1]) : pack_bf16x2(p[0], p[1]);
-          pk[16 * h2 + 2 * c4 + 1] = F8 ? pack_f16x2(p[2], p[3]) : pack_bf16x2(p[2], p[3]);
+          pk[16 * h2 + 2 * c4] = pack_bf16x2(p[0], p[1]);
+          pk[16 * h2 + 2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
         }
         float v[32];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          v[2 * c] = p16_to_f32<F8>(pk[16 * h2 + c] & 0xFFFFu);
-          v[2 * c + 1] = p16_to_f32<F8>(pk[16 * h2 + c] >> 16);
+          v[2 * c] = p16_to_f32(pk[16 * h2 + c] & 0xFFFFu);
+          v[2 * c + 1] = p16_to_f32(pk[16 * h2 + c] >> 16);
         }
         const float lsum = warp_transpose_sum32(v, lane);
         if (rescale) l_w[h2] *= fs[F_ALPHA + 64 * g + 32 * h2 + lane];
         l_w[h2] += lsum;
       }
-      if (extreme) flag_status(prm.status, MLA_DEV_SCORE_RANGE);
+      if (extreme) flags[FL_CLAMP] = 1;
       if (stid == 0) TRACE(14, t);
       // P^T's buffer (in both CTAs) is free once P.V of tile t - kPB is done; O is stable to
       // rescale once P.V of the previous tile is
@@ -1044,7 +1085,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const uint32_t w = pk[c >> 1];
-          const float pv = p16_to_f32<F8>((c & 1) ? (w >> 16) : (w & 0xFFFFu));
+          const float pv = p16_to_f32((c & 1) ? (w >> 16) : (w & 0xFFFFu));
           const float mx = warp_max_f32(pv);
           if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
         }
@@ -1140,7 +1181,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           const bool valid = lo + t * kTile + v * 32 + rr < hi;
           const float sc = *reinterpret_cast<const float*>(src + 8192 + rr * 16 +
                                                            ((q4 < 2 ? 0 : 2) + (int)rank) * 4);
-          const uint32_t s2 = pack_f16x2(sc, sc);
           const uint4* in = reinterpret_cast<const uint4*>(src + q4 * 2048 + rr * 64 + half * 32);
           const uint4 a0 = in[0], a1 = in[1];
           const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1148,10 +1188,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t u = (uint32_t)(half * 4 + k) ^ (uint32_t)(rr & 7);
-            const uint4 o = make_uint4(mul_f16x2(e4m3x2_to_f16x2(w[2 * k]), s2),
-                                       mul_f16x2(e4m3x2_to_f16x2(w[2 * k] >> 16), s2),
-                                       mul_f16x2(e4m3x2_to_f16x2(w[2 * k + 1]), s2),
-                                       mul_f16x2(e4m3x2_to_f16x2(w[2 * k + 1] >> 16), s2));
+            const uint4 o = make_uint4(e4m3x2_scaled_bf16x2(w[2 * k], sc),
+                                       e4m3x2_scaled_bf16x2(w[2 * k] >> 16, sc),
+                                       e4m3x2_scaled_bf16x2(w[2 * k + 1], sc),
+                                       e4m3x2_scaled_bf16x2(w[2 * k + 1] >> 16, sc));
             *reinterpret_cast<uint4*>(dst + u * 16) = valid ? o : z;
           }
           fence_proxy_async_smem();
@@ -1193,11 +1233,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         }
         bool ok4 = true;
         if (stid == 0) {
-          mbar_arrive_expect_tx(&bars->l_landed, kH * 4);
+          // with the sums goes this CTA's clamp flag, so that both CTAs take the same decision
+          st_async_b32(mapa(smem_u32(&flags[FL_PEER_CLAMP]), peer), (uint32_t)flags[FL_CLAMP],
+                       peer_l_bar);
+          mbar_arrive_expect_tx(&bars->l_landed, kH * 4 + 4);
           ok4 = wait_bar<true>(&bars->l_landed, 0, cx);
         }
         ok4 = bar_and(14, 256, ok4);
-        if (ok4 && stid < kH) {
+        // a clamped weight in either CTA: the outputs of this pass are not written, the unit
+        // runs again exactly
+        const bool replay = mode == 0 && (flags[FL_CLAMP] | flags[FL_PEER_CLAMP]) != 0;
+        if (replay && stid == 0) flags[FL_REPLAY] = 1;
+        if (ok4 && !replay && stid < kH) {
           const int h = stid;
           const float mine = fs[F_LLOC + h], other = fs[F_LRCV + h];
           const float Lsum = rank == 0 ? mine + other : other + mine;
@@ -1214,7 +1261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
           }
         }
         ok = bar_and(9, 256, ok4);
-        if (ok) {
+        if (ok && !replay) {
 #pragma unroll 1
           for (int blk = 0; blk < 2; ++blk) {
             const int dc = blk * 256 + (int)rank * 128 + i;
@@ -1238,14 +1285,126 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
         }
       }
     }
+    }
+  }
+
+}
+
+// End of a pass. Both CTAs decide from both CTAs' abort flags and from the replay flag (which
+// both derived from the same exchanged data), so they always meet at the same cluster barriers.
+// Returns whether another pass follows; if so, the barriers and flags are set up for it.
+template <bool F8>
+__device__ __forceinline__ bool end_of_pass(int mode, uint8_t* sm) {
+  float* fs = reinterpret_cast<float*>(sm + Lay<F8>::OFF_F);
+  int* flags = reinterpret_cast<int*>(fs + F_FLAG);
+  BarsT<F8>* bars = reinterpret_cast<BarsT<F8>*>(sm + Lay<F8>::OFF_BAR);
+  const int tid = threadIdx.x;
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) st_cluster_u32(mapa(smem_u32(&flags[FL_PEER_ABORT]), cluster_ctarank() ^ 1u), (uint32_t)flags[FL_ABORT]);
+  cluster_sync();
+  const bool again = flags[FL_ABORT] == 0 && flags[FL_PEER_ABORT] == 0 &&
+                     (mode == 1 || (mode == 0 && flags[FL_REPLAY] != 0));
+  if (!again) return false;
+  __syncthreads();   // every thread has read the flags
+  if (tid == 0) {
+    // every operation of the pass has completed and been waited for, except the arrivals that
+    // MMA commits make on barriers nobody waits on at the end (the last stages' "free"
+    // signals): give those a moment to land before the barriers are initialised again
+    const long long t0 = clock64();
+    while (clock64() - t0 < 4000) {
+    }
+    init_barriers<F8>(bars);
+  }
+  if (tid < F_END - F_FLAG) flags[tid] = 0;
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  return true;
+}
+
+// The same pass as an out-of-line function (the FP8 cache's passes run through it: measured
+// faster there than the pass inlined into the kernel).
+template <bool F8>
+__device__ __noinline__ void decode_pass_ool(const Maps& maps, const Params& prm, uint8_t* sm, int mode) {
+  decode_pass<F8>(maps, prm, sm, mode);
+}
+
+// The two extra passes of a unit whose first pass clamped a weight, out of line so that the
+// bf16 cache's ordinary pass stays straight-line code in the kernel.
+template <bool F8>
+__device__ __noinline__ void replay_passes(const Maps& maps, const Params& prm, uint8_t* sm) {
+  decode_pass<F8>(maps, prm, sm, 1);
+  if (end_of_pass<F8>(1, sm)) {
+    decode_pass<F8>(maps, prm, sm, 2);
+    end_of_pass<F8>(2, sm);
+  }
+}
+
+template <bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
+    decode_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params prm) {
+  using Ly = Lay<F8>;
+  using Bars = BarsT<F8>;
+  constexpr int kNS = Ly::NS, kNV = Ly::NV, kThreads = Ly::THREADS;
+  constexpr int OFF_Q = Ly::OFF_Q, OFF_S = Ly::OFF_S, OFF_V = Ly::OFF_V, OFF_P = Ly::OFF_P;
+  constexpr int kSStage = Ly::SSTAGE, kPB = Ly::PB;
+  constexpr int OFF_F = Ly::OFF_F, OFF_BAR = Ly::OFF_BAR;
+  const CUtensorMap& tmQ = maps.q;
+  const CUtensorMap& tmK = maps.k;
+  const CUtensorMap& tmV = maps.v;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  float* fs = reinterpret_cast<float*>(sm + OFF_F);
+  int* flags = reinterpret_cast<int*>(fs + F_FLAG);
+  Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+
+  // ---- which (sequence, query row, split) this pair owns
+  const int unit = blockIdx.x >> 1;
+  const int split = unit % prm.S;
+  const int row = unit / prm.S;           // b * n_q + j
+  const int b = row / prm.n_q, j = row % prm.n_q;
+  // ---- set-up
+  if (tid == 0) TRACE(11, 0);
+  if (tid == 0) init_barriers<F8>(bars);
+  if (tid < kH) fs[F_M + tid] = -CUDART_INF_F;
+  if (tid < F_END - F_FLAG) flags[tid] = 0;
+  if (warp == 1) {
+    tmem_alloc_pair(&bars->tmem_base, 512);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  // Everything above touches only this pair's own shared memory and TMEM, so with a
+  // programmatic launch it overlaps the tail of the preceding kernel on the stream; every
+  // read of the inputs comes after that kernel has completed.
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // A unit normally takes one pass (mode 0). If a weight had to be clamped in it, both CTAs
+  // run it again: mode 1 computes only the scores, for the exact per-head maxima over the
+  // whole range, and mode 2 is the ordinary pass with those maxima as the reference (so every
+  // weight is at most 1 and none is clamped).
+  if constexpr (F8) {
+    for (int mode = 0; mode < 3; ++mode) {
+      decode_pass_ool<F8>(maps, prm, sm, mode);
+      if (!end_of_pass<F8>(mode, sm)) break;
+    }
+  } else {
+    decode_pass<F8>(maps, prm, sm, 0);
+    if (end_of_pass<F8>(0, sm)) replay_passes<F8>(maps, prm, sm);
   }
 
   // ---- teardown
   if (tid == 128) TRACE(10, 0);
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();
-  if (warp == 1) tmem_dealloc_pair(tmem, 512);
+  if (warp == 1) tmem_dealloc_pair(bars->tmem_base, 512);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1351,16 +1510,11 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
     if (!tc::make_map(&maps.k, pool, prow, 64)) return cudaErrorInvalidValue;
     if (!tc::make_map(&maps.v, pool, prow, 32)) return cudaErrorInvalidValue;
   }
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[f8]) {
-    cudaError_t e = f8 ? cudaFuncSetAttribute(tc::decode_kernel<true>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              tc::kSmemBytes<true>)
-                       : cudaFuncSetAttribute(tc::decode_kernel<false>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              tc::kSmemBytes<false>);
+  static std::atomic<bool> attr_bf16[kMaxDevices], attr_f8[kMaxDevices];
+  {
+    cudaError_t e = f8 ? set_smem_limit_once(tc::decode_kernel<true>, tc::kSmemBytes<true>, attr_f8)
+                       : set_smem_limit_once(tc::decode_kernel<false>, tc::kSmemBytes<false>, attr_bf16);
     if (e != cudaSuccess) return e;
-    attr_done[f8] = true;
   }
   const size_t rows = (size_t)B * n_q * d.H;
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;

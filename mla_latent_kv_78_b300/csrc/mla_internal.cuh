@@ -1,9 +1,27 @@
 // Launchers shared between the C-ABI front end and the kernel files.
 #pragma once
 
+#include <atomic>
+
 #include "mla_common.cuh"
 
 namespace mla {
+
+constexpr int kMaxDevices = 64;
+
+// A kernel's dynamic shared-memory limit belongs to the device it runs on, so the attribute
+// is set once per device: `done` is the call site's per-device record. Two host threads that
+// race here both set the same value, which is harmless.
+template <typename Kern>
+cudaError_t set_smem_limit_once(Kern kernel, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // Launch with programmatic stream serialization: the kernel may begin while the preceding
 // kernel on `stream` is still running, so it must read no input before griddepcontrol.wait.

@@ -333,6 +333,12 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
       : "memory");
 }
 
+// Plain 4-byte store into shared memory anywhere in the cluster (address from mapa); visible to
+// the other CTA after a cluster barrier.
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // 4-byte asynchronous store into another CTA's shared memory (complete_tx on its barrier).
 __device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
                                              uint32_t cluster_bar) {
@@ -445,6 +451,22 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
       : "=r"(r)
       : "r"(two_codes));
+  return r;
+}
+
+// Two E4M3 codes (low byte first) times an fp32 scale -> packed bf16x2: the codes convert to
+// f16 and then fp32 exactly, the product is taken in fp32 and rounded once to bf16.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, float scale) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  float lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi * scale), "f"(lo * scale));
   return r;
 }
 

@@ -235,27 +235,112 @@ def test_empty_batch_and_empty_token_lists_are_noops():
     assert z.numel() == 0
 
 
-@needs_cuda
-def test_score_beyond_the_weight_range_is_flagged():
-    """The tensor-core decode clamps weights at 2^96 (bf16 P) above its running reference and
-    reports MLA_DEV_SCORE_RANGE: one cached token whose score jumps far above tile 0's scores
-    (raw score 30 * 40 = 1200, i.e. ~125 in log2 units after the 1/sqrt(192) scale) trips it.
-    One split, so that the token falls in a later tile than the one that sets the reference;
-    the same workload at ordinary scale leaves the status clear."""
-    wl = SMALL_BF16_LONG
+def _spike_case(wl, X, Y, pos):
+    """Decode with q_lat = X e_0 for every row and head, after token `pos` of sequence 0 was
+    appended again (through the library) with latent column 0 set to Y. The scores are then
+    X c_n[0] / sqrt(192): N(0, (X/13.9)^2) nats for ordinary tokens and X Y / 13.9 for the
+    spike. One split, so the spike falls in a later tile than the one that sets the tensor-core
+    kernel's first reference."""
     case = Case(wl, num_splits=1)
-    case.run_step()
-    assert case.step.status() == 0
-    assert M.mla_decode_kernel(case.cfg, wl.B, wl.n_q) == M.MLA_KERNEL_TC
-    # token 600 of sequence 0 (tile 2): latent column 0 set to 40 in the bf16 pool entry
-    pos = 600
-    page = int(case.bt_np[0, pos // wl.P])
-    entry = case.step.pool[page, pos % wl.P].view(torch.bfloat16)
-    entry[0] = 40.0
-    q = case.step.q_lat.clone()
-    q[0, :, :] = 0
-    q[0, :, 0] = 30.0
-    case.step.dev_status.zero_()
-    case.step.decode(q)
+    case.step.append(case.new_c, case.new_r)
+    lat = ACT[wl.latent_storage]
+    c0, r0 = wl.latents(0)
+    c0 = c0.copy()
+    c0[pos, 0] = Y
+    case.step.prefill(dev(c0[pos:pos + 1], lat), dev(r0[pos:pos + 1], lat),
+                      torch.zeros(1, dtype=torch.int32, device="cuda"),
+                      torch.full((1,), pos, dtype=torch.int32, device="cuda"))
+    q_lat = np.zeros((wl.B, wl.n_q, wl.H, wl.C + wl.R), np.float32)
+    q_lat[..., 0] = X
+    case.step.decode(dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act]))
     torch.cuda.synchronize()
-    assert case.step.status() & M.MLA_DEV_SCORE_RANGE
+    assert case.step.status() == 0
+    tau = O.softmax_scale(wl.D, wl.R)
+    for b in range(wl.B):
+        c, r = wl.latents(b)
+        if b == 0:
+            c = c.copy()
+            c[pos, 0] = Y
+        ce = O.cache_entries(c, r, np.arange(wl.seq_lens[b]), wl.cache, wl.rope_base)
+        ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
+        if b == 0:
+            others = np.delete(X * ce["c"][:, 0] * tau, pos)
+            jump = X * ce["c"][pos, 0] * tau - others.max()
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_o, f"o_lat[b={b}]")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"lse[b={b}]")
+    return jump
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [SMALL_BF16_LONG, SMALL_FP8_LONG], ids=["bf16", "fp8"])
+def test_late_score_spike_matches_oracle(wl):
+    """One cached token in a late tile scores ~30 nats above every earlier token
+    (「deepseek(2)——deepseek 關鍵技術」 §1: the softmax is exact, whatever the spread). The
+    tensor-core kernel's lagging reference absorbs it without clamping."""
+    jump = _spike_case(wl, X=30.0, Y=17.0, pos=600)
+    assert jump > 28.0
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [SMALL_BF16_LONG, SMALL_FP8_LONG], ids=["bf16", "fp8"])
+def test_score_spike_beyond_the_weight_range_matches_oracle(wl):
+    """A token ~80 nats above the earlier tokens, far beyond the 2^96 weight range the lagging
+    reference leaves (66.5 nats): the kernel clamps in its first pass, notices, and runs the
+    unit again with the exact per-head maxima as the reference. The result must still be the
+    oracle's."""
+    jump = _spike_case(wl, X=30.0, Y=40.0, pos=600)
+    assert jump > 75.0
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [SMALL_BF16_LONG, SMALL_FP8_LONG, SMALL_BF16_LONG_MTP],
+                         ids=["bf16", "fp8", "bf16-mtp"])
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_decode_wide_score_spread(wl, kernel):
+    """Queries scaled by 10: the scaled scores of a row span more than 40 nats and the weights
+    are close to one-hot; every head must still match the oracle."""
+    case = Case(wl, kernel=kernel)
+    case.step.append(case.new_c, case.new_r)
+    q_lat = W.round_to_storage(wl.latent_queries() * np.float32(10.0), wl.act)
+    case.step.decode(dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act]))
+    torch.cuda.synchronize()
+    assert case.step.status() == 0
+    tau = O.softmax_scale(wl.D, wl.R)
+    spread = 0.0
+    for b in range(wl.B):
+        ce = case.cache_of(b)
+        ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
+        n = int(wl.positions(b)[-1]) + 1
+        s = (q_lat[b, -1] @ np.concatenate([ce["c"], ce["k_r"]], axis=1)[:n].T) * tau
+        spread = max(spread, float(np.max(s.max(axis=1) - s.min(axis=1))))
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_o, f"o_lat[b={b}]")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"lse[b={b}]")
+    assert spread > 40.0
+
+
+SMALL_FP8_GROUPS = W.small_v2(3, [300, 700, 64], n_q=2, cache="fp8", seed=19,
+                              group_scales=(1.0, 1e-3, 1e-5, 1.0))
+
+
+@needs_cuda
+@pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
+def test_fp8_groups_far_below_unit_scale(kernel):
+    """FP8 cache whose second and third 1x128 groups are drawn 1e-3 and 1e-5 times smaller
+    (group scales amax/448 of about 8e-6 and 8e-8). Each group of o_lat is checked against the
+    oracle at the usual tolerance scaled to that group's own magnitude, so a group whose scale
+    lost precision, or flushed to zero, fails even though its values are tiny next to the
+    others (「Deepseek系列从v3到R易背面经版」 F8量化策略: one scale per 1x128 group)."""
+    wl = SMALL_FP8_GROUPS
+    case = _decode_only(wl, kernel)
+    tau = O.softmax_scale(wl.D, wl.R)
+    q_lat = wl.latent_queries()
+    for b in range(wl.B):
+        ce = case.cache_of(b)
+        ref_o, _ = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
+        got = gpu_rows(case.step.o_lat, wl, b)
+        for k, m in enumerate(wl.group_scales):
+            cols = slice(128 * k, 128 * (k + 1))
+            ref_g = ref_o[..., cols]
+            err = float(np.max(np.abs(got[..., cols] - ref_g)))
+            tol = 1e-2 * float(np.max(np.abs(ref_g))) + 1e-3 * m
+            assert err <= tol, f"b={b} group {k} (x{m:g}): {err:.3e} > {tol:.3e}"

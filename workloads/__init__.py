@@ -82,6 +82,9 @@ class Workload:
     permute_pages: bool = False
     seed: int = 0
     rope_base: float = 10000.0
+    # optional per-128-column multipliers of the c_KV draws (groups of very different
+    # magnitude, e.g. to exercise FP8 group scales far below 1)
+    group_scales: Optional[Tuple[float, ...]] = None
 
     # ---- derived sizes -------------------------------------------------
     @property
@@ -140,6 +143,9 @@ class Workload:
         L = self.seq_lens[b]
         g = self._rng(_K_LATENT, b)
         x = g.standard_normal((L, self.C + self.R), dtype=np.float32) * np.float32(self.latent_std)
+        if self.group_scales is not None:
+            for k, m in enumerate(self.group_scales):
+                x[:, 128 * k:128 * (k + 1)] *= np.float32(m)
         x = round_to_storage(x, self.latent_storage)
         return np.ascontiguousarray(x[:, :self.C]), np.ascontiguousarray(x[:, self.C:])
 
@@ -208,10 +214,11 @@ def config(n: int) -> Workload:
 
 
 def small_v2(B: int, seq_lens: Sequence[int], n_q: int = 1, cache: str = "bf16",
-             permute_pages: bool = True, seed: int = 1234, H: int = 128) -> Workload:
+             permute_pages: bool = True, seed: int = 1234, H: int = 128,
+             group_scales: Optional[Tuple[float, ...]] = None) -> Workload:
     """A V2-shaped workload small enough for the oracle to finish in seconds."""
     assert len(seq_lens) == B
     return Workload(name=f"v2-small-b{B}", B=B, H=H, D=128, C=512, R=64, n_q=n_q, P=64,
                     seq_lens=tuple(int(x) for x in seq_lens), cache=cache, act="bf16",
                     latent_std=1.0, w_std=0.02, q_std=1.0, permute_pages=permute_pages,
-                    seed=seed)
+                    seed=seed, group_scales=group_scales)
