@@ -218,6 +218,18 @@ int mla_decode_noalloc(const mla_config* cfg, const void* q_lat, const void* kv_
                        int32_t num_splits, void* o_lat, float* lse, int32_t* dev_status,
                        void* stream);
 
+/*
+ * mla_debug_decode_fault — test hook for the device-side failure path (no counterpart on the
+ * pages). wait_cycles > 0 sets the limit, in SM clock cycles, after which every bounded wait of
+ * the tensor-core decode gives up (0 restores the default, about 2 s); withhold_chunk >= 0
+ * makes the bf16 kernel's latent producer in the even CTA of every pair register that latent
+ * chunk's bytes (chunks count 32-token, 256-column loads from the start of a pair's range)
+ * without issuing its loads, so the P.V issuer's wait for it runs out with nothing in flight:
+ * the decode then sets MLA_DEV_TIMEOUT, abandons its outputs and returns. -1 turns it off.
+ * Process-wide; affects launches made after the call. Returns MLA_OK or MLA_ERR_INVALID_ARG.
+ */
+int mla_debug_decode_fault(long long wait_cycles, int32_t withhold_chunk);
+
 /* Human-readable text of a return code (static storage). */
 const char* mla_status_string(int code);
 

@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     MLA_DEV_BAD_SEQLEN,
     MLA_DEV_INDEX_OUT_OF_RANGE,
     MLA_DEV_TIMEOUT,
+    MLA_ERR_INVALID_ARG,
     MLA_F32,
     MLA_FP8_E4M3,
     MLA_KERNEL_AUTO,

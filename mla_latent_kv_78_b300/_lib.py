@@ -81,6 +81,7 @@ _SIGS = {
     "mla_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _I, _I, _P, _I,
                                           _I, _I, _I, _P, _P, _P, _P]),
     "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mla_debug_decode_fault": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_int32]),
 }
 EXPORTED = tuple(_SIGS)
 

@@ -146,6 +146,8 @@ struct Maps {
 };
 
 struct Params {
+  long long wait_limit;   // clock cycles a bounded wait gives up after
+  int withhold;           // test hook: latent chunk the even CTA never loads (-1: none)
   const int32_t* bt;
   int maxp, num_pages;
   const int32_t* seq_lens;
@@ -164,6 +166,7 @@ struct Params {
 struct Ctx {
   volatile int* abort_flag;
   int32_t* status;
+  long long limit;   // clock cycles
 };
 
 #ifdef MLA_TC_TRACE
@@ -235,7 +238,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const C
   while (true) {
     if (*cx.abort_flag) return false;
     if (test()) return true;
-    if (clock64() - t0 > kTimeout) {
+    if (clock64() - t0 > cx.limit) {
       *cx.abort_flag = 1;
       flag_status(cx.status, MLA_DEV_TIMEOUT);
       return false;
@@ -328,7 +331,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
   const int split = unit % prm.S;
   const int row = unit / prm.S;           // b * n_q + j
   const int b = row / prm.n_q, j = row % prm.n_q;
-  Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status};
+  Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status, prm.wait_limit};
   const uint32_t tmem = bars->tmem_base;
   const int L = prm.seq_lens[b];
   const bool bad_len = (L < prm.n_q || L > prm.max_seq_len);
@@ -685,9 +688,12 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
               } else {
                 bar = mapa(smem_u32(&bars->v_ready[st]), 0);
               }
-              for (int q4 = 0; q4 < 4; ++q4)
-                tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
-                                 (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
+              // (test hook: the even CTA registers a withheld chunk's bytes but never loads
+              // them, so the P.V issuer's wait for it runs out; nothing is left in flight)
+              if (!(even && v_cnt == prm.withhold))
+                for (int q4 = 0; q4 < 4; ++q4)
+                  tma_load_2d_pair(sm + OFF_V + st * 16384 + q4 * 4096, &tmV,
+                                   (q4 >> 1) * 256 + (int)rank * 128 + (q4 & 1) * 64, y, bar, pol_v);
               TRACE(19, v_cnt);
             }
           }
@@ -764,7 +770,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         const long long t0 = clock64();
         while (*ticket != J) {
           if (*cx.abort_flag) return false;
-          if (clock64() - t0 > kTimeout) {
+          if (clock64() - t0 > cx.limit) {
             *cx.abort_flag = 1;
             flag_status(cx.status, MLA_DEV_TIMEOUT);
             return false;
@@ -1453,6 +1459,11 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Test hook state (mla_debug_decode_fault): the limit of every bounded wait and a latent
+// chunk the bf16 kernel withholds.
+static std::atomic<long long> g_wait_limit{0};
+static std::atomic<int> g_withhold{-1};
+
 static int pick_splits(int B, int n_q, int max_seq_len, int num_splits, int num_sms) {
   if (num_splits > 0) return num_splits;
   const int units = B * n_q;
@@ -1520,6 +1531,9 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
   if (ws_bytes < part) return cudaErrorInvalidValue;
   tc::Params prm;
+  const long long lim = tc::g_wait_limit.load();
+  prm.wait_limit = lim > 0 ? lim : tc::kTimeout;
+  prm.withhold = tc::g_withhold.load();
   prm.bt = bt;
   prm.maxp = maxp;
   prm.num_pages = num_pages;
@@ -1548,6 +1562,13 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
 }
 
 }  // namespace mla
+
+extern "C" int mla_debug_decode_fault(long long wait_cycles, int withhold_chunk) {
+  if (wait_cycles < 0 || withhold_chunk < -1) return MLA_ERR_INVALID_ARG;
+  mla::tc::g_wait_limit.store(wait_cycles);
+  mla::tc::g_withhold.store(withhold_chunk);
+  return MLA_OK;
+}
 
 #ifdef MLA_TC_TRACE
 extern "C" int mla_debug_set_tc_trace(void* p) {

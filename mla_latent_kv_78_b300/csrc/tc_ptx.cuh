@@ -438,22 +438,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with f16 A and B, fp32 D.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4)                       // D format: f32 (A, B format 0: f16)
-         | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-// Two E4M3 codes (low byte first) -> f16x2, exactly (every E4M3 value is an f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-      : "=r"(r)
-      : "r"(two_codes));
-  return r;
-}
-
 // Two E4M3 codes (low byte first) times an fp32 scale -> packed bf16x2: the codes convert to
 // f16 and then fp32 exactly, the product is taken in fp32 and rounded once to bf16.
 __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, float scale) {
@@ -467,25 +451,6 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, flo
       : "r"(h2));
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi * scale), "f"(lo * scale));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// Two fp32 -> packed f16x2 (round to nearest even); `lo` lands in the low half.
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ float f16_to_f32(uint32_t h16) {
-  float r;
-  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(r) : "r"(h16));
   return r;
 }
 

@@ -344,3 +344,38 @@ def test_fp8_groups_far_below_unit_scale(kernel):
             err = float(np.max(np.abs(got[..., cols] - ref_g)))
             tol = 1e-2 * float(np.max(np.abs(ref_g))) + 1e-3 * m
             assert err <= tol, f"b={b} group {k} (x{m:g}): {err:.3e} > {tol:.3e}"
+
+
+@needs_cuda
+def test_bounded_wait_runs_out_and_the_next_call_is_exact():
+    """The device-side failure path, made on purpose without a fault: through the test hook
+    the even CTA of every pair never issues the loads of one latent chunk whose bytes it has
+    registered, and every wait gives up after 2e5 cycles (about 0.1 ms) instead of about 2 s.
+    The decode must return with MLA_DEV_TIMEOUT set, and the next ordinary call on the same
+    stream must match the oracle (the context is still usable)."""
+    wl = SMALL_BF16_LONG
+    case = Case(wl, num_splits=1)
+    case.step.append(case.new_c, case.new_r)
+    assert M.mla_decode_kernel(case.cfg, wl.B, wl.n_q) == M.MLA_KERNEL_TC
+    q_lat = wl.latent_queries()
+    q_dev = dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act])
+    lib = M.lib()
+    try:
+        assert lib.mla_debug_decode_fault(200_000, 3) == 0
+        case.step.dev_status.zero_()
+        case.step.decode(q_dev)
+        torch.cuda.synchronize()
+        assert case.step.status() & M.MLA_DEV_TIMEOUT
+    finally:
+        assert lib.mla_debug_decode_fault(0, -1) == 0
+    assert lib.mla_debug_decode_fault(-1, -1) == M.MLA_ERR_INVALID_ARG
+    case.step.dev_status.zero_()
+    case.step.decode(q_dev)
+    torch.cuda.synchronize()
+    assert case.step.status() == 0
+    tau = O.softmax_scale(wl.D, wl.R)
+    for b in range(wl.B):
+        ce = case.cache_of(b)
+        ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_o, f"o_lat[b={b}]")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"lse[b={b}]")
