@@ -143,32 +143,25 @@ def _cpu_oracle_sample(wl, budget_s: float = 12.0, max_heads: int = 1 << 30):
     return done_bytes / t_total / 1e9, sample, threads, t_total
 
 
-PROFILE = os.path.join(ROOT, "profiles", "decode_tc_v2_b64_l4096.md")
+PROFILE = os.path.join(ROOT, "profiles", "decode_tc_v2_b64_l4096.json")
 DECODE_SOURCE = os.path.join(ROOT, "mla_latent_kv_78_b300", "csrc", "decode_tc.cu")
 
 
 def _ncu_traffic():
-    """DRAM bytes (read + write) per decode launch from the committed ncu summary, or None when
-    the summary is missing or was taken on a different decode_tc.cu (its recorded sha256)."""
+    """DRAM bytes (read + write) per decode launch from the committed ncu record (a JSON file
+    beside the summary), or None when it is missing or was taken on a different decode_tc.cu
+    (its recorded sha256)."""
     import hashlib
 
     try:
-        text = open(PROFILE).read()
+        rec = json.load(open(PROFILE))
         sha = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()
-    except OSError:
+    except (OSError, ValueError):
         return None
-    fields = {}
-    for line in text.splitlines():
-        line = line.strip().strip("`").lstrip("- ")
-        if ":" in line:
-            k, v = line.split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("decode_tc.cu sha256") != sha:
+    if rec.get("source_sha256") != sha:
         return None
-    try:
-        return int(fields["dram bytes per launch"])
-    except (KeyError, ValueError):
-        return None
+    v = rec.get("dram_bytes_per_launch")
+    return int(v) if isinstance(v, (int, float)) else None
 
 
 def reduce_max_over_ranks(xs, device):
@@ -187,6 +180,15 @@ def whole_job_gbs(world: int, bytes_per_step: float, steps: int, total_ms: float
     """Latent-cache GB/s of the whole job: every rank's replica moved bytes_per_step per step,
     and the job took the slowest rank's total_ms."""
     return world * bytes_per_step * steps / (total_ms * 1e-3) / 1e9
+
+
+def _workload_config(wl, extra=None):
+    """The `config` object of the JSON line: the workload by name and its sizes."""
+    c = {"workload": wl.name, "batch": wl.B, "seq_len": wl.seq_lens[0], "n_heads": wl.H,
+         "d_head": wl.D, "d_latent": wl.C, "d_rope": wl.R, "n_q": wl.n_q, "page_size": wl.P,
+         "cache": wl.cache, "l2": "flushed before every timed step"}
+    c.update(extra or {})
+    return c
 
 
 def _combine_launches(M, cfg, wl, splits) -> int:
@@ -215,23 +217,28 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     wl = W.config(WORKLOAD_ID)
-    rates = []
+    rates, secs = [], []
     sample = ""
     threads = 1
     for i in range(args.warmup + args.steps):
         v, sample, threads, t = _cpu_oracle_sample(wl, budget_s=args.ref_seconds_per_step)
         if i >= args.warmup:
             rates.append(v)
+            secs.append(t)
     value = statistics.median(rates)
     cache_bytes, _, flops = _workload_sizes(wl)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        # a whole step of the oracle would take this long at the sampled rate (an
+        # extrapolation); each timed step ran for sample_seconds_per_step
         "ms_per_step": cache_bytes / (value * 1e9) * 1e3,
+        "ms_per_step_is": "extrapolated from the sampled rate",
+        "sample_seconds_per_step": statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.B, "seq_len": wl.seq_lens[0], "n_heads": wl.H,
-                   "d_latent": wl.C, "d_rope": wl.R, "n_q": wl.n_q, "cache": wl.cache},
+        "config": _workload_config(wl, {"parallelism": "single", "decode_kernel": "fp64 oracle (CPU)",
+                                        "num_splits": 0}),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -417,12 +424,10 @@ def run_ours(args, world, rank, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.B, "seq_len": wl.seq_lens[0], "n_heads": wl.H,
-                   "d_head": wl.D, "d_latent": wl.C, "d_rope": wl.R, "n_q": wl.n_q,
-                   "page_size": wl.P, "cache": wl.cache, "l2": "flushed before every timed step",
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "decode_kernel": {1: "simt", 2: "tcgen05"}.get(kernel_used, str(kernel_used)),
-                   "num_splits": args.splits},
+        "config": _workload_config(wl, {
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "decode_kernel": {1: "simt", 2: "tcgen05"}.get(kernel_used, str(kernel_used)),
+            "num_splits": args.splits}),
         "us_per_step": ms_per_step * 1e3,
         "step_tflops": flops / (ms_per_step * 1e-3) / 1e12,
         "decode": {"us": dec_avg_ms * 1e3, "gbs": achieved,
