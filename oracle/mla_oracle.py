@@ -18,6 +18,9 @@ Sources are five web pages on DeepSeek-V2; they are cited by title:
 * [v3-notes]  「Deepseek系列从v3到R易背面经版」, www.coreui.cn — "MLA"
   (W^{UK} fused into the query side turns MHA into MQA) and "F8量化策略"
   (E4M3, per-token 1x128 activation groups).
+* [V2-explainer] §3.1.3 (长上下文扩展): YaRN on the decoupled RoPE for the 4K -> 128K
+  extension, scale s = 40, alpha = 1, beta = 32, target 160K, and a length factor
+  sqrt(t) = 0.0707 ln s + 1 that regulates the attention entropy.
 
 The reference function ``mla_decode_naive`` is the plain, non-absorbed
 definition: it decompresses k^C = W^{UK} c and v^C = W^{UV} c for every cached
@@ -44,6 +47,14 @@ design notes):
    round-to-nearest-even and saturation; the cached value is code * scale.
 5. W^{UK}, W^{UV} in R^{(n_h d_h) x d_c} are held as [H][D][C]: head i owns
    rows i*D .. i*D + D - 1.
+6. YaRN ([V2-explainer] §3.1.3 names the method and its parameters but not its
+   formula). Reading, the published "by parts" interpolation: for RoPE pair k with
+   frequency theta_k and wavelength lambda_k = 2 pi / theta_k, r_k = L / lambda_k with L
+   the original context (4096: the 4K the extension starts from; 4096 s = 160K is the
+   target the page names); gamma_k = clip((r_k - alpha) / (beta - alpha), 0, 1); the new
+   frequency is (1 - gamma_k) theta_k / s + gamma_k theta_k. q^R and k^R both rotate by
+   it (the relative-position property needs the same frequencies on both sides). The
+   factor sqrt(t) multiplies q and k alike, so every logit is scaled by t = sqrt(t)^2.
 
 Parity status: every function here is pinned by tests/test_oracle.py
 (closed forms, special cases, brute force in 50-digit decimal arithmetic,
@@ -64,14 +75,39 @@ FP8_GROUP = 128
 # --------------------------------------------------------------------------
 # Decoupled RoPE  ([V2-explainer] §2.2.2; [key-tech] §1 q^R, k^R equations)
 # --------------------------------------------------------------------------
-def rope_angles(pos: np.ndarray, R: int, base: float) -> np.ndarray:
-    """angle[..., k] = pos * base^(-2k/R), k = 0 .. R/2 - 1, in fp64."""
+def rope_theta(R: int, base: float) -> np.ndarray:
+    """theta_k = base^(-2k/R), k = 0 .. R/2 - 1, in fp64."""
     k = np.arange(R // 2, dtype=np.float64)
-    theta = np.power(np.float64(base), -2.0 * k / R)
-    return np.asarray(pos, dtype=np.float64)[..., None] * theta
+    return np.power(np.float64(base), -2.0 * k / R)
 
 
-def apply_rope(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
+def yarn_theta(R: int, base: float, s: float, alpha: float = 1.0, beta: float = 32.0,
+               orig_context: int = 4096) -> np.ndarray:
+    """YaRN frequencies of the decoupled RoPE ([V2-explainer] §3.1.3; reading 6).
+
+    Pairs whose wavelength fits in the original context fewer than alpha times are
+    interpolated fully (theta / s), pairs that fit more than beta times keep theta, and the
+    ones between move linearly in r = orig_context / wavelength.
+    """
+    theta = rope_theta(R, base)
+    r = orig_context / (2.0 * math.pi / theta)
+    gamma = np.clip((r - alpha) / (beta - alpha), 0.0, 1.0)
+    return (1.0 - gamma) * theta / s + gamma * theta
+
+
+def yarn_attention_factor(s: float, coef: float = 0.0707) -> float:
+    """t with sqrt(t) = coef ln s + 1 ([V2-explainer] §3.1.3): every logit is scaled by t."""
+    return (coef * math.log(s) + 1.0) ** 2
+
+
+def rope_angles(pos: np.ndarray, R: int, base: float, theta: Optional[np.ndarray] = None) -> np.ndarray:
+    """angle[..., k] = pos * theta_k (theta_k = base^(-2k/R) unless given), in fp64."""
+    if theta is None:
+        theta = rope_theta(R, base)
+    return np.asarray(pos, dtype=np.float64)[..., None] * np.asarray(theta, dtype=np.float64)
+
+
+def apply_rope(x: np.ndarray, pos: np.ndarray, base: float, theta: Optional[np.ndarray] = None) -> np.ndarray:
     """Rotate interleaved pairs of the last axis of x by the position's angles.
 
     x: [..., R]; pos broadcasts against x's leading axes.
@@ -80,7 +116,7 @@ def apply_rope(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
     """
     x = np.asarray(x, dtype=np.float64)
     R = x.shape[-1]
-    a = rope_angles(pos, R, base)
+    a = rope_angles(pos, R, base, theta)
     c, s = np.cos(a), np.sin(a)
     x0, x1 = x[..., 0::2], x[..., 1::2]
     y = np.empty(np.broadcast_shapes(x.shape, a.shape[:-1] + (R,)), dtype=np.float64)
@@ -192,13 +228,13 @@ def dequantize_fp8_groups(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
 # ([V2-explainer] §2.2.2: only c^{KV}_t and k^R_t are cached)
 # --------------------------------------------------------------------------
 def cache_entries(c_kv: np.ndarray, k_r: np.ndarray, pos: np.ndarray, cache: str,
-                  rope_base: float):
+                  rope_base: float, theta: Optional[np.ndarray] = None):
     """Values of the cached (c_KV, k^R) for tokens at positions pos.
 
     Returns a dict with fp64 'c' [n, C] and 'k_r' [n, R] (the values attention
     sees), and for an FP8 cache also 'codes' and 'scales'.
     """
-    k_rot = apply_rope(k_r, pos, rope_base)
+    k_rot = apply_rope(k_r, pos, rope_base, theta)
     if cache == "f32":
         return {"c": round_storage(c_kv, "f32"), "k_r": round_storage(k_rot, "f32")}
     if cache == "bf16":
@@ -226,7 +262,8 @@ def softmax_scale(D: int, R: int) -> float:
 
 def mla_decode_naive(c: np.ndarray, k_r_cached: np.ndarray, q_c: np.ndarray, q_r: np.ndarray,
                      w_uk: np.ndarray, w_uv: np.ndarray, positions: np.ndarray,
-                     rope_base: float, heads: Optional[np.ndarray] = None):
+                     rope_base: float, heads: Optional[np.ndarray] = None,
+                     theta: Optional[np.ndarray] = None, scale: Optional[float] = None):
     """One sequence's MLA decode, computed the long way.
 
     c          [L, C]    cached latents c^{KV}_n (values attention sees)
@@ -236,6 +273,8 @@ def mla_decode_naive(c: np.ndarray, k_r_cached: np.ndarray, q_c: np.ndarray, q_r
     w_uk, w_uv [H, D, C]
     positions  [n_q]     position of each query token (query j sees n <= positions[j])
     heads      optional subset of head indices to compute
+    theta      RoPE frequencies (default base^(-2k/R); YaRN's from yarn_theta)
+    scale      softmax scale (default 1/sqrt(D + R); with YaRN times yarn_attention_factor)
 
     For each head i: k^C_{n,i} = W^{UK}_i c_n, v^C_{n,i} = W^{UV}_i c_n,
     k_{n,i} = [k^C_{n,i}; k^R_n], q_{j,i} = [q^C_{j,i}; RoPE_{pos_j}(q^R_{j,i})],
@@ -252,7 +291,7 @@ def mla_decode_naive(c: np.ndarray, k_r_cached: np.ndarray, q_c: np.ndarray, q_r
     R = q_r.shape[-1]
     C = c.shape[1]
     heads = np.arange(H) if heads is None else np.asarray(heads)
-    tau = softmax_scale(D, R)
+    tau = softmax_scale(D, R) if scale is None else scale
     o = np.zeros((n_q, len(heads), D))
     o_lat = np.zeros((n_q, len(heads), C))
     lse = np.zeros((n_q, len(heads)))
@@ -262,7 +301,7 @@ def mla_decode_naive(c: np.ndarray, k_r_cached: np.ndarray, q_c: np.ndarray, q_r
         k = np.concatenate([k_c, k_r_cached], axis=1)           # [L, D + R]
         for j in range(n_q):
             p_j = int(positions[j])
-            q_rot = apply_rope(q_r[j, i], np.int64(p_j), rope_base)
+            q_rot = apply_rope(q_r[j, i], np.int64(p_j), rope_base, theta)
             q = np.concatenate([np.asarray(q_c[j, i], dtype=np.float64), q_rot])
             s = (k[:p_j + 1] @ q) * tau
             m = np.max(s)
@@ -280,14 +319,14 @@ def mla_decode_naive(c: np.ndarray, k_r_cached: np.ndarray, q_c: np.ndarray, q_r
 # into W^O"; [v3-notes] MLA: the query-side fusion turns MHA into MQA)
 # --------------------------------------------------------------------------
 def absorb_q(q_c: np.ndarray, q_r: np.ndarray, pos: np.ndarray, w_uk: np.ndarray,
-             rope_base: float) -> np.ndarray:
+             rope_base: float, theta: Optional[np.ndarray] = None) -> np.ndarray:
     """q_lat[t, i] = [q^C_{t,i}^T W^{UK}_i ; RoPE_{pos_t}(q^R_{t,i})]   (step a2).
 
     q_c [T, H, D], q_r [T, H, R], pos [T], w_uk [H, D, C] -> [T, H, C + R].
     """
     q_c = np.asarray(q_c, dtype=np.float64)
     lat = np.einsum("thd,hdc->thc", q_c, np.asarray(w_uk, dtype=np.float64))
-    rot = apply_rope(q_r, np.asarray(pos)[:, None], rope_base)
+    rot = apply_rope(q_r, np.asarray(pos)[:, None], rope_base, theta)
     return np.concatenate([lat, rot], axis=-1)
 
 

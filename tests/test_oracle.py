@@ -456,3 +456,77 @@ def test_cache_entries_fp8_group_hand_worked():
     want[:4] = np.array([144.0, -288.0, 72.0, 448.0]) * float(scale)
     np.testing.assert_array_equal(e["c"][0], want)
     np.testing.assert_array_equal(e["k_r"][0], [1.0, 2.0, -0.5, 0.25])
+
+
+# ---------------------------------------------------------------- YaRN (§3.1.3)
+YARN = dict(s=40.0, alpha=1.0, beta=32.0, orig_context=4096)   # 「一文通透DeepSeek-V2」 §3.1.3
+
+
+def test_yarn_reduces_to_plain_rope_at_scale_one():
+    """s = 1 extends nothing: every frequency is base^(-2k/R) and the logit factor is 1."""
+    np.testing.assert_allclose(O.yarn_theta(64, 10000.0, 1.0), O.rope_theta(64, 10000.0), rtol=1e-15, atol=0)
+    assert O.yarn_attention_factor(1.0) == 1.0
+
+
+def test_yarn_ramp_ends_hand_counted():
+    """V2's decoupled RoPE (R = 64, base 10000) with the page's s = 40, alpha = 1, beta = 32
+    over a 4096-token original context. Worked by hand: pair k keeps its frequency while
+    4096 theta_k / 2pi > 32, i.e. k < 32 ln(4096 / 64pi) / ln 10000 = 10.47, so k = 0..10;
+    it is divided by s while 4096 theta_k / 2pi < 1, i.e. k > 32 ln(4096 / 2pi) / ln 10000
+    = 22.51, so k = 23..31; the 12 pairs between move part of the way."""
+    th = O.rope_theta(64, 10000.0)
+    y = O.yarn_theta(64, 10000.0, **YARN)
+    np.testing.assert_array_equal(y[:11], th[:11])
+    np.testing.assert_allclose(y[23:], th[23:] / 40.0, rtol=1e-15, atol=0)
+    mid = y[11:23] / th[11:23]
+    assert np.all((mid < 1.0) & (mid > 1.0 / 40.0))
+    # the ratio falls monotonically from 1 to 1/s, and the frequencies stay ordered
+    ratio = y / th
+    assert np.all(np.diff(ratio) <= 1e-15) and np.all(np.diff(y) < 0)
+
+
+def test_yarn_hand_worked_middle_pair():
+    """Pair k = 16 of the same setting, by hand: theta = 10000^(-1/2) = 0.01, wavelength
+    2pi / 0.01 = 628.3185, r = 4096 / 628.3185 = 6.51897, gamma = (6.51897 - 1) / 31 =
+    0.178031, new theta = 0.01 ((1 - 0.178031) / 40 + 0.178031) = 0.00198580."""
+    y = O.yarn_theta(64, 10000.0, **YARN)
+    assert abs(y[16] - 0.00198580) < 2e-8
+
+
+def test_yarn_attention_factor_value():
+    """sqrt(t) = 0.0707 ln 40 + 1 = 0.0707 * 3.688879 + 1 = 1.260804, t = 1.589627."""
+    assert abs(O.yarn_attention_factor(40.0) - 1.589627) < 2e-6
+
+
+def test_yarn_keeps_the_relative_position_property():
+    """With the interpolated frequencies on both sides, RoPE_m(q) . RoPE_n(k) still depends
+    only on n - m (what lets the decoupled key be cached rotated), at positions up to 160K."""
+    g = _rng(42)
+    q, k = g.standard_normal(64), g.standard_normal(64)
+    th = O.yarn_theta(64, 10000.0, **YARN)
+    d = 1234
+    ref = O.apply_rope(q, np.int64(0), 10000.0, th) @ O.apply_rope(k, np.int64(d), 10000.0, th)
+    for m in [1, 4096, 100000, 160000 - d]:
+        v = O.apply_rope(q, np.int64(m), 10000.0, th) @ O.apply_rope(k, np.int64(m + d), 10000.0, th)
+        assert abs(v - ref) < 1e-8
+
+
+def test_yarn_absorbed_equals_naive():
+    """The absorbed path with YaRN frequencies and the scaled logits equals the naive form."""
+    g = _rng(43)
+    H, D, C, R, L = 3, 8, 16, 8, 40
+    c = g.standard_normal((L, C))
+    k_r = g.standard_normal((L, R))
+    w_uk, w_uv = g.standard_normal((2, H, D, C)) * 0.3
+    q_c, q_r = g.standard_normal((1, H, D)), g.standard_normal((1, H, R))
+    th = O.yarn_theta(R, 10000.0, 40.0, 1.0, 32.0, 16)
+    tau = O.softmax_scale(D, R) * O.yarn_attention_factor(40.0)
+    pos = np.array([L - 1])
+    ce = O.cache_entries(c, k_r, np.arange(L), "f32", 10000.0, th)
+    o, o_lat, lse = O.mla_decode_naive(ce["c"], ce["k_r"], q_c, q_r, w_uk, w_uv, pos, 10000.0,
+                                        theta=th, scale=tau)
+    q_lat = O.absorb_q(q_c, q_r, pos, w_uk, 10000.0, th)
+    o_lat2, lse2 = O.latent_attention(q_lat, ce["c"], ce["k_r"], pos, tau)
+    np.testing.assert_allclose(o_lat2[0], o_lat[0], atol=1e-12)
+    np.testing.assert_allclose(O.unabsorb(o_lat2, w_uv)[0], o[0], atol=1e-12)
+    np.testing.assert_allclose(lse2[0], lse[0], atol=1e-12)
