@@ -92,6 +92,18 @@ typedef struct mla_config {
   int32_t kernel;       /* MLA_KERNEL_*                                           */
   float softmax_scale;  /* 0 -> 1/sqrt(d_head + d_rope)                            */
   float rope_base;      /* 0 -> 10000                                             */
+  /* YaRN on the decoupled RoPE (「一文通透DeepSeek-V2」 §3.1.3, the 4K -> 128K extension).
+   * rope_scaling = s <= 1 leaves plain RoPE. With s > 1, RoPE pair k (frequency
+   * theta_k = base^(-2k/R), wavelength 2pi/theta_k) gets the frequency
+   * (1 - g) theta_k / s + g theta_k, g = clip((r - alpha) / (beta - alpha), 0, 1),
+   * r = rope_orig_context / wavelength, for q^R (mla_absorb_q) and k^R (mla_append_cache)
+   * alike; and every logit of mla_decode is scaled by t = (mscale_coef ln s + 1)^2 on top of
+   * softmax_scale. Zero fields take the page's values. */
+  float rope_scaling;         /* s (0 or <= 1: off; the page uses 40)                  */
+  int32_t rope_orig_context;  /* original context length (0 -> 4096)                   */
+  float rope_yarn_alpha;      /* 0 -> 1                                                */
+  float rope_yarn_beta;       /* 0 -> 32                                               */
+  float rope_mscale_coef;     /* sqrt(t) = coef ln s + 1 (0 -> 0.0707)                 */
 } mla_config;
 
 /*

@@ -55,13 +55,23 @@ class mla_config(ctypes.Structure):
         ("kernel", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("rope_base", ctypes.c_float),
+        ("rope_scaling", ctypes.c_float),
+        ("rope_orig_context", ctypes.c_int32),
+        ("rope_yarn_alpha", ctypes.c_float),
+        ("rope_yarn_beta", ctypes.c_float),
+        ("rope_mscale_coef", ctypes.c_float),
     ]
 
 
 def make_config(H: int, D: int, C: int, R: int, P: int, cache: str = "bf16", act: str = "bf16",
                 kernel: int = MLA_KERNEL_AUTO, softmax_scale: float = 0.0,
-                rope_base: float = 10000.0) -> mla_config:
-    return mla_config(H, D, C, R, P, _DTYPES[cache], _DTYPES[act], kernel, softmax_scale, rope_base)
+                rope_base: float = 10000.0, rope_scaling: float = 0.0,
+                rope_orig_context: int = 0, rope_yarn_alpha: float = 0.0,
+                rope_yarn_beta: float = 0.0, rope_mscale_coef: float = 0.0) -> mla_config:
+    """A filled mla_config; the rope_* YaRN fields stay 0 (plain RoPE) unless given."""
+    return mla_config(H, D, C, R, P, _DTYPES[cache], _DTYPES[act], kernel, softmax_scale, rope_base,
+                      rope_scaling, rope_orig_context, rope_yarn_alpha, rope_yarn_beta,
+                      rope_mscale_coef)
 
 
 _lib: Optional[ctypes.CDLL] = None

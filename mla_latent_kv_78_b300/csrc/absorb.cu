@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(128) absorb_kernel(Dims d, const Act* __restri
                                                      const Act* __restrict__ q_r,
                                                      const int32_t* __restrict__ pos, int T,
                                                      const Act* __restrict__ w_uk,
-                                                     Act* __restrict__ q_lat) {
+                                                     Act* __restrict__ q_lat, const RopeTable rt) {
   extern __shared__ float sm[];
   const int t0 = blockIdx.y * kTok;
   const int nt = min(kTok, T - t0);
@@ -57,7 +57,10 @@ __global__ void __launch_bounds__(128) absorb_kernel(Dims d, const Act* __restri
     for (int idx = threadIdx.x; idx < nt * R2; idx += blockDim.x) {
       const int t = idx / R2, k = idx % R2;
       double c, s;
-      rope_cos_sin(pos[t0 + t], k, d.R, (double)d.rope_base, &c, &s);
+      if (k < kMaxRopePairs)
+        sincos((double)pos[t0 + t] * rt.th[k], &s, &c);
+      else
+        rope_cos_sin(pos[t0 + t], k, d.R, (double)d.rope_base, &c, &s);
       cs[idx] = (float)c;
       sn[idx] = (float)s;
     }
@@ -117,13 +120,15 @@ cudaError_t launch_absorb(const Dims& d, const void* q_c, const void* q_r, const
   const int rope_blocks = (d.H + 31) / 32;
   dim3 grid(d.H + rope_blocks, (T + kTok - 1) / kTok);
   const size_t smem = sizeof(float) * (size_t)kTok * (d.D > d.R ? d.D : d.R);
+  RopeTable rt;
+  fill_rope_table(&rt, d);
   if (d.act_dtype == MLA_F32)
     absorb_kernel<float><<<grid, 128, smem, stream>>>(d, (const float*)q_c, (const float*)q_r, pos,
-                                                      T, (const float*)w_uk, (float*)q_lat);
+                                                      T, (const float*)w_uk, (float*)q_lat, rt);
   else
     absorb_kernel<__nv_bfloat16><<<grid, 128, smem, stream>>>(
         d, (const __nv_bfloat16*)q_c, (const __nv_bfloat16*)q_r, pos, T,
-        (const __nv_bfloat16*)w_uk, (__nv_bfloat16*)q_lat);
+        (const __nv_bfloat16*)w_uk, (__nv_bfloat16*)q_lat, rt);
   return cudaGetLastError();
 }
 

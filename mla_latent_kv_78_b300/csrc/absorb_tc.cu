@@ -265,7 +265,7 @@ cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, co
   p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
   p.status = nullptr;
   for (int k = 0; k < tca::kR / 2; ++k) {
-    const double th = pow((double)d.rope_base, -2.0 * (double)k / (double)tca::kR);
+    const double th = rope_theta_host(d, k);
     p.theta_hi[k] = (float)th;
     p.theta_lo[k] = (float)(th - (double)p.theta_hi[k]);
   }

@@ -126,7 +126,7 @@ cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, cons
   const int blocks = (T * 32 + threads - 1) / threads;
   uint8_t* out = static_cast<uint8_t*>(pool);
   RopeTable rt;
-  fill_rope_table(&rt, d.R, (double)d.rope_base);
+  fill_rope_table(&rt, d);
   switch (d.cache_dtype) {
     case MLA_F32:
       append_kernel<float, MLA_F32><<<blocks, threads, 0, stream>>>(

@@ -47,6 +47,18 @@ int make_dims(const mla_config* c, Dims* d) {
   d->scale = c->softmax_scale > 0.f ? c->softmax_scale : 1.0f / sqrtf((float)(c->d_head + c->d_rope));
   d->rope_base = c->rope_base > 0.f ? c->rope_base : 10000.0f;
   d->entry_bytes = (int)entry_bytes(c);
+  // YaRN (「一文通透DeepSeek-V2」 §3.1.3): defaults are the page's values
+  d->yarn_s = c->rope_scaling > 1.f ? c->rope_scaling : 1.f;
+  d->yarn_orig = c->rope_orig_context > 0 ? c->rope_orig_context : 4096;
+  d->yarn_alpha = c->rope_yarn_alpha > 0.f ? c->rope_yarn_alpha : 1.f;
+  d->yarn_beta = c->rope_yarn_beta > 0.f ? c->rope_yarn_beta : 32.f;
+  if (d->yarn_s > 1.f) {
+    if (!(d->yarn_beta > d->yarn_alpha) || c->rope_orig_context < 0) return MLA_ERR_INVALID_ARG;
+    if (d->R / 2 > mla::kMaxRopePairs) return MLA_ERR_UNSUPPORTED;
+    const float coef = c->rope_mscale_coef > 0.f ? c->rope_mscale_coef : 0.0707f;
+    const float sqrt_t = coef * logf(d->yarn_s) + 1.f;
+    d->scale *= sqrt_t * sqrt_t;
+  }
   if (c->cache_dtype == MLA_FP8_E4M3 && (d->entry_bytes % 16)) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }

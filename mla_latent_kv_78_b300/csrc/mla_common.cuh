@@ -16,10 +16,25 @@ constexpr float kE4M3Max = 448.0f;
 struct Dims {
   int H, D, C, R, P;
   int cache_dtype, act_dtype;
-  float scale;       // softmax scale
+  float scale;       // softmax scale (YaRN's logit factor included)
   float rope_base;
   int entry_bytes;   // bytes of one pool entry
+  // YaRN on the decoupled RoPE (yarn_s <= 1: plain RoPE)
+  float yarn_s, yarn_alpha, yarn_beta;
+  int yarn_orig;
 };
+
+// RoPE frequency of pair k, computed on the host in fp64: base^(-2k/R), or with YaRN
+// (「一文通透DeepSeek-V2」 §3.1.3) the by-parts interpolation between theta/s and theta over
+// r = original context / wavelength.
+inline double rope_theta_host(const Dims& d, int k) {
+  const double th = pow((double)d.rope_base, -2.0 * (double)k / (double)d.R);
+  if (!(d.yarn_s > 1.f)) return th;
+  const double r = (double)d.yarn_orig * th / (2.0 * 3.14159265358979323846);
+  double g = (r - (double)d.yarn_alpha) / ((double)d.yarn_beta - (double)d.yarn_alpha);
+  g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
+  return (1.0 - g) * th / (double)d.yarn_s + g * th;
+}
 
 __device__ __forceinline__ void flag_status(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);
@@ -50,9 +65,9 @@ struct RopeTable {
   double th[kMaxRopePairs];
 };
 
-inline void fill_rope_table(RopeTable* t, int R, double base) {
-  for (int k = 0; k < R / 2 && k < kMaxRopePairs; ++k) {
-    const double th = pow(base, -2.0 * (double)k / (double)R);
+inline void fill_rope_table(RopeTable* t, const Dims& d) {
+  for (int k = 0; k < d.R / 2 && k < kMaxRopePairs; ++k) {
+    const double th = rope_theta_host(d, k);
     t->th[k] = th;
     t->hi[k] = (float)th;
     t->lo[k] = (float)(th - (double)t->hi[k]);

@@ -18,7 +18,21 @@ def dev(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
 
 
 def config_of(wl: Workload, kernel: int = M.MLA_KERNEL_AUTO) -> M.mla_config:
-    return M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act, kernel=kernel)
+    return M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act, kernel=kernel,
+                         rope_scaling=wl.rope_scaling if wl.rope_scaling > 1 else 0.0)
+
+
+def theta_of(wl: Workload):
+    """The oracle's RoPE frequencies for a workload (None: plain RoPE)."""
+    if wl.rope_scaling > 1:
+        return O.yarn_theta(wl.R, wl.rope_base, wl.rope_scaling)
+    return None
+
+
+def tau_of(wl: Workload) -> float:
+    """The oracle's softmax scale for a workload (YaRN's logit factor included)."""
+    tau = O.softmax_scale(wl.D, wl.R)
+    return tau * O.yarn_attention_factor(wl.rope_scaling) if wl.rope_scaling > 1 else tau
 
 
 def tolerance(wl: Workload, ref: np.ndarray):
@@ -102,14 +116,15 @@ class Case:
     def cache_of(self, b: int):
         wl = self.wl
         c, r = wl.latents(b)
-        return O.cache_entries(c, r, np.arange(wl.seq_lens[b]), wl.cache, wl.rope_base)
+        return O.cache_entries(c, r, np.arange(wl.seq_lens[b]), wl.cache, wl.rope_base, theta_of(wl))
 
     def oracle(self, b: int, heads=None):
         """(o, o_lat, lse) of sequence b from the naive definition."""
         wl = self.wl
         ce = self.cache_of(b)
         return O.mla_decode_naive(ce["c"], ce["k_r"], self.q_c_np[b], self.q_r_np[b], self.w_uk_np,
-                                  self.w_uv_np, wl.positions(b), wl.rope_base, heads=heads)
+                                  self.w_uv_np, wl.positions(b), wl.rope_base, heads=heads,
+                                  theta=theta_of(wl), scale=tau_of(wl))
 
 
 def gpu_rows(t: torch.Tensor, wl: Workload, b: int) -> np.ndarray:

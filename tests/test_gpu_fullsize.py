@@ -17,7 +17,7 @@ import torch
 import workloads as W
 from oracle import mla_oracle as O
 
-from _support import Case, assert_close, gpu_rows
+from _support import Case, assert_close, gpu_rows, tau_of, theta_of
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -46,12 +46,12 @@ def test_full_size_decode_step(n):
     assert case.step.status() == 0
     assert bool(torch.isfinite(case.step.o).all())
     assert bool(torch.isfinite(case.step.lse).all())
-    tau = O.softmax_scale(wl.D, wl.R)
+    tau = tau_of(wl)
     seqs = _sampled_sequences(wl)
     for k, b in enumerate(seqs):
         pos = wl.positions(b)
         ce = case.cache_of(b)
-        q_lat = O.round_bf16(O.absorb_q(case.q_c_np[b], case.q_r_np[b], pos, case.w_uk_np, wl.rope_base))
+        q_lat = O.round_bf16(O.absorb_q(case.q_c_np[b], case.q_r_np[b], pos, case.w_uk_np, wl.rope_base, theta_of(wl)))
         ref_lat, ref_lse = O.latent_attention(q_lat, ce["c"], ce["k_r"], pos, tau)
         assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_lat, f"cfg{n} o_lat[b={b}] (all heads)")
         assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"cfg{n} lse[b={b}] (all heads)")

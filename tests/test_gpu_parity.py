@@ -13,7 +13,7 @@ import mla_latent_kv_78_b300 as M
 import workloads as W
 from oracle import mla_oracle as O
 
-from _support import ACT, Case, assert_close, config_of, dev, gpu_rows
+from _support import ACT, Case, assert_close, config_of, dev, gpu_rows, tau_of, theta_of
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +31,21 @@ SMALL_FP8_LONG_MTP = W.small_v2(3, [513, 256, 900], n_q=2, cache="fp8", seed=18)
 SMALL_BF16_T200 = W.small_v2(100, [3] * 100, n_q=2, cache="bf16", seed=16)
 TINY = W.config(1)
 TINY_PERM = W.config(1).with_(permute_pages=True)
+# YaRN on the decoupled RoPE (「一文通透DeepSeek-V2」 §3.1.3: s = 40), short and long sequences;
+# the long one puts the query near position 150K of the 160K the extension targets
+SMALL_YARN = W.small_v2(3, [700, 257, 1000], n_q=1, cache="bf16", seed=31, rope_scaling=40.0)
+SMALL_YARN_FP8 = W.small_v2(2, [300, 129], n_q=2, cache="fp8", seed=32, rope_scaling=40.0)
+LONG_YARN = W.small_v2(2, [150000, 3000], n_q=1, cache="bf16", seed=33, rope_scaling=40.0)
+TINY_YARN = W.config(1).with_(rope_scaling=40.0)
+
+
+def _rope_tol(ref: np.ndarray, k_r: np.ndarray) -> np.ndarray:
+    """Bound on a bf16-stored rotated k^R value: one bf16 ulp of the oracle's value, plus
+    the fp32 arithmetic error of the rotation, which scales with the pair's magnitude
+    |x_2k| + |x_2k+1| rather than with the result (a rotation that nearly cancels)."""
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    pair = np.abs(k_r[:, 0::2]) + np.abs(k_r[:, 1::2])
+    return ulp + 2.0 ** -20 * np.repeat(pair, 2, axis=1)
 
 
 def _bits_equal(a: np.ndarray, b: np.ndarray) -> bool:
@@ -38,7 +53,8 @@ def _bits_equal(a: np.ndarray, b: np.ndarray) -> bool:
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8], ids=lambda w: w.name + ("-perm" if w.permute_pages else ""))
+@pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_YARN, TINY_YARN],
+                         ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + ("-yarn" if w.rope_scaling > 1 else ""))
 def test_append_writes_each_token_to_its_slot(wl):
     """Every cached token lands in pool[block_table[b][pos // P]][pos % P] and nowhere else
     (bit-exact); c_KV is copied (or E4M3-coded, bit-exact), k^R is RoPE'd (<= 1 ulp)."""
@@ -51,7 +67,7 @@ def test_append_writes_each_token_to_its_slot(wl):
     for b in range(wl.B):
         L = wl.seq_lens[b]
         c, r = wl.latents(b)
-        ce = O.cache_entries(c, r, np.arange(L), wl.cache, wl.rope_base)
+        ce = O.cache_entries(c, r, np.arange(L), wl.cache, wl.rope_base, theta_of(wl))
         pg, sl = O.page_slots(np.full(L, b), np.arange(L), case.bt_np, wl.P)
         ent = pool[pg, sl]                       # [L, entry]
         touched[pg, sl] = True
@@ -64,23 +80,22 @@ def test_append_writes_each_token_to_its_slot(wl):
             got_c = ent[:, :2 * wl.C].copy().view(np.uint16)
             assert np.array_equal(got_c, W.to_bf16_bits(c))
             got_r = W.bf16_bits_to_f32(ent[:, 2 * wl.C:].copy().view(np.uint16)).astype(np.float64)
-            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ce["k_r"]), 1e-30))) - 7)
-            assert np.all(np.abs(got_r - ce["k_r"]) <= ulp)
+            assert np.all(np.abs(got_r - ce["k_r"]) <= _rope_tol(ce["k_r"], r))
         else:
             codes = ent[:, :wl.C]
             got_r = W.bf16_bits_to_f32(ent[:, wl.C:wl.C + 2 * wl.R].copy().view(np.uint16)).astype(np.float64)
             scales = ent[:, wl.C + 2 * wl.R:].copy().view(np.float32)
             assert np.array_equal(codes, ce["codes"]), "E4M3 codes differ"
             assert _bits_equal(scales, ce["scales"].astype(np.float32)), "group scales differ"
-            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ce["k_r"]), 1e-30))) - 7)
-            assert np.all(np.abs(got_r - ce["k_r"]) <= ulp)
+            assert np.all(np.abs(got_r - ce["k_r"]) <= _rope_tol(ce["k_r"], r))
     # slots no token maps to stay untouched (the pool starts zeroed)
     assert not pool[~touched].any()
 
 
 @needs_cuda
-@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_FP8, SMALL_BF16_LONG_MTP, SMALL_BF16_T200],
-                         ids=lambda w: w.name + f"-T{w.B * w.n_q}")
+@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_FP8, SMALL_BF16_LONG_MTP, SMALL_BF16_T200, SMALL_YARN,
+                                TINY_YARN],
+                         ids=lambda w: w.name + f"-T{w.B * w.n_q}" + ("-yarn" if w.rope_scaling > 1 else ""))
 @pytest.mark.parametrize("kernel", [M.MLA_KERNEL_SIMT, M.MLA_KERNEL_AUTO], ids=["simt", "auto"])
 def test_absorb_q(wl, kernel):
     case = Case(wl, kernel=kernel, prefill=False)
@@ -88,7 +103,7 @@ def test_absorb_q(wl, kernel):
     torch.cuda.synchronize()
     pos = np.concatenate([wl.positions(b) for b in range(wl.B)])
     ref = O.absorb_q(case.q_c_np.reshape(-1, wl.H, wl.D), case.q_r_np.reshape(-1, wl.H, wl.R), pos,
-                     case.w_uk_np, wl.rope_base)
+                     case.w_uk_np, wl.rope_base, theta_of(wl))
     got = case.step.q_lat.float().cpu().numpy()
     assert_close(wl, got[..., :wl.C], ref[..., :wl.C], "q_lat latent part")
     assert_close(wl, got[..., wl.C:], ref[..., wl.C:], "q_lat RoPE part")
@@ -115,7 +130,7 @@ def _decode_only(wl, kernel, num_splits=0):
     case.step.decode(dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act]))
     torch.cuda.synchronize()
     assert case.step.status() == 0
-    tau = O.softmax_scale(wl.D, wl.R)
+    tau = tau_of(wl)
     for b in range(wl.B):
         ce = case.cache_of(b)
         ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
@@ -160,8 +175,9 @@ def test_tensor_core_kernel_is_selected_for_v2_shapes():
 
 @needs_cuda
 @pytest.mark.parametrize("wl", [TINY, TINY_PERM, SMALL_BF16, SMALL_FP8, SMALL_BF16_MTP, SMALL_BF16_LONG,
-                                SMALL_FP8_LONG_MTP],
-                         ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + f"-L{max(w.seq_lens)}")
+                                SMALL_FP8_LONG_MTP, SMALL_YARN, SMALL_YARN_FP8, TINY_YARN],
+                         ids=lambda w: w.name + ("-perm" if w.permute_pages else "") + f"-L{max(w.seq_lens)}"
+                         + ("-yarn" if w.rope_scaling > 1 else ""))
 def test_decode_step_end_to_end(wl):
     """append -> absorb -> decode -> unabsorb against the non-absorbed oracle."""
     case = Case(wl)
@@ -255,13 +271,13 @@ def _spike_case(wl, X, Y, pos):
     case.step.decode(dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act]))
     torch.cuda.synchronize()
     assert case.step.status() == 0
-    tau = O.softmax_scale(wl.D, wl.R)
+    tau = tau_of(wl)
     for b in range(wl.B):
         c, r = wl.latents(b)
         if b == 0:
             c = c.copy()
             c[pos, 0] = Y
-        ce = O.cache_entries(c, r, np.arange(wl.seq_lens[b]), wl.cache, wl.rope_base)
+        ce = O.cache_entries(c, r, np.arange(wl.seq_lens[b]), wl.cache, wl.rope_base, theta_of(wl))
         ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
         if b == 0:
             others = np.delete(X * ce["c"][:, 0] * tau, pos)
@@ -305,7 +321,7 @@ def test_decode_wide_score_spread(wl, kernel):
     case.step.decode(dev(q_lat.reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act]))
     torch.cuda.synchronize()
     assert case.step.status() == 0
-    tau = O.softmax_scale(wl.D, wl.R)
+    tau = tau_of(wl)
     spread = 0.0
     for b in range(wl.B):
         ce = case.cache_of(b)
@@ -332,7 +348,7 @@ def test_fp8_groups_far_below_unit_scale(kernel):
     others (「Deepseek系列从v3到R易背面经版」 F8量化策略: one scale per 1x128 group)."""
     wl = SMALL_FP8_GROUPS
     case = _decode_only(wl, kernel)
-    tau = O.softmax_scale(wl.D, wl.R)
+    tau = tau_of(wl)
     q_lat = wl.latent_queries()
     for b in range(wl.B):
         ce = case.cache_of(b)
@@ -373,9 +389,31 @@ def test_bounded_wait_runs_out_and_the_next_call_is_exact():
     case.step.decode(q_dev)
     torch.cuda.synchronize()
     assert case.step.status() == 0
-    tau = O.softmax_scale(wl.D, wl.R)
+    tau = tau_of(wl)
     for b in range(wl.B):
         ce = case.cache_of(b)
         ref_o, ref_lse = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
         assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_o, f"o_lat[b={b}]")
         assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"lse[b={b}]")
+
+
+@needs_cuda
+def test_yarn_long_context_step():
+    """YaRN at long context (「一文通透DeepSeek-V2」 §3.1.3: 4K -> 128K, target 160K): a query
+    near position 150K. Every head's o_lat and lse against the oracle's latent attention, and
+    o of a few heads against the non-absorbed definition."""
+    wl = LONG_YARN
+    case = Case(wl)
+    case.run_step()
+    assert case.step.status() == 0
+    heads = np.array([0, 63, 127])
+    for b in range(wl.B):
+        pos = wl.positions(b)
+        ce = case.cache_of(b)
+        q_lat = O.round_bf16(O.absorb_q(case.q_c_np[b], case.q_r_np[b], pos, case.w_uk_np, wl.rope_base,
+                                        theta_of(wl)))
+        ref_lat, ref_lse = O.latent_attention(q_lat, ce["c"], ce["k_r"], pos, tau_of(wl))
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_lat, f"o_lat[b={b}]")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"lse[b={b}]")
+        o, _, _ = case.oracle(b, heads=heads)
+        assert_close(wl, gpu_rows(case.step.o, wl, b)[:, heads], o, f"o[b={b}]")

@@ -85,6 +85,9 @@ class Workload:
     # optional per-128-column multipliers of the c_KV draws (groups of very different
     # magnitude, e.g. to exercise FP8 group scales far below 1)
     group_scales: Optional[Tuple[float, ...]] = None
+    # YaRN factor s of the decoupled RoPE (1: plain RoPE); the method itself lives in the
+    # library and the oracle, this only names the setting
+    rope_scaling: float = 1.0
 
     # ---- derived sizes -------------------------------------------------
     @property
@@ -215,10 +218,10 @@ def config(n: int) -> Workload:
 
 def small_v2(B: int, seq_lens: Sequence[int], n_q: int = 1, cache: str = "bf16",
              permute_pages: bool = True, seed: int = 1234, H: int = 128,
-             group_scales: Optional[Tuple[float, ...]] = None) -> Workload:
+             group_scales: Optional[Tuple[float, ...]] = None, rope_scaling: float = 1.0) -> Workload:
     """A V2-shaped workload small enough for the oracle to finish in seconds."""
     assert len(seq_lens) == B
     return Workload(name=f"v2-small-b{B}", B=B, H=H, D=128, C=512, R=64, n_q=n_q, P=64,
                     seq_lens=tuple(int(x) for x in seq_lens), cache=cache, act="bf16",
                     latent_std=1.0, w_std=0.02, q_std=1.0, permute_pages=permute_pages,
-                    seed=seed, group_scales=group_scales)
+                    seed=seed, group_scales=group_scales, rope_scaling=rope_scaling)
