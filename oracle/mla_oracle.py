@@ -55,6 +55,13 @@ design notes):
    frequency is (1 - gamma_k) theta_k / s + gamma_k theta_k. q^R and k^R both rotate by
    it (the relative-position property needs the same frequencies on both sides). The
    factor sqrt(t) multiplies q and k alike, so every logit is scaled by t = sqrt(t)^2.
+7. The latent's RMSNorm ([V2-explainer] §3.1.4: an extra RMSNorm after the compressed
+   latent, and extra scaling factors at the width bottlenecks). Reading: c^{KV} =
+   g * x / sqrt(mean(x^2) + eps) with x = W^{DKV} h, a learned gain g per latent
+   dimension that also carries the bottleneck's scaling factor, eps = 1e-6 (not on the
+   pages); k^R = W^{KR} h is not normalised. The projected c^{KV} and k^R are stored in
+   the activation type before they are cached, as when the projection and the cache
+   write are separate calls.
 
 Parity status: every function here is pinned by tests/test_oracle.py
 (closed forms, special cases, brute force in 50-digit decimal arithmetic,
@@ -375,6 +382,35 @@ def combine_partials(o_parts: np.ndarray, lse_parts: np.ndarray):
     z = np.sum(w, axis=0)
     o = np.sum(w[..., None] * np.asarray(o_parts, dtype=np.float64), axis=0) / z[..., None]
     return o, m + np.log(z)
+
+
+# --------------------------------------------------------------------------
+# Upstream of the cache and downstream of the attention
+# ([V2-explainer] §2.2.1 c^{KV} = W^{DKV} h, §2.2.2 k^R = RoPE(W^{KR} h), §3.1.4 the
+# latent's RMSNorm; §2.1.2 and [key-tech] §1 u_t = W^O [o_{t,1}; ...; o_{t,n_h}])
+# --------------------------------------------------------------------------
+def rms_norm(x: np.ndarray, gain: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    """gain * x / sqrt(mean(x^2 over the last axis) + eps) (reading 7)."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.asarray(gain, dtype=np.float64) * x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def project_latent(h: np.ndarray, w_dkv: np.ndarray, w_kr: np.ndarray, gain: np.ndarray,
+                   eps: float = 1e-6):
+    """The cached quantities of tokens with hidden states h [T, d], before RoPE:
+    c^{KV} = RMSNorm(W^{DKV} h) [T, C] and k^R = W^{KR} h [T, R] (W^{DKV} [C, d], W^{KR}
+    [R, d], gain [C]). cache_entries() then rotates k^R and stores both."""
+    h = np.asarray(h, dtype=np.float64)
+    c = rms_norm(h @ np.asarray(w_dkv, dtype=np.float64).T, gain, eps)
+    k = h @ np.asarray(w_kr, dtype=np.float64).T
+    return c, k
+
+
+def output_projection(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
+    """u_t = W^O [o_{t,1}; ...; o_{t,n_h}]: o [T, H, D] (heads concatenated in order),
+    W^O [d, H D] -> u [T, d]."""
+    o = np.asarray(o, dtype=np.float64)
+    return o.reshape(o.shape[0], -1) @ np.asarray(w_o, dtype=np.float64).T
 
 
 # --------------------------------------------------------------------------

@@ -530,3 +530,73 @@ def test_yarn_absorbed_equals_naive():
     np.testing.assert_allclose(o_lat2[0], o_lat[0], atol=1e-12)
     np.testing.assert_allclose(O.unabsorb(o_lat2, w_uv)[0], o[0], atol=1e-12)
     np.testing.assert_allclose(lse2[0], lse[0], atol=1e-12)
+
+
+# ---------------------------------------------------------------- upstream / downstream
+def test_rms_norm_closed_forms():
+    """RMSNorm of the compressed latent (「一文通透DeepSeek-V2」 §3.1.4), eps = 0 here:
+    x = (3, 4) has mean square 12.5, so it maps to (3, 4) / sqrt(12.5) = (0.848528, 1.131371);
+    a gain multiplies elementwise; the output's root mean square is the gain's magnitude; a
+    positive factor on the input changes nothing."""
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), np.ones(2), eps=0.0),
+                               [0.848528137423857, 1.131370849898476], rtol=1e-14)
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), np.array([2.0, -1.0]), eps=0.0),
+                               [1.697056274847714, -1.131370849898476], rtol=1e-14)
+    g = _rng(50)
+    x = g.standard_normal((5, 512))
+    y = O.rms_norm(x, np.full(512, 0.7), eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 0.7, rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(37.5 * x, np.ones(512), eps=0.0), O.rms_norm(x, np.ones(512), eps=0.0), rtol=1e-13)
+    # eps bounds the gain on tiny inputs: x * g / sqrt(eps) when mean(x^2) << eps
+    t = np.full(4, 1e-9)
+    np.testing.assert_allclose(O.rms_norm(t, np.ones(4), eps=1e-6), t / 1e-3, rtol=1e-6)
+
+
+def test_project_latent_selects_and_normalises():
+    """c^{KV} = RMSNorm(W^{DKV} h), k^R = W^{KR} h (「deepseek(2)——deepseek 關鍵技術」 §1,
+    「一文通透DeepSeek-V2」 §2.2.1-2.2.2): with W^{DKV} and W^{KR} selecting disjoint slices of
+    h, the latent is the normalised first slice and k^R the raw second one."""
+    g = _rng(51)
+    d, C, R = 40, 16, 8
+    h = g.standard_normal((3, d))
+    w_dkv = np.zeros((C, d)); w_dkv[:, :C] = np.eye(C)
+    w_kr = np.zeros((R, d)); w_kr[:, C:C + R] = np.eye(R)
+    gain = g.uniform(0.5, 1.5, C)
+    c, k = O.project_latent(h, w_dkv, w_kr, gain)
+    np.testing.assert_allclose(c, O.rms_norm(h[:, :C], gain), rtol=1e-14)
+    np.testing.assert_array_equal(k, h[:, C:C + R])
+
+
+def test_output_projection_hand_worked():
+    """u_t = W^O [o_{t,1}; o_{t,2}] with n_h = 2, d_h = 2, d = 3, worked by hand:
+    o = ((1, 2), (3, 4)) concatenates to (1, 2, 3, 4); the rows of W^O pick element 1,
+    element 3 and the sum: u = (1, 3, 10). It also equals the per-head sum
+    sum_i W^O[:, i d_h:(i+1) d_h] o_{t,i}."""
+    o = np.array([[[1.0, 2.0], [3.0, 4.0]]])
+    w_o = np.array([[1.0, 0, 0, 0], [0, 0, 1.0, 0], [1.0, 1.0, 1.0, 1.0]])
+    np.testing.assert_array_equal(O.output_projection(o, w_o), [[1.0, 3.0, 10.0]])
+    g = _rng(52)
+    o = g.standard_normal((4, 3, 5))
+    w_o = g.standard_normal((7, 15))
+    per_head = sum(o[:, i] @ w_o[:, 5 * i:5 * (i + 1)].T for i in range(3))
+    np.testing.assert_allclose(O.output_projection(o, w_o), per_head, rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_is_causal_attention_over_the_prompt():
+    """The non-absorbed prefill path (「一文通透DeepSeek-V2」 §2.2.1: the naive formula restores
+    k^C, v^C from the cached latent) is the naive decode with every prompt position as a query:
+    query t sees tokens 0..t. Checked against one-query decodes at each position."""
+    g = _rng(53)
+    H, D, C, R, L = 2, 4, 8, 4, 6
+    c, k_r = g.standard_normal((L, C)), g.standard_normal((L, R))
+    w_uk, w_uv = g.standard_normal((2, H, D, C)) * 0.5
+    q_c, q_r = g.standard_normal((L, H, D)), g.standard_normal((L, H, R))
+    ce = O.cache_entries(c, k_r, np.arange(L), "f32", 10000.0)
+    o, o_lat, lse = O.mla_decode_naive(ce["c"], ce["k_r"], q_c, q_r, w_uk, w_uv, np.arange(L), 10000.0)
+    for t in range(L):
+        o1, _, lse1 = O.mla_decode_naive(ce["c"][:t + 1], ce["k_r"][:t + 1], q_c[t:t + 1], q_r[t:t + 1],
+                                          w_uk, w_uv, np.array([t]), 10000.0)
+        np.testing.assert_allclose(o[t], o1[0], atol=1e-13)
+        np.testing.assert_allclose(lse[t], lse1[0], atol=1e-13)
+    # the first token attends to itself only
+    np.testing.assert_allclose(o[0], np.einsum("hdc,c->hd", w_uv, ce["c"][0]), atol=1e-13)
