@@ -201,6 +201,46 @@ int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, c
                  float* o, void* stream);
 
 /*
+ * mla_project_append — the fused upstream append: this step's hidden states to their cache
+ * entries in one call (「一文通透DeepSeek-V2」 §2.2.1 c^{KV}_t = W^{DKV} h_t, §3.1.4 the extra
+ * RMSNorm after the compressed latent, §2.2.2 k^R_t = RoPE(W^{KR} h_t)).
+ *
+ *   h          [T][d_model] bf16 hidden states (d_model a multiple of 8, 16-byte aligned)
+ *   w_dkv_kr   [C + R][d_model] bf16: rows 0..C-1 hold W^{DKV}, rows C..C+R-1 hold W^{KR}
+ *   gain       [C] fp32 gain of the latent's RMSNorm (it also carries the bottleneck's scaling)
+ *   eps        RMSNorm epsilon (> 0)
+ *   seq_idx, pos, block_table, batch, max_pages_per_seq, num_pages, kv_pool: as
+ *              mla_append_cache (bf16 or FP8 cache)
+ *   workspace  >= mla_project_append_workspace_size() bytes of device scratch
+ * x = W^{DKV} h and k^R = W^{KR} h are formed on the tensor cores with fp32 accumulation;
+ * c^{KV} = gain * x / sqrt(mean(x^2) + eps) in fp32; both are rounded to bf16 (the type a
+ * separate projection would store) and then cached exactly as mla_append_cache caches them
+ * (RoPE of k^R at the token's position, optional E4M3 groups). Errors as mla_append_cache;
+ * MLA_ERR_UNSUPPORTED for an fp32 cache or activations.
+ */
+size_t mla_project_append_workspace_size(const mla_config* cfg, int32_t d_model, int32_t num_tokens);
+int mla_project_append(const mla_config* cfg, const void* h, int32_t d_model, int32_t num_tokens,
+                       const void* w_dkv_kr, const float* gain, float eps, const int32_t* seq_idx,
+                       const int32_t* pos, const int32_t* block_table, int32_t batch,
+                       int32_t max_pages_per_seq, int32_t num_pages, void* kv_pool,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * mla_output_projection — u_t = W^O [o_{t,1}; ...; o_{t,n_h}] (「一文通透DeepSeek-V2」 §2.1.2,
+ * W^O in R^{d x d_h n_h}; 「deepseek(2)——deepseek 關鍵技術」 §1).
+ *   o     [T][H * D] bf16: the heads' outputs, concatenated in head order
+ *   w_o   [d_model][H * D] bf16 (H * D and d_model multiples of 8; 16-byte aligned)
+ *   u     [T][d_model] fp32
+ *   workspace >= mla_output_projection_workspace_size() bytes (fp32 split partials; may be 0)
+ * fp32 accumulation on the tensor cores; partial sums over K ranges are added in a fixed order,
+ * so the result does not depend on scheduling.
+ */
+size_t mla_output_projection_workspace_size(const mla_config* cfg, int32_t d_model, int32_t num_tokens);
+int mla_output_projection(const mla_config* cfg, const void* o, int32_t num_tokens, const void* w_o,
+                          int32_t d_model, float* u, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+
+/*
  * mla_decode_noalloc — mla_decode for callers that cannot allocate device memory. The pages
  * have no counterpart to this call; it is a convenience of this library.
  *

@@ -27,6 +27,10 @@ from ._lib import (  # noqa: F401
     mla_decode_kernel,
     mla_decode_noalloc,
     mla_decode_workspace_size,
+    mla_output_projection,
+    mla_output_projection_workspace_size,
+    mla_project_append,
+    mla_project_append_workspace_size,
     mla_status_string,
     mla_unabsorb,
 )

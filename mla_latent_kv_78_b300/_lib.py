@@ -91,6 +91,12 @@ _SIGS = {
     "mla_decode_noalloc": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _I, _I, _P, _I,
                                           _I, _I, _I, _P, _P, _P, _P]),
     "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mla_project_append_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(mla_config), _I, _I]),
+    "mla_project_append": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _I, _I, _P, _P, ctypes.c_float,
+                                          _P, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P, _P]),
+    "mla_output_projection_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(mla_config), _I, _I]),
+    "mla_output_projection": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _I, _P, _I, _P, _P,
+                                             ctypes.c_size_t, _P, _P]),
     "mla_debug_decode_fault": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_int32]),
 }
 EXPORTED = tuple(_SIGS)
@@ -191,6 +197,38 @@ def mla_decode_noalloc(cfg: mla_config, q_lat, kv_pool, block_table, seq_lens, n
     _check("mla_decode_noalloc", lib().mla_decode_noalloc(
         ctypes.byref(cfg), _ptr(q_lat), _ptr(kv_pool), _ptr(block_table), maxp, num_pages,
         _ptr(seq_lens), batch, n_q, max_seq_len, num_splits, _ptr(o_lat), _ptr(lse),
+        _ptr(dev_status), _stream(stream)))
+
+
+def mla_project_append_workspace_size(cfg: mla_config, d_model: int, num_tokens: int) -> int:
+    return int(lib().mla_project_append_workspace_size(ctypes.byref(cfg), d_model, num_tokens))
+
+
+def mla_project_append(cfg: mla_config, h, w_dkv_kr, gain, eps: float, seq_idx, pos, block_table,
+                       kv_pool, workspace, num_pages: Optional[int] = None, dev_status=None,
+                       stream=None) -> None:
+    T, d_model = h.shape
+    batch, maxp = block_table.shape
+    if num_pages is None:
+        num_pages = kv_pool.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("mla_project_append", lib().mla_project_append(
+        ctypes.byref(cfg), _ptr(h), d_model, T, _ptr(w_dkv_kr), _ptr(gain), eps, _ptr(seq_idx),
+        _ptr(pos), _ptr(block_table), batch, maxp, num_pages, _ptr(kv_pool), _ptr(workspace),
+        ws_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def mla_output_projection_workspace_size(cfg: mla_config, d_model: int, num_tokens: int) -> int:
+    return int(lib().mla_output_projection_workspace_size(ctypes.byref(cfg), d_model, num_tokens))
+
+
+def mla_output_projection(cfg: mla_config, o, w_o, u, workspace=None, dev_status=None,
+                          stream=None) -> None:
+    T = o.shape[0]
+    d_model = w_o.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_output_projection", lib().mla_output_projection(
+        ctypes.byref(cfg), _ptr(o), T, _ptr(w_o), d_model, _ptr(u), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream(stream)))
 
 

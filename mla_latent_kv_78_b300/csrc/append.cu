@@ -10,6 +10,7 @@
 // once; the FP8 scale and the per-element division are IEEE fp32 (__fdiv_rn), so the integer
 // codes match a CPU encoder that takes the same fp32 decisions.
 #include "mla_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace mla {
 
@@ -43,34 +44,12 @@ __device__ __forceinline__ void rope_pair(const RopeTable& rt, int pos, int k, i
   }
 }
 
+// One token's cache entry (one warp): [c ; RoPE_pos(k^R)] into its slot, c as E4M3 codes with
+// per-group fp32 scales for an FP8 cache. src_c / src_r may point to global or shared memory.
 template <typename In, int CACHE>
-__global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restrict__ c_kv,
-                                                     const In* __restrict__ k_r,
-                                                     const int32_t* __restrict__ seq_idx,
-                                                     const int32_t* __restrict__ pos, int T,
-                                                     const int32_t* __restrict__ bt, int batch,
-                                                     int maxp, int num_pages,
-                                                     uint8_t* __restrict__ pool,
-                                                     int32_t* status, const RopeTable rt) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const In* src_c = c_kv + (size_t)t * d.C;
-  const In* src_r = k_r + (size_t)t * d.R;
-  const int b = seq_idx[t];
-  const int p = pos[t];
-  if (b < 0 || b >= batch || p < 0 || p / d.P >= maxp) {
-    if (lane == 0) flag_status(status, MLA_DEV_INDEX_OUT_OF_RANGE);
-    return;
-  }
-  const int page = bt[(size_t)b * maxp + p / d.P];
-  if (page < 0 || page >= num_pages) {
-    if (lane == 0) flag_status(status, MLA_DEV_INDEX_OUT_OF_RANGE);
-    return;
-  }
-  uint8_t* dst = pool + ((size_t)page * d.P + (p % d.P)) * (size_t)d.entry_bytes;
+__device__ __forceinline__ void write_entry(const Dims& d, const In* src_c, const In* src_r, int p,
+                                            uint8_t* dst, const RopeTable& rt, int lane) {
   const double base = (double)d.rope_base;
-
   if constexpr (CACHE != MLA_FP8_E4M3) {
     In* out = reinterpret_cast<In*>(dst);
     // the latent row: 16-byte vectors when the row and both ends are 16-byte aligned
@@ -119,6 +98,91 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restric
   }
 }
 
+// The pool entry of token (b, p), or nullptr (flagged) when an index is out of range.
+__device__ __forceinline__ uint8_t* entry_of(const Dims& d, int b, int p, const int32_t* bt, int batch,
+                                             int maxp, int num_pages, uint8_t* pool, int32_t* status,
+                                             int lane) {
+  if (b < 0 || b >= batch || p < 0 || p / d.P >= maxp) {
+    if (lane == 0) flag_status(status, MLA_DEV_INDEX_OUT_OF_RANGE);
+    return nullptr;
+  }
+  const int page = bt[(size_t)b * maxp + p / d.P];
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0) flag_status(status, MLA_DEV_INDEX_OUT_OF_RANGE);
+    return nullptr;
+  }
+  return pool + ((size_t)page * d.P + (p % d.P)) * (size_t)d.entry_bytes;
+}
+
+template <typename In, int CACHE>
+__global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restrict__ c_kv,
+                                                     const In* __restrict__ k_r,
+                                                     const int32_t* __restrict__ seq_idx,
+                                                     const int32_t* __restrict__ pos, int T,
+                                                     const int32_t* __restrict__ bt, int batch,
+                                                     int maxp, int num_pages,
+                                                     uint8_t* __restrict__ pool,
+                                                     int32_t* status, const RopeTable rt) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int p = pos[t];
+  uint8_t* dst = entry_of(d, seq_idx[t], p, bt, batch, maxp, num_pages, pool, status, lane);
+  if (!dst) return;
+  write_entry<In, CACHE>(d, c_kv + (size_t)t * d.C, k_r + (size_t)t * d.R, p, dst, rt, lane);
+}
+
+// Epilogue of the fused upstream append (「一文通透DeepSeek-V2」 §2.2.1 c^{KV} = W^{DKV} h, §3.1.4
+// the RMSNorm after the compressed latent, §2.2.2 k^R = RoPE(W^{KR} h)), one warp per token:
+// the projection's split partials [splits][T][C + R] are summed in split order, the latent is
+// normalised (gain * x / sqrt(mean(x^2) + eps), fp32), both parts are rounded to bf16 in shared
+// memory (the activation type a separate projection would have produced) and the entry is
+// written as mla_append_cache writes it.
+template <int CACHE>
+__global__ void __launch_bounds__(128) project_append_kernel(
+    Dims d, const float* __restrict__ part, int splits, const float* __restrict__ gain, float eps,
+    const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ pos, int T,
+    const int32_t* __restrict__ bt, int batch, int maxp, int num_pages, uint8_t* __restrict__ pool,
+    int32_t* status, const RopeTable rt) {
+  // per warp: the latent's fp32 sums [C], then the bf16 row [C + R] the entry is written from
+  extern __shared__ __align__(16) float stage[];
+  ptx::griddep_wait();
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int CR = d.C + d.R;
+  float* xs = stage + (size_t)(threadIdx.x >> 5) * (d.C + (CR + 1) / 2 + 4);
+  __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(xs + d.C);
+  const size_t count = (size_t)T * CR;
+  const float* src = part + (size_t)t * CR;
+  float sq = 0.f;
+  for (int k = lane; k < CR; k += 32) {
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += src[(size_t)s * count + k];
+    if (k < d.C) {
+      xs[k] = acc;
+      sq += acc * acc;
+    } else {
+      row[k] = __float2bfloat16_rn(acc);   // k^R: no norm
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  const float inv = 1.0f / sqrtf(sq / (float)d.C + eps);
+  __syncwarp();
+  for (int k = lane; k < d.C; k += 32) row[k] = __float2bfloat16_rn(xs[k] * inv * gain[k]);
+  __syncwarp();
+  const int p = pos[t];
+  uint8_t* dst = entry_of(d, seq_idx[t], p, bt, batch, maxp, num_pages, pool, status, lane);
+  if (!dst) return;
+  write_entry<__nv_bfloat16, CACHE>(d, row, row + d.C, p, dst, rt, lane);
+}
+
+// Shared-memory bytes of project_append_kernel's 128-thread block.
+inline size_t project_append_smem(const Dims& d) {
+  return 4 * sizeof(float) * ((size_t)d.C + (size_t)(d.C + d.R + 1) / 2 + 4);
+}
+
 cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, const int32_t* seq_idx,
                           const int32_t* pos, int T, const int32_t* bt, int batch, int maxp,
                           int num_pages, void* pool, int32_t* status, cudaStream_t stream) {
@@ -145,6 +209,32 @@ cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, cons
       break;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_project_append(const Dims& d, const void* h, int d_model, const void* w, int T,
+                                  const float* gain, float eps, const int32_t* seq_idx,
+                                  const int32_t* pos, const int32_t* bt, int batch, int maxp,
+                                  int num_pages, void* pool, void* ws, int splits, int32_t* status,
+                                  cudaStream_t stream) {
+  const int CR = d.C + d.R;
+  float* part = static_cast<float*>(ws);
+  // [c^{KV}; k^R] pre-norm, as split partials: X = h [T][d_model], W = [W^{DKV}; W^{KR}] [CR][d_model]
+  cudaError_t e = launch_gemm(h, w, T, CR, d_model, splits, part, nullptr, kGemmPartials, status, stream);
+  if (e != cudaSuccess) return e;
+  RopeTable rt;
+  fill_rope_table(&rt, d);
+  const size_t smem = project_append_smem(d);
+  const int blocks = (T * 32 + 127) / 128;
+  uint8_t* out = static_cast<uint8_t*>(pool);
+  if (d.cache_dtype == MLA_FP8_E4M3)
+    e = launch_programmatic(project_append_kernel<MLA_FP8_E4M3>, dim3(blocks), dim3(128), smem, stream, d,
+                            (const float*)part, splits, gain, eps, seq_idx, pos, T, bt, batch, maxp,
+                            num_pages, out, status, rt);
+  else
+    e = launch_programmatic(project_append_kernel<MLA_BF16>, dim3(blocks), dim3(128), smem, stream, d,
+                            (const float*)part, splits, gain, eps, seq_idx, pos, T, bt, batch, maxp,
+                            num_pages, out, status, rt);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace mla

@@ -199,6 +199,68 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
                                          o_lat, lse, dev_status, (cudaStream_t)stream));
 }
 
+size_t mla_project_append_workspace_size(const mla_config* cfg, int32_t d_model, int32_t num_tokens) {
+  Dims d;
+  if (make_dims(cfg, &d) != MLA_OK || d_model < 1 || num_tokens < 1) return 0;
+  const int N = d.C + d.R;
+  const int s = mla::gemm_pick_splits(num_tokens, N, d_model, num_sms());
+  return ((size_t)s * num_tokens * N * sizeof(float) + 255) / 256 * 256;
+}
+
+int mla_project_append(const mla_config* cfg, const void* h, int32_t d_model, int32_t num_tokens,
+                       const void* w_dkv_kr, const float* gain, float eps, const int32_t* seq_idx,
+                       const int32_t* pos, const int32_t* block_table, int32_t batch,
+                       int32_t max_pages_per_seq, int32_t num_pages, void* kv_pool,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc != MLA_OK) return rc;
+  if (num_tokens < 0 || d_model < 1 || batch < 0 || max_pages_per_seq < 0 || num_pages < 0 || !(eps > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  if (d.act_dtype != MLA_BF16 || d.cache_dtype == MLA_F32) return MLA_ERR_UNSUPPORTED;
+  if (d_model % 8 || d.C % 8 || d.R % 2) return MLA_ERR_UNSUPPORTED;
+  if (!h || !w_dkv_kr || !gain || !seq_idx || !pos || !block_table || !kv_pool || batch < 1 ||
+      max_pages_per_seq < 1 || num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w_dkv_kr) || !aligned16(kv_pool)) return MLA_ERR_ALIGNMENT;
+  const size_t need = mla_project_append_workspace_size(cfg, d_model, num_tokens);
+  if (workspace_bytes < need || !workspace) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+  const int splits = mla::gemm_pick_splits(num_tokens, d.C + d.R, d_model, num_sms());
+  return cuda_rc(mla::launch_project_append(d, h, d_model, w_dkv_kr, num_tokens, gain, eps, seq_idx,
+                                            pos, block_table, batch, max_pages_per_seq, num_pages,
+                                            kv_pool, workspace, splits, dev_status,
+                                            (cudaStream_t)stream));
+}
+
+size_t mla_output_projection_workspace_size(const mla_config* cfg, int32_t d_model, int32_t num_tokens) {
+  Dims d;
+  if (make_dims(cfg, &d) != MLA_OK || d_model < 1 || num_tokens < 1) return 0;
+  return mla::gemm_workspace_bytes(num_tokens, d_model, d.H * d.D, MLA_F32, num_sms());
+}
+
+int mla_output_projection(const mla_config* cfg, const void* o, int32_t num_tokens, const void* w_o,
+                          int32_t d_model, float* u, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc != MLA_OK) return rc;
+  if (num_tokens < 0 || d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  if (d.act_dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
+  const int K = d.H * d.D;
+  if (K % 8 || d_model % 8) return MLA_ERR_UNSUPPORTED;
+  if (!o || !w_o || !u) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(w_o)) return MLA_ERR_ALIGNMENT;
+  const size_t need = mla_output_projection_workspace_size(cfg, d_model, num_tokens);
+  if (workspace_bytes < need || (need && !workspace)) return MLA_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+  const int splits = mla::gemm_pick_splits(num_tokens, d_model, K, num_sms());
+  return cuda_rc(mla::launch_gemm(o, w_o, num_tokens, d_model, K, splits, static_cast<float*>(workspace),
+                                  u, MLA_F32, dev_status, (cudaStream_t)stream));
+}
+
 int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, const void* w_uv,
                  float* o, void* stream) {
   Dims d;

@@ -71,6 +71,22 @@ cudaError_t launch_decode_simt(const Dims& d, const void* q_lat, const void* poo
 cudaError_t launch_combine(int C, int S, const float* ws_o, const float* ws_lse, void* o_lat,
                            int act_dtype, float* lse, size_t rows, cudaStream_t stream);
 
+// Tensor-core projection Y = X . W^T (X [T][K], W [N][K] bf16; K a multiple of 8). Y is fp32 or
+// bf16 (out_dtype); kGemmPartials leaves the fp32 split partials [splits][T][N] in `part`.
+constexpr int kGemmPartials = -1;
+int gemm_pick_splits(int T, int N, int K, int num_sms);
+size_t gemm_workspace_bytes(int T, int N, int K, int out_dtype, int num_sms);
+cudaError_t launch_gemm(const void* x, const void* w, int T, int N, int K, int splits, float* part,
+                        void* y, int out_dtype, int32_t* status, cudaStream_t stream);
+
+// Fused upstream append: [W^{DKV}; W^{KR}] h as split partials in ws, then RMSNorm, RoPE and the
+// cache write in one epilogue kernel.
+cudaError_t launch_project_append(const Dims& d, const void* h, int d_model, const void* w, int T,
+                                  const float* gain, float eps, const int32_t* seq_idx,
+                                  const int32_t* pos, const int32_t* bt, int batch, int maxp,
+                                  int num_pages, void* pool, void* ws, int splits, int32_t* status,
+                                  cudaStream_t stream);
+
 // Tensor-core decode (tcgen05 + TMEM + TMA), V2 head shapes only.
 bool tc_supported(const Dims& d, int n_q);
 size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,
