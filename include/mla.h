@@ -241,6 +241,24 @@ int mla_output_projection(const mla_config* cfg, const void* o, int32_t num_toke
                           int32_t* dev_status, void* stream);
 
 /*
+ * mla_prefill — the non-absorbed path over a prompt (「一文通透DeepSeek-V2」 §2.2.1: the naive
+ * formula restores k^C_{n,i} = W^{UK}_i c^{KV}_n and v^C_{n,i} = W^{UV}_i c^{KV}_n;
+ * 「deepseek(2)——deepseek 關鍵技術」 §1 for q, k and o), causal over positions 0 .. L-1:
+ *   o[t][i] = sum_{n <= t} softmax_n([q^C_{t,i}; RoPE_t(q^R_{t,i})] . [k^C_{n,i}; k^R_n] * scale) v^C_{n,i}
+ *   c_kv   [L][C] bf16   the prompt's latents as cached
+ *   k_r    [L][R] bf16   the prompt's RoPE keys, already rotated (as cached)
+ *   q_c    [L][H][D], q_r [L][H][R] bf16 (q^R before rotation)
+ *   w_uk, w_uv [H][D][C] bf16;  o [L][H][D] fp32
+ *   workspace >= mla_prefill_workspace_size() bytes (K^C, V^C and the assembled queries)
+ * Tensor-core path for d_head = 128, d_rope = 64, bf16 activations (MLA_ERR_UNSUPPORTED
+ * otherwise); RoPE and the softmax scale follow cfg (YaRN included).
+ */
+size_t mla_prefill_workspace_size(const mla_config* cfg, int32_t prompt_len);
+int mla_prefill(const mla_config* cfg, const void* c_kv, const void* k_r, int32_t prompt_len,
+                const void* q_c, const void* q_r, const void* w_uk, const void* w_uv, float* o,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * mla_decode_noalloc — mla_decode for callers that cannot allocate device memory. The pages
  * have no counterpart to this call; it is a convenience of this library.
  *

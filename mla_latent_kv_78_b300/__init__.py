@@ -29,6 +29,8 @@ from ._lib import (  # noqa: F401
     mla_decode_workspace_size,
     mla_output_projection,
     mla_output_projection_workspace_size,
+    mla_prefill,
+    mla_prefill_workspace_size,
     mla_project_append,
     mla_project_append_workspace_size,
     mla_status_string,

@@ -95,6 +95,9 @@ _SIGS = {
     "mla_project_append": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _I, _I, _P, _P, ctypes.c_float,
                                           _P, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P, _P]),
     "mla_output_projection_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(mla_config), _I, _I]),
+    "mla_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(mla_config), _I]),
+    "mla_prefill": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _I, _P, _P, _P, _P, _P, _P,
+                                   ctypes.c_size_t, _P, _P]),
     "mla_output_projection": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _I, _P, _I, _P, _P,
                                              ctypes.c_size_t, _P, _P]),
     "mla_debug_decode_fault": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_int32]),
@@ -230,6 +233,19 @@ def mla_output_projection(cfg: mla_config, o, w_o, u, workspace=None, dev_status
     _check("mla_output_projection", lib().mla_output_projection(
         ctypes.byref(cfg), _ptr(o), T, _ptr(w_o), d_model, _ptr(u), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream(stream)))
+
+
+def mla_prefill_workspace_size(cfg: mla_config, prompt_len: int) -> int:
+    return int(lib().mla_prefill_workspace_size(ctypes.byref(cfg), prompt_len))
+
+
+def mla_prefill(cfg: mla_config, c_kv, k_r, q_c, q_r, w_uk, w_uv, o, workspace, dev_status=None,
+                stream=None) -> None:
+    L = c_kv.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("mla_prefill", lib().mla_prefill(
+        ctypes.byref(cfg), _ptr(c_kv), _ptr(k_r), L, _ptr(q_c), _ptr(q_r), _ptr(w_uk), _ptr(w_uv),
+        _ptr(o), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)))
 
 
 def mla_unabsorb(cfg: mla_config, o_lat, w_uv, o, stream=None) -> None:

@@ -38,6 +38,7 @@ struct GemmParams {
   int T, N, K;
   int k_steps;     // 64-wide K steps per split
   float* out;      // [T][N] when splits == 1, else partials [splits][T][N]
+  __nv_bfloat16* out_bf16;   // non-null: Y [T][N] in bf16 directly (splits == 1)
   int32_t* status;
 };
 
@@ -150,7 +151,12 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
       for (int x = 0; x < 32; ++x) {
         const int t = t0 + c + x;
-        if (t < p.T) out[(size_t)t * p.N + n] = v[x];
+        if (t < p.T) {
+          if (p.out_bf16)
+            p.out_bf16[(size_t)t * p.N + n] = __float2bfloat16_rn(v[x]);
+          else
+            out[(size_t)t * p.N + n] = v[x];
+        }
       }
     }
   }
@@ -188,7 +194,7 @@ int gemm_pick_splits(int T, int N, int K, int num_sms) {
 // Partial-sum bytes launch_gemm needs for these sizes and output type.
 size_t gemm_workspace_bytes(int T, int N, int K, int out_dtype, int num_sms) {
   const int s = gemm_pick_splits(T, N, K, num_sms);
-  return (s > 1 || out_dtype != MLA_F32) ? ((size_t)s * T * N * sizeof(float) + 255) / 256 * 256 : 0;
+  return s > 1 ? ((size_t)s * T * N * sizeof(float) + 255) / 256 * 256 : 0;
 }
 
 // Y = X . W^T: X [T][K] bf16, W [N][K] bf16, Y [T][N] of out_dtype (MLA_F32 or MLA_BF16).
@@ -217,8 +223,9 @@ cudaError_t launch_gemm(const void* x, const void* w, int T, int N, int K, int s
   p.K = K;
   p.k_steps = (steps + splits - 1) / splits;
   p.status = status;
-  const bool direct = splits == 1 && out_dtype == MLA_F32;
-  p.out = direct ? static_cast<float*>(y) : part;
+  const bool direct = splits == 1 && (out_dtype == MLA_F32 || out_dtype == MLA_BF16);
+  p.out = direct && out_dtype == MLA_F32 ? static_cast<float*>(y) : part;
+  p.out_bf16 = direct && out_dtype == MLA_BF16 ? static_cast<__nv_bfloat16*>(y) : nullptr;
   const bool reduce = !direct && out_dtype != kGemmPartials;
   dim3 grid((N + gemm::kBM - 1) / gemm::kBM, (T + bn - 1) / bn, splits);
   cudaError_t e;

@@ -261,6 +261,31 @@ int mla_output_projection(const mla_config* cfg, const void* o, int32_t num_toke
                                   u, MLA_F32, dev_status, (cudaStream_t)stream));
 }
 
+size_t mla_prefill_workspace_size(const mla_config* cfg, int32_t prompt_len) {
+  Dims d;
+  if (make_dims(cfg, &d) != MLA_OK || prompt_len < 1 || !mla::prefill_supported(d)) return 0;
+  return mla::prefill_workspace_bytes(d, prompt_len);
+}
+
+int mla_prefill(const mla_config* cfg, const void* c_kv, const void* k_r, int32_t prompt_len,
+                const void* q_c, const void* q_r, const void* w_uk, const void* w_uv, float* o,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc != MLA_OK) return rc;
+  if (prompt_len < 0) return MLA_ERR_INVALID_ARG;
+  if (prompt_len == 0) return MLA_OK;
+  if (!mla::prefill_supported(d)) return MLA_ERR_UNSUPPORTED;
+  if (!c_kv || !k_r || !q_c || !q_r || !w_uk || !w_uv || !o) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_kv) || !aligned16(k_r) || !aligned16(q_c) || !aligned16(q_r) || !aligned16(w_uk) ||
+      !aligned16(w_uv) || !aligned16(o))
+    return MLA_ERR_ALIGNMENT;
+  if (workspace_bytes < mla::prefill_workspace_bytes(d, prompt_len) || !workspace) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+  return cuda_rc(mla::launch_prefill(d, c_kv, k_r, prompt_len, q_c, q_r, w_uk, w_uv, o, workspace,
+                                     dev_status, (cudaStream_t)stream));
+}
+
 int mla_unabsorb(const mla_config* cfg, const void* o_lat, int32_t num_tokens, const void* w_uv,
                  float* o, void* stream) {
   Dims d;

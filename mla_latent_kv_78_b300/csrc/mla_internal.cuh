@@ -87,6 +87,13 @@ cudaError_t launch_project_append(const Dims& d, const void* h, int d_model, con
                                   int num_pages, void* pool, void* ws, int splits, int32_t* status,
                                   cudaStream_t stream);
 
+// Non-absorbed prefill (K^C, V^C by the projection GEMM, causal tcgen05 attention).
+bool prefill_supported(const Dims& d);
+size_t prefill_workspace_bytes(const Dims& d, int L);
+cudaError_t launch_prefill(const Dims& d, const void* c_kv, const void* k_r, int L, const void* q_c,
+                           const void* q_r, const void* w_uk, const void* w_uv, float* o, void* ws,
+                           int32_t* status, cudaStream_t stream);
+
 // Tensor-core decode (tcgen05 + TMEM + TMA), V2 head shapes only.
 bool tc_supported(const Dims& d, int n_q);
 size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,

@@ -146,3 +146,37 @@ def test_project_append_then_decode_matches_the_chain(cache):
                                        np.array([L - 1]), 10000.0)
     assert_close(wl, step.o.cpu().numpy(), o, "o")
     assert_close(wl, step.o_lat.float().cpu().numpy(), o_lat, "o_lat")
+
+
+@needs_cuda
+@pytest.mark.parametrize("L,yarn", [(200, False), (1, False), (64, False), (300, True)],
+                         ids=["L200", "L1", "L64", "L300-yarn"])
+def test_prefill_matches_the_naive_definition(L, yarn):
+    """mla_prefill (k^C, v^C restored from the latents, causal attention over the prompt)
+    against the oracle's non-absorbed definition with every prompt position as a query
+    (「一文通透DeepSeek-V2」 §2.2.1; 「deepseek(2)——deepseek 關鍵技術」 §1), on a subset of the 128
+    heads; L = 200 leaves a ragged 72-query block and a partly masked key block."""
+    from _support import tau_of, theta_of
+    wl = W.small_v2(1, [L], n_q=1, cache="bf16", seed=200 + L, rope_scaling=40.0 if yarn else 1.0)
+    H, D, C, R = wl.H, wl.D, wl.C, wl.R
+    cfg = M.make_config(H, D, C, R, wl.P, rope_scaling=wl.rope_scaling if yarn else 0.0)
+    g = _rng(300 + L)
+    c = _bf16(g.standard_normal((L, C)))
+    k_r = _bf16(g.standard_normal((L, R)))
+    q_c = _bf16(g.standard_normal((L, H, D)))
+    q_r = _bf16(g.standard_normal((L, H, R)))
+    w_uk, w_uv = wl.weights()
+    ce = O.cache_entries(c, k_r, np.arange(L), "bf16", wl.rope_base, theta_of(wl))
+    o = torch.full((L, H, D), float("nan"), device="cuda")
+    ws = torch.empty(M.mla_prefill_workspace_size(cfg, L), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.mla_prefill(cfg, dev(ce["c"], BF), dev(ce["k_r"], BF), dev(q_c, BF), dev(q_r, BF), dev(w_uk, BF),
+                  dev(w_uv, BF), o, ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    heads = np.array([0, 1, 63, 64, 127])
+    ref, _, _ = O.mla_decode_naive(ce["c"], ce["k_r"], q_c, q_r, w_uk, w_uv, np.arange(L), wl.rope_base,
+                                   heads=heads, theta=theta_of(wl), scale=tau_of(wl))
+    got = o.cpu().numpy()[:, heads]
+    assert np.all(np.isfinite(o.cpu().numpy()))
+    assert_close(wl, got, ref, f"prefill o (L={L})")
