@@ -309,6 +309,83 @@ def _other_workloads(M, W, torch, dev, flush, peaks, steps: int = 5):
     return out
 
 
+def _time_ms(torch, fn, flush, steps=7):
+    """Median CUDA-event time of fn() captured once as a CUDA graph and replayed `steps` times,
+    L2 flushed before each replay (so host-side launch work is not timed)."""
+    fn()   # first call outside the capture: one-time per-process set-up
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    with torch.cuda.graph(graph):
+        ev[0].record()
+        fn()
+        ev[1].record()
+    ts = []
+    for k in range(steps + 2):
+        flush.fill_(float(k))
+        graph.replay()
+        torch.cuda.synchronize()
+        if k >= 2:
+            ts.append(ev[0].elapsed_time(ev[1]))
+    return statistics.median(ts)
+
+
+def _next_rows(M, W, torch, dev, flush, peaks):
+    """The steps either side of the decode, at DeepSeek-V2 sizes (d = 5120), each against its
+    roofline: the fused upstream append for one decode step's 64 tokens, the W^O output
+    projection for those tokens, and the non-absorbed prefill of a 4096-token prompt."""
+    bf = torch.bfloat16
+    g = torch.Generator(device=dev)
+    g.manual_seed(7890)
+    H, D, C, R, P, d_model = 128, 128, 512, 64, 64, 5120
+    out = {}
+    # fused upstream append: h [64][5120] -> cache entries of 64 sequences
+    T = 64
+    cfg = M.make_config(H, D, C, R, P)
+    h = torch.randn(T, d_model, device=dev, generator=g).to(bf)
+    w = (torch.randn(C + R, d_model, device=dev, generator=g) * 0.02).to(bf)
+    gain = torch.rand(C, device=dev, generator=g) + 0.5
+    bt = torch.arange(T, dtype=torch.int32, device=dev).reshape(T, 1)
+    pool = torch.zeros(T, P, M.mla_cache_entry_bytes(cfg), dtype=torch.uint8, device=dev)
+    seq = torch.arange(T, dtype=torch.int32, device=dev)
+    pos = torch.full((T,), 17, dtype=torch.int32, device=dev)
+    ws = torch.empty(M.mla_project_append_workspace_size(cfg, d_model, T), dtype=torch.uint8, device=dev)
+    ms = _time_ms(torch, lambda: M.mla_project_append(cfg, h, w, gain, 1e-6, seq, pos, bt, pool, ws), flush)
+    byt = (C + R) * d_model * 2 + T * d_model * 2 + T * (C + R) * 2
+    out["project_append_t64"] = {"us": ms * 1e3, "gbs": byt / (ms * 1e-3) / 1e9,
+                                 "hbm_frac": byt / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                 "algorithmic_bytes": byt, "bound": "hbm (weights)"}
+    # W^O: u [64][5120] = o [64][16384] . W^O^T
+    o = (torch.randn(T, H * D, device=dev, generator=g) * 0.05).to(bf)
+    w_o = (torch.randn(d_model, H * D, device=dev, generator=g) * 0.006).to(bf)
+    u = torch.empty(T, d_model, device=dev)
+    ws2 = torch.empty(max(M.mla_output_projection_workspace_size(cfg, d_model, T), 16), dtype=torch.uint8, device=dev)
+    ms = _time_ms(torch, lambda: M.mla_output_projection(cfg, o, w_o, u, ws2), flush)
+    byt = d_model * H * D * 2 + T * H * D * 2 + T * d_model * 4
+    out["output_projection_t64"] = {"us": ms * 1e3, "gbs": byt / (ms * 1e-3) / 1e9,
+                                    "hbm_frac": byt / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                    "algorithmic_bytes": byt, "bound": "hbm (weights)"}
+    del o, w_o, u, ws2
+    # prefill of one 4096-token prompt: decompression GEMMs + causal attention
+    L = 4096
+    c = torch.randn(L, C, device=dev, generator=g).to(bf)
+    k_r = torch.randn(L, R, device=dev, generator=g).to(bf)
+    q_c = torch.randn(L, H, D, device=dev, generator=g).to(bf)
+    q_r = torch.randn(L, H, R, device=dev, generator=g).to(bf)
+    w_uk = (torch.randn(H, D, C, device=dev, generator=g) * 0.02).to(bf)
+    w_uv = (torch.randn(H, D, C, device=dev, generator=g) * 0.02).to(bf)
+    op = torch.empty(L, H, D, device=dev)
+    ws3 = torch.empty(M.mla_prefill_workspace_size(cfg, L), dtype=torch.uint8, device=dev)
+    ms = _time_ms(torch, lambda: M.mla_prefill(cfg, c, k_r, q_c, q_r, w_uk, w_uv, op, ws3), flush, steps=5)
+    flops = 2 * 2 * L * C * H * D + H * (L * (L + 1) // 2) * 2 * (D + R + D)
+    out["prefill_l4096"] = {"us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
+                            "tensor_frac": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                            "flops": flops, "bound": "tensor"}
+    del c, k_r, q_c, q_r, w_uk, w_uv, op, ws3
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, world, rank, local_rank):
     import torch
 
@@ -446,6 +523,7 @@ def run_ours(args, world, rank, local_rank):
     }
     if not args.no_extra:
         line["other_workloads"] = _other_workloads(M, W, torch, dev, flush, peaks)
+        line["next_rows"] = _next_rows(M, W, torch, dev, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         v, sample, threads, t = _cpu_oracle_sample(wl, budget_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
