@@ -133,30 +133,31 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restric
 }
 
 // Epilogue of the fused upstream append (「一文通透DeepSeek-V2」 §2.2.1 c^{KV} = W^{DKV} h, §3.1.4
-// the RMSNorm after the compressed latent, §2.2.2 k^R = RoPE(W^{KR} h)), one warp per token:
-// the projection's split partials [splits][T][C + R] are summed in split order, the latent is
-// normalised (gain * x / sqrt(mean(x^2) + eps), fp32), both parts are rounded to bf16 in shared
-// memory (the activation type a separate projection would have produced) and the entry is
-// written as mla_append_cache writes it.
+// the RMSNorm after the compressed latent, §2.2.2 k^R = RoPE(W^{KR} h)), one 256-thread block per
+// token: the projection's split partials [splits][T][C + R] are summed in split order (each
+// thread a few elements, so many loads are in flight), the latent is normalised
+// (gain * x / sqrt(mean(x^2) + eps), fp32, a block-wide sum of squares), both parts are rounded
+// to bf16 in shared memory (the activation type a separate projection would have produced) and
+// warp 0 writes the entry as mla_append_cache writes it.
 template <int CACHE>
-__global__ void __launch_bounds__(128) project_append_kernel(
+__global__ void __launch_bounds__(256) project_append_kernel(
     Dims d, const float* __restrict__ part, int splits, const float* __restrict__ gain, float eps,
     const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ pos, int T,
     const int32_t* __restrict__ bt, int batch, int maxp, int num_pages, uint8_t* __restrict__ pool,
     int32_t* status, const RopeTable rt) {
-  // per warp: the latent's fp32 sums [C], then the bf16 row [C + R] the entry is written from
+  // the latent's fp32 sums [C], the bf16 row [C + R], 8 warp partial sums of squares
   extern __shared__ __align__(16) float stage[];
   ptx::griddep_wait();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int CR = d.C + d.R;
-  float* xs = stage + (size_t)(threadIdx.x >> 5) * (d.C + (CR + 1) / 2 + 4);
-  __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(xs + d.C);
+  float* xs = stage;
+  __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(stage + d.C);
+  float* red = stage + d.C + (CR + 1) / 2 + 3;
   const size_t count = (size_t)T * CR;
   const float* src = part + (size_t)t * CR;
   float sq = 0.f;
-  for (int k = lane; k < CR; k += 32) {
+  for (int k = threadIdx.x; k < CR; k += blockDim.x) {
     float acc = 0.f;
     for (int s = 0; s < splits; ++s) acc += src[(size_t)s * count + k];
     if (k < d.C) {
@@ -168,19 +169,24 @@ __global__ void __launch_bounds__(128) project_append_kernel(
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-  const float inv = 1.0f / sqrtf(sq / (float)d.C + eps);
-  __syncwarp();
-  for (int k = lane; k < d.C; k += 32) row[k] = __float2bfloat16_rn(xs[k] * inv * gain[k]);
-  __syncwarp();
+  if (lane == 0) red[warp] = sq;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)d.C + eps);
+  for (int k = threadIdx.x; k < d.C; k += blockDim.x) row[k] = __float2bfloat16_rn(xs[k] * inv * gain[k]);
+  __syncthreads();
+  if (warp != 0) return;
   const int p = pos[t];
   uint8_t* dst = entry_of(d, seq_idx[t], p, bt, batch, maxp, num_pages, pool, status, lane);
   if (!dst) return;
   write_entry<__nv_bfloat16, CACHE>(d, row, row + d.C, p, dst, rt, lane);
 }
 
-// Shared-memory bytes of project_append_kernel's 128-thread block.
+// Shared-memory bytes of project_append_kernel's block.
 inline size_t project_append_smem(const Dims& d) {
-  return 4 * sizeof(float) * ((size_t)d.C + (size_t)(d.C + d.R + 1) / 2 + 4);
+  return sizeof(float) * ((size_t)d.C + (size_t)(d.C + d.R + 1) / 2 + 3 + 8 + 4);
 }
 
 cudaError_t launch_append(const Dims& d, const void* c_kv, const void* k_r, const int32_t* seq_idx,
@@ -224,14 +230,13 @@ cudaError_t launch_project_append(const Dims& d, const void* h, int d_model, con
   RopeTable rt;
   fill_rope_table(&rt, d);
   const size_t smem = project_append_smem(d);
-  const int blocks = (T * 32 + 127) / 128;
   uint8_t* out = static_cast<uint8_t*>(pool);
   if (d.cache_dtype == MLA_FP8_E4M3)
-    e = launch_programmatic(project_append_kernel<MLA_FP8_E4M3>, dim3(blocks), dim3(128), smem, stream, d,
+    e = launch_programmatic(project_append_kernel<MLA_FP8_E4M3>, dim3(T), dim3(256), smem, stream, d,
                             (const float*)part, splits, gain, eps, seq_idx, pos, T, bt, batch, maxp,
                             num_pages, out, status, rt);
   else
-    e = launch_programmatic(project_append_kernel<MLA_BF16>, dim3(blocks), dim3(128), smem, stream, d,
+    e = launch_programmatic(project_append_kernel<MLA_BF16>, dim3(T), dim3(256), smem, stream, d,
                             (const float*)part, splits, gain, eps, seq_idx, pos, T, bt, batch, maxp,
                             num_pages, out, status, rt);
   return e == cudaSuccess ? cudaGetLastError() : e;

@@ -8,8 +8,9 @@
 // path forms K^C, V^C with the projection GEMM (bf16, [L][H d_h]), assembles Q = [q^C; RoPE(q^R)]
 // ([L][H][d_h + d_h^R]) and runs causal attention per head:
 //   one CTA per (head, 128 queries); 64-key blocks; S = Q K^T (M = 128 queries, N = 64 keys,
-//   K = 192) into one of two TMEM buffers; a softmax thread per query row (exact running
-//   maximum, O rescaled in TMEM when it rises); P (bf16) through shared memory;
+//   K = 192) into one of two TMEM buffers; a softmax thread per query row (a reference maximum
+//   that moves when a block's maximum exceeds it by more than 2^8, O rescaled in TMEM then);
+//   P (bf16) through shared memory;
 //   O += P V (M = 128, N = 128, K = 64) in TMEM; TMA loads of Q once, of K^C, k^R and V^C in
 //   3-stage rings. Warp 0 loads, warp 1 issues the MMAs, warps 2-5 run the softmax
 //   (TMEM lane quadrant = warp % 4). Every wait is bounded.
@@ -206,31 +207,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_empty[b]);
       const int k0 = j * kBK;
-      float mx = m;
+      float mx = -CUDART_INF_F;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const bool valid = k0 + c <= qi && k0 + c < p.L;
         s[c] = valid ? s[c] * p.scale_log2 : -CUDART_INF_F;
         mx = fmaxf(mx, s[c]);
       }
-      const float alpha = (m == -CUDART_INF_F) ? 0.f : ex2(m - mx);
-      m = mx;
+      // Lazy reference: the row keeps m while this block's maximum exceeds it by at most 8
+      // (log2 units; weights up to 2^8 are exact in bf16 and fp32), so most blocks need no
+      // rescale of O and need not wait for the previous P.V. A larger maximum moves m here,
+      // before any weight is formed, so no weight is ever clamped.
+      const bool move = mx > m + 8.f;
+      const float m_new = move ? mx : m;
+      const float alpha = move ? (m == -CUDART_INF_F ? 0.f : ex2(m - m_new)) : 1.f;
+      m = m_new;
       uint32_t pk[32];
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = mx == -CUDART_INF_F ? 0.f : ex2(s[2 * c] - mx);
-        const float p1 = mx == -CUDART_INF_F ? 0.f : ex2(s[2 * c + 1] - mx);
+        const float p0 = m == -CUDART_INF_F ? 0.f : ex2(s[2 * c] - m);
+        const float p1 = m == -CUDART_INF_F ? 0.f : ex2(s[2 * c + 1] - m);
         pk[c] = pack_bf16x2(p0, p1);
         sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
       }
       l = l * alpha + sum;
-      // O and the P buffer are free once P.V of the previous block has completed
-      if (j >= 1) ok = wait_bounded(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
+      // The P buffer of this block is free once P.V of block j - 2 is done; O may be rescaled
+      // only once P.V of block j - 1 is.
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, alpha != 1.f);
+      const int wj = rescale ? j - 1 : j - 2;
+      if (wj >= 0) ok = wait_bounded(&bars->pv_done[wj & 1], (wj >> 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < kD; c += 32) {
           float o[32];
@@ -277,33 +287,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-// Q[t][i] = [q^C[t][i] ; RoPE_t(q^R[t][i])] (bf16), one thread per (token, head, 8 columns).
+// Q[t][i] = [q^C[t][i] ; RoPE_t(q^R[t][i])] (bf16), one block per token: the token's cos/sin
+// pairs once in shared memory (they do not depend on the head), then one thread per
+// (head, 16 bytes) of the output row.
 __global__ void __launch_bounds__(256) prefill_q_kernel(const __nv_bfloat16* __restrict__ q_c,
                                                          const __nv_bfloat16* __restrict__ q_r, int L, int H,
                                                          __nv_bfloat16* __restrict__ q, const RopeTable rt) {
+  __shared__ float cs[kR / 2], sn[kR / 2];
   griddep_wait();
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;   // (t, h, unit of 8)
-  const int u = (int)(idx % (kDQ / 8));
-  const size_t th = idx / (kDQ / 8);
-  if (th >= (size_t)L * H) return;
-  const int t = (int)(th / H);
-  uint4* dst = reinterpret_cast<uint4*>(q + th * kDQ) + u;
-  if (u < kD / 8) {
-    *dst = reinterpret_cast<const uint4*>(q_c + th * kD)[u];
-    return;
-  }
-  const uint4 x = reinterpret_cast<const uint4*>(q_r + th * kR)[u - kD / 8];
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-  uint32_t o[4];
+  const int t = blockIdx.x;
+  if (threadIdx.x < kR / 2) rope_cs(t, rt.hi[threadIdx.x], rt.lo[threadIdx.x], &cs[threadIdx.x], &sn[threadIdx.x]);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < H * (kDQ / 8); idx += blockDim.x) {
+    const int h = idx / (kDQ / 8), u = idx % (kDQ / 8);
+    const size_t th = (size_t)t * H + h;
+    uint4* dst = reinterpret_cast<uint4*>(q + th * kDQ) + u;
+    if (u < kD / 8) {
+      *dst = reinterpret_cast<const uint4*>(q_c + th * kD)[u];
+      continue;
+    }
+    const uint4 x = reinterpret_cast<const uint4*>(q_r + th * kR)[u - kD / 8];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int k = (u - kD / 8) * 4 + e;   // RoPE pair
-    float c, s;
-    rope_cs(t, rt.hi[k], rt.lo[k], &c, &s);
-    const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
-    o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+    for (int e = 0; e < 4; ++e) {
+      const int k = (u - kD / 8) * 4 + e;   // RoPE pair
+      const float c = cs[k], s = sn[k];
+      const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
+      o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+    }
+    *dst = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  *dst = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace pf
@@ -333,12 +347,9 @@ cudaError_t launch_prefill(const Dims& d, const void* c_kv, const void* k_r, int
   if (e != cudaSuccess) return e;
   RopeTable rt;
   fill_rope_table(&rt, d);
-  {
-    const size_t n = (size_t)L * d.H * (pf::kDQ / 8);
-    e = launch_programmatic(pf::prefill_q_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream,
-                            (const __nv_bfloat16*)q_c, (const __nv_bfloat16*)q_r, L, d.H, q, rt);
-    if (e != cudaSuccess) return e;
-  }
+  e = launch_programmatic(pf::prefill_q_kernel, dim3((unsigned)L), dim3(256), 0, stream,
+                          (const __nv_bfloat16*)q_c, (const __nv_bfloat16*)q_r, L, d.H, q, rt);
+  if (e != cudaSuccess) return e;
   CUtensorMap tmQ, tmK, tmKR, tmV;
   {
     const uint64_t dims[3] = {(uint64_t)pf::kDQ, (uint64_t)d.H, (uint64_t)L};
