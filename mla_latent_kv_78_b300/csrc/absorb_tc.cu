@@ -85,12 +85,15 @@ __global__ void __launch_bounds__(128, 2)
   const uint32_t tmem = *slot;
   const int t = warp * 32 + lane;   // this thread's token (TMEM lane) in the tile
   griddep_launch_dependents();   // the decode may start its set-up while this grid finishes
-  if (threadIdx.x == 0) {
+  // the six boxes from six lanes of warp 0: a warp's TMA loads issued by separate
+  // instructions complete one after another on this part, those of one instruction overlap
+  if (warp == 0) {
     const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(&bars[0], 6 * 16384);
-    for (int kb = 0; kb < 2; ++kb) tma_load_3d(sA + kb * 16384, &tmQ, kb * 64, i, t0, &bars[0], pol);
-    for (int j = 0; j < 4; ++j)
-      tma_load_2d(sB + j * 16384, &tmW, (4 * half + j) * 64, i * kD, &bars[0], pol);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[0], 6 * 16384);
+    __syncwarp();
+    if (lane < 2) tma_load_3d(sA + lane * 16384, &tmQ, lane * 64, i, t0, &bars[0], pol);
+    else if (lane < 6)
+      tma_load_2d(sB + (lane - 2) * 16384, &tmW, (4 * half + lane - 2) * 64, i * kD, &bars[0], pol);
   }
   // the first half's CTA also rotates q^R while the operands land (a rolled loop: four
   // sin/cos pairs of code per iteration), straight into q_lat's last 64 columns
@@ -194,13 +197,17 @@ __global__ void __launch_bounds__(128, 1)
   // launched programmatically after the decode: the set-up above overlaps its tail, the inputs
   // are read only once it has completed
   griddep_wait();
-  if (threadIdx.x == 0) {
+  // slice j's two boxes from lane j of warp 0 (one instruction per box kind for all slices)
+  if (warp == 0) {
     const uint64_t pol = policy_evict_first();
-    for (int j = 0; j < 8; ++j) {
-      mbar_arrive_expect_tx(&bars[j], 16384 + 8192);
-      tma_load_2d(sA + j * 16384, &tmW, j * 64, i * kD, &bars[j], pol);
-      tma_load_3d(sB + j * 8192, &tmO, j * 64, i, t0, &bars[j], pol);
+    if (lane < 8) {
+      mbar_arrive_expect_tx(&bars[lane], 16384 + 8192);
+      tma_load_2d(sA + lane * 16384, &tmW, lane * 64, i * kD, &bars[lane], pol);
+      tma_load_3d(sB + lane * 8192, &tmO, lane * 64, i, t0, &bars[lane], pol);
     }
+    __syncwarp();
+  }
+  if (threadIdx.x == 0) {
     const uint32_t id = idesc_bf16_f32(128, kUnNT, 0, 0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
     for (int j = 0; j < 8; ++j) {

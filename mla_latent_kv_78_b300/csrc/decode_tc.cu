@@ -13,7 +13,7 @@
 //    tokens' 576-d keys and HALF of Q (its 64 heads), and every MMA runs at full rate
 //    (N = 128). With a bf16 cache the Q half is not resident: each [128 tokens x 64 dims]
 //    key chunk is staged together with the matching [64 heads x 64 dims] Q chunk (an L2
-//    hit after the first tile), which leaves shared memory for a 4-deep key ring, a 3-deep
+//    hit after the first tile), which leaves shared memory for a 3-deep key ring, a 4-deep
 //    latent ring and two P^T buffers.
 //  * The output is accumulated transposed, O^T[d_c][head] = V^T . P^T, again 2-SM
 //    (M = 256 latent rows per MMA, two MMAs per K step): each CTA holds half of O^T,
@@ -95,8 +95,8 @@ struct Lay {
   // FP8: Q stays resident.
   static constexpr bool QRES = F8;
   static constexpr int SSTAGE = QRES ? 16384 : 16384 + 8192;   // S-phase stage bytes
-  static constexpr int NS = F8 ? 2 : 4;     // S-phase ring
-  static constexpr int NV = F8 ? 2 : 3;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
+  static constexpr int NS = F8 ? 2 : 3;     // S-phase ring
+  static constexpr int NV = F8 ? 2 : 4;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
   static constexpr int PB = F8 ? 1 : 2;     // P^T buffers [256 tok x 64 heads] = 32 KB each
   static constexpr int RS = F8 ? 3 : 0;     // raw key-chunk slots (kRawS bytes)
   static constexpr int RV = F8 ? 2 : 0;     // raw latent-chunk slots (kRawV bytes)

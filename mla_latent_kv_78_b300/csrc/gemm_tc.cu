@@ -23,6 +23,7 @@ using namespace ptx;
 constexpr int kBM = 128;       // rows of W per CTA
 constexpr int kBK = 64;        // K per stage: one 128-byte swizzle atom of bf16
 constexpr int kStages = 6;
+constexpr int kGroup = 3;   // stages refilled per producer step (kStages is a multiple)
 constexpr long long kTimeout = 4000000000LL;
 
 template <int BN>
@@ -89,27 +90,25 @@ __global__ void __launch_bounds__(128, 1)
   griddep_wait();
   bool ok = true;
   if (warp == 0) {
-    // ---- producer: a stage's two boxes come from two lanes (TMA loads issued by one thread
-    // complete one after another), rotating over the warp
+    // ---- producer: stages are refilled kGroup at a time, stage g * kGroup + j by lane j, so
+    // one instruction issues kGroup boxes (a warp's TMA loads issued by separate instructions
+    // complete one after another on this part; the boxes of one instruction overlap)
     const uint64_t pol_w = policy_evict_first();   // weights are read once
     const uint64_t pol_x = policy_evict_last();    // activations are shared by the row tiles
-    for (int ks = 0; ks < nk && ok; ++ks) {
+    for (int g = 0; g * kGroup < nk && ok; ++g) {
+      const int ks = g * kGroup + lane;
+      const bool mine = lane < kGroup && ks < nk;
       const int st = ks % kStages;
-      const int q = lane - 2 * (ks & 15);
       bool r = true;
-      if (q == 0 || q == 1) {
-        if (ks >= kStages) r = wait_bounded(&freeb[st], ((ks / kStages) - 1) & 1, p.status);
-        if (r) {
-          uint8_t* dst = sm + st * Ly::STAGE;
-          if (q == 0) {
-            mbar_arrive_expect_tx(&full[st], Ly::STAGE);
-            tma_load_2d(dst, &tmW, k0 + ks * kBK, n0, &full[st], pol_w);
-          } else {
-            tma_load_2d(dst + Ly::A, &tmX, k0 + ks * kBK, t0, &full[st], pol_x);
-          }
-        }
-      }
+      if (mine && ks >= kStages) r = wait_bounded(&freeb[st], ((ks / kStages) - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, r);
+      if (!ok) break;
+      if (mine) {
+        uint8_t* dst = sm + st * Ly::STAGE;
+        mbar_arrive_expect_tx(&full[st], Ly::STAGE);
+        tma_load_2d(dst, &tmW, k0 + ks * kBK, n0, &full[st], pol_w);
+        tma_load_2d(dst + Ly::A, &tmX, k0 + ks * kBK, t0, &full[st], pol_x);
+      }
     }
   } else if (warp == 1) {
     // ---- MMA issuer: D[row][token] += W[row][k] . X[token][k]
