@@ -95,28 +95,35 @@ __global__ void __launch_bounds__(128, 2)
     else if (lane < 6)
       tma_load_2d(sB + (lane - 2) * 16384, &tmW, (4 * half + lane - 2) * 64, i * kD, &bars[0], pol);
   }
-  // the first half's CTA also rotates q^R while the operands land (a rolled loop: four
-  // sin/cos pairs of code per iteration), straight into q_lat's last 64 columns
+  // the first half's CTA also rotates q^R while the operands land: two threads per token,
+  // 16 RoPE pairs each, all four 16-byte loads issued before any is used
   const uint32_t rsw = (uint32_t)(t & 7);
-  if (half == 0 && t < nt) {
-    const size_t row = (size_t)(t0 + t) * p.H + i;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q_r + row * kR);
-    uint4* dst = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + kC);
-    const int pos = p.pos[t0 + t];
-#pragma unroll 1
-    for (int q = 0; q < kR / 8; ++q) {
-      const uint4 x = src[q];
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-      uint32_t o[4];
+  if (half == 0) {
+    const int tt = threadIdx.x >> 1, part = threadIdx.x & 1;
+    for (int tb = 0; tb < kAbsNT; tb += 64) {
+      const int tok = tb + tt;
+      if (tok >= nt) break;
+      const size_t row = (size_t)(t0 + tok) * p.H + i;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_r + row * kR) + part * 4;
+      uint4* dst = reinterpret_cast<uint4*>(p.q_lat + row * (kC + kR) + kC) + part * 4;
+      const int pos = p.pos[t0 + tok];
+      uint4 x[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k = q * 4 + e;
-        float c, s;
-        rope_cs(pos, p.theta_hi[k], p.theta_lo[k], &c, &s);
-        const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
-        o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+      for (int q = 0; q < 4; ++q) x[q] = src[q];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = (part * 4 + q) * 4 + e;
+          float c, s;
+          rope_cs(pos, p.theta_hi[k], p.theta_lo[k], &c, &s);
+          const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xFFFF0000u);
+          o[e] = pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+        }
+        dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
   if (threadIdx.x == 0) {
