@@ -67,3 +67,17 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
                                 16, None, None, None)
     assert rc == L.MLA_ERR_SCRATCH_LIMIT
     assert "scratch" in M.mla_status_string(rc)
+
+
+@needs_cuda
+def test_noalloc_at_the_edge_of_its_scratch():
+    """Sizes whose split-KV partials fill the fixed scratch to within 10 % of its size: the
+    no-alloc call accepts them and matches mla_decode on the same inputs bit for bit (same
+    kernels, same split), so the scratch is usable up to its end."""
+    wl = W.small_v2(8, [4096] * 8, n_q=1, cache="bf16", seed=24)
+    cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act)
+    splits = 15   # fp32 partials: 8 x 128 heads x 15 x 513 x 4 B = 31.5 MB of 32 MiB
+    need = M.mla_decode_workspace_size(cfg, wl.B, wl.n_q, max(wl.seq_lens), splits)
+    assert 0.9 * L.NOALLOC_SCRATCH_BYTES < need <= L.NOALLOC_SCRATCH_BYTES
+    ref_o, ref_lse, o, lse = _both(wl, M.MLA_KERNEL_AUTO, splits)
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
