@@ -62,6 +62,14 @@ design notes):
    pages); k^R = W^{KR} h is not normalised. The projected c^{KV} and k^R are stored in
    the activation type before they are cached, as when the projection and the cache
    write are separate calls.
+8. FP8 scores ([v3-notes] F8量化策略: E4M3 operands with 1x128 activation groups, partial
+   sums promoted to fp32 every 128 products). Reading for the decode's scores over an FP8
+   cache: q_lat's latent part (its first d_c dims) is quantised per (query row, head) in
+   1x128 groups exactly as the cache's c_KV is (reading 4); each group's product of codes is
+   scaled by the two groups' scales and summed in fp32, and the bf16 RoPE part is added as
+   in the bf16 path. The exact value of that sum is q8 . [c; k^R] with q8 = q_lat whose
+   latent part is replaced by code * scale, which is what ``quantize_q_latent`` returns; the
+   softmax and P . V are unchanged.
 
 Parity status: every function here is pinned by tests/test_oracle.py
 (closed forms, special cases, brute force in 50-digit decimal arithmetic,
@@ -228,6 +236,21 @@ def dequantize_fp8_groups(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     n, C = codes.shape
     v = e4m3_decode(codes).reshape(n, C // FP8_GROUP, FP8_GROUP)
     return (v * np.asarray(scales, dtype=np.float64)[..., None]).reshape(n, C)
+
+
+def quantize_q_latent(q_lat: np.ndarray, C: int):
+    """The query side of FP8 scores (reading 8): q_lat [..., C + R] with its latent part
+    (first C dims) quantised per (row, head) in 1x128 groups like the cache (reading 4).
+
+    Returns (q8 [..., C + R] fp64 with the latent part replaced by code * scale and the RoPE
+    part unchanged, codes uint8 [..., C], scales fp32 [..., C / 128]).
+    """
+    q = np.asarray(q_lat, dtype=np.float64)
+    lead = q.shape[:-1]
+    codes, scales = quantize_fp8_groups(q[..., :C].reshape(-1, C))
+    q8 = q.copy()
+    q8[..., :C] = dequantize_fp8_groups(codes, scales).reshape(lead + (C,))
+    return q8, codes.reshape(lead + (C,)), scales.reshape(lead + (C // FP8_GROUP,))
 
 
 # --------------------------------------------------------------------------

@@ -356,6 +356,50 @@ def test_fp8_group_quantiser():
     assert rel.max() <= 2.0 ** -4 + 1e-7
 
 
+def test_query_quantiser_against_torch_codec():
+    """FP8 scores (reading 8): q_lat's latent part is quantised per (row, head) in 1x128
+    groups. The codes equal torch's independent float -> float8_e4m3fn conversion of the
+    fp32 quotient by the group scale, the scale is the group's amax / 448 in fp32, and the
+    RoPE part passes through untouched."""
+    torch = pytest.importorskip("torch")
+    g = _rng(12)
+    q = g.standard_normal((3, 5, 576)).astype(np.float32) * np.float32(0.15)
+    q[1, 2, 256:384] = 0.0            # an all-zero group: scale 1, codes 0
+    q8, codes, scales = O.quantize_q_latent(q, 512)
+    assert codes.shape == (3, 5, 512) and scales.shape == (3, 5, 4)
+    grp = q[..., :512].reshape(3, 5, 4, 128)
+    amax = np.abs(grp).max(-1)
+    np.testing.assert_array_equal(scales, np.where(amax > 0, amax / np.float32(448.0), 1.0).astype(np.float32))
+    quot = (grp / scales[..., None]).astype(np.float32)
+    ref = torch.from_numpy(np.ascontiguousarray(quot)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, ref.reshape(3, 5, 512))
+    np.testing.assert_array_equal(q8[..., 512:], q[..., 512:].astype(np.float64))
+    back = torch.from_numpy(ref).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(q8[..., :512], (back * scales[..., None]).reshape(3, 5, 512))
+
+
+def test_query_quantiser_is_exact_on_representable_groups():
+    """A group whose values are E4M3 values times a power of two, with its largest magnitude
+    at 448 times that power, quantises without error (scale = the power of two exactly), so
+    the FP8 scores equal the exact scores; a general group moves by at most half an E4M3
+    step (2^-4 relative) per element."""
+    vals = O.e4m3_values()
+    fin = vals[np.isfinite(vals) & (np.abs(vals) <= 448)]
+    g = _rng(13)
+    grp = g.choice(fin, size=(2, 128))
+    grp[:, 0] = 448.0
+    grp *= np.array([[2.0 ** -5], [2.0 ** 3]])
+    q = np.zeros((2, 576))
+    q[:, :128] = grp
+    q[:, 128:512] = g.standard_normal((2, 384))
+    q8, _, scales = O.quantize_q_latent(q, 512)
+    assert scales[0, 0] == 2.0 ** -5 and scales[1, 0] == 2.0 ** 3
+    np.testing.assert_array_equal(q8[:, :128], grp)
+    rel = np.abs(q8[:, 128:512] - q[:, 128:512]) / np.abs(q[:, 128:512])
+    big = np.abs(q[:, 128:512]) >= np.repeat(scales[:, 1:], 128, axis=1) * 2.0 ** -6
+    assert rel[big].max() <= 2.0 ** -4 + 1e-7
+
+
 # ---------------------------------------------------------------- page / slot mapping
 def test_page_slot_mapping():
     bt = np.array([[5, 2, -1], [0, 4, 1]], dtype=np.int32)
