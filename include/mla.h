@@ -80,6 +80,16 @@ extern "C" {
                                reference by more than 2^96 is computed again with the
                                exact per-head maxima as the reference. Non-finite inputs
                                give non-finite outputs. */
+#define MLA_KERNEL_TC_FP8_SCORES 3  /* the tensor-core kernel over an FP8 cache with the
+                               scores on FP8 tensor cores (「Deepseek系列从v3到R易背面经版」
+                               F8量化策略): in the kernel q_lat's latent part is quantised
+                               per (query row, head) in 1x128 groups to E4M3 exactly as the
+                               cache's latents are (scale = amax/448 in fp32), each group's
+                               code product (tcgen05 kind::f8f6f4, fp32 accumulation) is
+                               scaled by the two group scales and summed in fp32, and the
+                               bf16 RoPE part is added. Softmax and P.V as MLA_KERNEL_TC.
+                               FP8 cache, same shapes as MLA_KERNEL_TC; else
+                               MLA_ERR_UNSUPPORTED. */
 
 typedef struct mla_config {
   int32_t n_heads;      /* H  = n_h                                               */

@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     MLA_KERNEL_AUTO,
     MLA_KERNEL_SIMT,
     MLA_KERNEL_TC,
+    MLA_KERNEL_TC_FP8_SCORES,
     MlaError,
     lib,
     make_config,

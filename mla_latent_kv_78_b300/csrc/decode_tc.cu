@@ -75,7 +75,8 @@ constexpr int F_LLOC = F_ALPHA + 128;  // [128]
 constexpr int F_LRCV = F_LLOC + 128;   // [128]
 constexpr int F_INV = F_LRCV + 128;    // [128]
 constexpr int F_X0 = F_INV + 128;     // [128] the peer's tile-0 per-head maxima
-constexpr int F_FLAG = F_X0 + 128;    // ints, see FL_*
+constexpr int F_SQ = F_X0 + 128;     // [128 heads][4] FP8 scores: query group scales (both CTAs')
+constexpr int F_FLAG = F_SQ + 4 * kH;    // ints, see FL_*
 constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for this tile
 constexpr int FL_ABORT = 2;    // a bounded wait gave up
 constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
@@ -123,6 +124,9 @@ struct BarsT {
   uint64_t rs_ready[RS], rs_free[RS], rv_ready[RV], rv_free[RV];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_landed[2], p_ready[2], o_done[2];
+  uint64_t gs_ready[2], gs_free[2];   // FP8 scores: latent code groups (even CTA / both)
+  uint64_t q8_done;      // FP8 scores: Q quantised (the group ring may overwrite its bf16 rows)
+  uint64_t sq_ready;     // FP8 scores: the peer's query group scales have landed
   uint64_t x0_ready;     // the peer's tile-0 maxima have landed
   uint64_t l_landed;
   uint64_t teardown;
@@ -143,12 +147,16 @@ struct Maps {
   CUtensorMap ss;    // box 16 B x 64 rows (the 4 scales of a token)
   CUtensorMap sv;    // box 16 B x 32 rows
   CUtensorMap kr;    // box 128 B x 64 rows (bf16 RoPE keys)
+  CUtensorMap c8;    // box 128 B x 64 rows, 128-byte swizzle: one latent group's codes as an
+                     // FP8 MMA operand (FP8 scores)
 };
 
 struct Params {
   long long wait_limit;   // clock cycles a bounded wait gives up after
   int withhold;           // test hook: latent chunk the even CTA never loads (-1: none)
   const int32_t* bt;
+  const uint8_t* pool;     // FP8 scores: the key scales are read from the entries
+  int q8;                  // FP8 scores (MLA_KERNEL_TC_FP8_SCORES)
   int maxp, num_pages;
   const int32_t* seq_lens;
   int B, n_q, max_seq_len, S;
@@ -297,6 +305,12 @@ __device__ __forceinline__ void init_barriers(BarsT<F8>* bars) {
       mbar_init(&bars->p_ready[s], 2);
       mbar_init(&bars->o_done[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->gs_ready[s], 1);
+      mbar_init(&bars->gs_free[s], 1);
+    }
+    mbar_init(&bars->q8_done, 1);
+    mbar_init(&bars->sq_ready, 1);
     mbar_init(&bars->x0_ready, 1);
     mbar_init(&bars->l_landed, 1);
     mbar_init(&bars->teardown, 2);   // both issuing threads' last commits
@@ -306,7 +320,8 @@ __device__ __forceinline__ void init_barriers(BarsT<F8>* bars) {
 // One pass over this pair's unit. mode 0 is the ordinary pass; modes 1 and 2 run only when
 // mode 0 had to clamp a weight (see kRange): 1 computes the scores alone, for the exact
 // per-head maxima, 2 is the ordinary pass with those maxima as the reference.
-template <bool F8>
+// Q8: the FP8 cache with the scores on FP8 tensor cores (MLA_KERNEL_TC_FP8_SCORES).
+template <bool F8, bool Q8 = false>
 __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm, uint8_t* sm, const int mode) {
   using Ly = Lay<F8>;
   using Bars = BarsT<F8>;
@@ -467,12 +482,37 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       ++m_cnt;
       return __all_sync(0xffffffffu, r);
     };
+    // FP8 scores: one latent group's codes of this CTA's 128 tokens (two pages), the MMA's A
+    // operand as loaded, into a 2-slot ring over the bf16 Q rows 4-7 (free once Q is
+    // quantised); both boxes from one instruction, both CTAs' bytes on the even CTA's barrier
+    int g_cnt = 0;
+    auto load_group = [&](int g, int y0, int y1) -> bool {   // whole warp
+      const int st = g_cnt & 1;
+      bool r = true;
+      if (leader && g_cnt >= 2) r = wait_bar(&bars->gs_free[st], ((g_cnt >> 1) - 1) & 1, cx);
+      if (!__shfl_sync(0xffffffffu, r, 0)) return false;
+      if (leader && even) mbar_arrive_expect_tx(&bars->gs_ready[st], 2 * 16384);
+      __syncwarp();
+      if (lane < 2)
+        tma_load_2d_pair(sm + OFF_Q + 32768 + st * 16384 + lane * 8192, &maps.c8, g * 128, lane ? y1 : y0,
+                         at_even(&bars->gs_ready[st]), pol_s);
+      ++g_cnt;
+      return true;
+    };
     // key chunks of every tile in order (the latent chunks have their own producer)
     bool ok = true;
+    if (F8 && Q8) {
+      if (leader) ok = wait_bar(&bars->q8_done, 0, cx);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
     for (int k = 0; k < nt && ok; ++k) {
       const int ys0 = page_y(4 * k + 2 * (int)rank);
       const int ys1 = page_y(4 * k + 2 * (int)rank + 1);
-      if constexpr (F8) {
+      if (F8 && Q8) {
+        for (int g = 0; g < 4 && ok; ++g) ok = load_group(g, ys0, ys1);
+        if (ok) ok = load_raw_s(true, 0, ys0, 0);
+        if (ok) ok = load_raw_s(true, 0, ys1, 0);
+      } else if constexpr (F8) {
         for (int c = 0; c < kKCh + 1 && ok; ++c) {   // 8 latent chunks, 2 RoPE half chunks
           ok = c < 8 ? load_raw_s(false, c, ys0, ys1) : load_raw_s(true, 0, c == 8 ? ys0 : ys1, 0);
         }
@@ -517,6 +557,53 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
 #endif
       // bf16: Q travels with the key chunks; FP8: both CTAs' resident Q halves have landed
       bool ok = F8 ? wait_bar<true>(&bars->q_conv, 0, cx) : true;
+      if (F8 && Q8) {
+        // FP8 scores: per tile five partial products, one per TMEM buffer use (partial n of
+        // the unit in buffer n % 2): the four latent groups on FP8 tensor cores (codes of the
+        // CTA's tokens . codes of its Q half, K = 128) and the bf16 RoPE part. The softmax
+        // warps promote them to fp32 with the group scales; the fifth lands in buffer t % 2.
+        const uint32_t id8 = idesc_e4m3_f32(256, 128);
+        const uint64_t dG = smem_desc(smem_u32(sm + OFF_Q + 32768), 16, 1024, kSw128);
+        const uint64_t dQ8 = smem_desc(smem_u32(sm + OFF_Q), 16, 1024, kSw128);
+        uint32_t g_st = 0, g_ph = 0;
+        int n = 0;
+        for (int t = 0; t < nt && ok; ++t) {
+          for (int p = 0; p < 5 && ok; ++p, ++n) {
+            const int b = n & 1, u = n >> 1;
+            if (u >= 1) ok = wait_bar(&bars->s_empty[b], (u - 1) & 1, cx);
+            if (!ok) break;
+            const uint32_t d = tmem + (uint32_t)b * 128u;
+            if (p < 4) {
+              ok = wait_bar<true>(&bars->gs_ready[g_st], g_ph, cx);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t a0 = dG + g_st * (16384u >> 4), b0 = dQ8 + (uint32_t)p * (8192u >> 4);
+              mma_e4m3_pair(d, a0, b0, id8, 0);
+              mma_e4m3_pair(d, a0 + 2, b0 + 2, id8, 1);
+              mma_e4m3_pair(d, a0 + 4, b0 + 4, id8, 1);
+              mma_e4m3_pair(d, a0 + 6, b0 + 6, id8, 1);
+              mma_commit_pair(&bars->gs_free[g_st], 0x3);
+              if (++g_st == 2) {
+                g_st = 0;
+                g_ph ^= 1u;
+              }
+            } else {
+              // the RoPE keys, converted into operand slot t % kNS by the converter warps
+              const int st = t % kNS;
+              ok = wait_bar<true>(&bars->s_ready[st], (t / kNS) & 1, cx);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t a0 = dS + (uint32_t)st * (uint32_t)(kSStage >> 4), b0 = dQ + 8u * 512u;
+              mma_bf16_pair(d, a0, b0, idS, 0);
+              mma_bf16_pair(d, a0 + 2, b0 + 2, idS, 1);
+              mma_bf16_pair(d, a0 + 4, b0 + 4, idS, 1);
+              mma_bf16_pair(d, a0 + 6, b0 + 6, idS, 1);
+              mma_commit_pair(&bars->s_free[st], 0x3);
+            }
+            mma_commit_pair(&bars->s_full[b], 0x3);
+          }
+        }
+      } else
       for (int t = 0; t < nt && ok; ++t) {
         TRACE(22, t);
         // TMEM buffer t % 2 is free once the softmax has read S^T(t-2)
@@ -762,8 +849,9 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       bool ok = true;
       if (ct == 0) ok = wait_bar(&bars->q_ready, 0, cx);
       ok = bar_and(10, 96, ok);
-      // Q needs no conversion (bf16 already): report this CTA's half as landed
-      if (ok && ct == 0) arrive_even(&bars->q_conv, rank);
+      // Q needs no conversion (bf16 already): report this CTA's half as landed (with FP8
+      // scores the softmax warps quantise Q and report it)
+      if (ok && ct == 0 && !Q8) arrive_even(&bars->q_conv, rank);
       // lane 0: wait until job J is next to acquire its slots
       volatile int* ticket = &flags[FL_TICKET];
       auto my_turn = [&](int J) -> bool {
@@ -783,9 +871,11 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         *ticket = J + 1;
       };
       // Key chunk job n (tile n / 9, chunk n % 9), raw key chunks m .. m (+1 for the RoPE keys).
+      // (FP8 scores: job n is tile n's RoPE keys alone, raw chunks 2n and 2n + 1; the latent
+      // groups go to the tensor cores as loaded)
       auto key_job = [&](int J, int n) -> bool {
-        const int c = n % kKCh;
-        const int m = (n / kKCh) * (kKCh + 1) + c;   // 10 raw key chunks per tile
+        const int c = Q8 ? kKCh - 1 : n % kKCh;
+        const int m = Q8 ? 2 * n : (n / kKCh) * (kKCh + 1) + c;   // 10 raw key chunks per tile
         const int st = n % kNS;
         uint8_t* dst = sm + OFF_S + st * kSStage;
         bool r = true;
@@ -844,7 +934,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         if (lane == 0) arrive_even(&bars->s_ready[st], rank);
         return true;
       };
-      for (int n = cw; n < nt * kKCh && ok; n += 3) ok = key_job(n, n);
+      for (int n = cw; n < (Q8 ? nt : nt * kKCh) && ok; n += 3) ok = key_job(n, n);
 #ifdef MLA_TC_TRACE
       prof[7] = clock64() - prof_start;
       if (lane == 0) PROF_STORE(544 + 8 * cw);
@@ -893,7 +983,141 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
     const long long prof_start = clock64();
 #endif
     bool ok = true;
-    if (mode == 1) {
+    // ---- FP8 scores (「Deepseek系列从v3到R易背面经版」 F8量化策略: E4M3 with 1x128 activation
+    // groups, partial sums promoted to fp32 every 128 products). This CTA's Q half is quantised
+    // per (head, 128-dim group) as the cache's latents are: thread = (head hq, group gq); the
+    // codes replace bf16 rows 0-3 of the resident Q in the FP8 operand layout (128-byte rows,
+    // 128-byte swizzle) and the scale goes to both CTAs' F_SQ. Every pass does it, as every
+    // pass loads Q again.
+    float skv[4] = {0.f, 0.f, 0.f, 0.f}, skn[4] = {0.f, 0.f, 0.f, 0.f};
+    // the four key group scales of this thread's token of tile t (0 past the range)
+    auto key_scales = [&](int t, float* out) {
+      const int tok = lo + t * kTile + (int)rank * 128 + i;
+      out[0] = out[1] = out[2] = out[3] = 0.f;
+      if (tok < hi) {
+        const int pg = __ldg(prm.bt + (size_t)b * prm.maxp + tok / kP);
+        if (pg >= 0 && pg < prm.num_pages) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(
+              prm.pool + ((size_t)pg * kP + (size_t)(tok % kP)) * (size_t)(kC + 2 * kR + 16) + kC + 2 * kR));
+          out[0] = v.x;
+          out[1] = v.y;
+          out[2] = v.z;
+          out[3] = v.w;
+        }
+      }
+    };
+    if (F8 && Q8) {
+      bool okq = true;
+      if (stid == 0) okq = wait_bar(&bars->q_ready, 0, cx);
+      okq = bar_and(1, 256, okq);
+      const int hq = stid >> 2, gq = stid & 3;
+      const uint32_t swq = (uint32_t)(hq & 7);
+      uint4 cw8[8];
+      float sq = 1.f;
+      if (okq) {
+        // group gq = bf16 rows 2gq and 2gq + 1 of head hq; logical 16-byte unit u of a row is at
+        // u ^ (hq & 7)
+        float amax = 0.f;
+#pragma unroll
+        for (int uu = 0; uu < 16; ++uu) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sm + OFF_Q + (2 * gq + (uu >> 3)) * 8192 + hq * 128 +
+                                                          ((((uint32_t)uu & 7u) ^ swq) << 4));
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            amax = fmaxf(amax, fmaxf(fabsf(p16_to_f32(w[e] & 0xFFFFu)), fabsf(p16_to_f32(w[e] >> 16))));
+        }
+        sq = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 1.f;
+        // code unit cu (codes 16cu .. 16cu + 15) comes from bf16 units 2cu, 2cu + 1 of the group
+#pragma unroll
+        for (int cu = 0; cu < 8; ++cu) {
+          uint32_t c4[4];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int uu = 2 * cu + k;
+            const uint4 x = *reinterpret_cast<const uint4*>(sm + OFF_Q + (2 * gq + (uu >> 3)) * 8192 + hq * 128 +
+                                                            ((((uint32_t)uu & 7u) ^ swq) << 4));
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t a = w[2 * e], bb = w[2 * e + 1];
+              c4[2 * k + e] = (uint32_t)e4m3_encode(__fdiv_rn(p16_to_f32(a & 0xFFFFu), sq)) |
+                              ((uint32_t)e4m3_encode(__fdiv_rn(p16_to_f32(a >> 16), sq)) << 8) |
+                              ((uint32_t)e4m3_encode(__fdiv_rn(p16_to_f32(bb & 0xFFFFu), sq)) << 16) |
+                              ((uint32_t)e4m3_encode(__fdiv_rn(p16_to_f32(bb >> 16), sq)) << 24);
+            }
+          }
+          cw8[cu] = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+        }
+      }
+      bar_sync(2, 256);   // every bf16 row has been read before any is overwritten
+      if (okq) {
+        uint8_t* dst = sm + OFF_Q + gq * 8192 + hq * 128;
+#pragma unroll
+        for (int cu = 0; cu < 8; ++cu) *reinterpret_cast<uint4*>(dst + ((((uint32_t)cu) ^ swq) << 4)) = cw8[cu];
+        const int hh = (int)rank * 64 + hq;
+        fs[F_SQ + hh * 4 + gq] = sq;
+        st_async_b32(mapa(smem_u32(fs + F_SQ + hh * 4 + gq), peer), __float_as_uint(sq),
+                     mapa(smem_u32(&bars->sq_ready), peer));
+        fence_proxy_async_smem();
+      }
+      bar_sync(3, 256);   // all codes written and fenced for the tensor core
+      bool okx = okq;
+      if (stid == 0 && okq) {
+        mbar_arrive(&bars->q8_done);          // the group ring may overwrite bf16 rows 4-7
+        arrive_even(&bars->q_conv, rank);     // this CTA's Q half is ready for the MMAs
+        mbar_arrive_expect_tx(&bars->sq_ready, 64 * 4 * 4);
+        okx = wait_bar<true>(&bars->sq_ready, 0, cx);
+      }
+      ok = bar_and(4, 256, okx);
+      key_scales(0, skn);
+    }
+    // the five partial products of tile t promoted to fp32 (x key scale x query scale per
+    // latent group, x 1 for the RoPE part), written into buffer par for the softmax below
+    auto promote = [&](int t, int par) -> bool {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) skv[k] = skn[k];
+      if (t + 1 < nt) key_scales(t + 1, skn);
+      float acc[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+#pragma unroll 1
+      for (int p = 0; p < 5; ++p) {
+        const int n = 5 * t + p, bb = n & 1, u = n >> 1;
+        bool okp = true;
+        if (stid == 0) okp = wait_bar(&bars->s_full[bb], (uint32_t)(u & 1), cx);
+        if (!bar_and(1, 256, okp)) return false;
+        tc_fence_after();
+        const float f = p == 0 ? skv[0] : p == 1 ? skv[1] : p == 2 ? skv[2] : p == 3 ? skv[3] : 1.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float x[32];
+          tmem_ld32(lane_addr + (uint32_t)bb * 128u + 64 * g + 32 * h2, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float qs = p < 4 ? fs[F_SQ + (64 * g + 32 * h2 + c) * 4 + p] : 1.f;
+            acc[32 * h2 + c] = fmaf(f * qs, x[c], acc[32 * h2 + c]);
+          }
+        }
+        if (p < 4) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0)
+              mbar_arrive(&bars->s_empty[bb]);
+            else
+              mbar_arrive_remote_relaxed(mapa(smem_u32(&bars->s_empty[bb]), 0));
+          }
+        }
+      }
+      tmem_st32(lane_addr + (uint32_t)par * 128u + 64 * g, acc);
+      tmem_st32(lane_addr + (uint32_t)par * 128u + 64 * g + 32, acc + 32);
+      tmem_st_wait();
+      return true;
+    };
+    if (!ok) {
+    } else if (mode == 1) {
       // ---- scores only: the exact per-head maxima of this range. Lane j of each warp keeps
       // the running maxima of heads 64g + j and 64g + 32 + j over the warp's tokens; the
       // warps, then the two CTAs, combine them into F_M, which the next pass uses as its
@@ -902,7 +1126,10 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       for (int t = 0; t < nt; ++t) {
         const int par = t & 1;
         bool ok1 = true;
-        if (stid == 0) ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
+        if (F8 && Q8)
+          ok1 = promote(t, par);
+        else if (stid == 0)
+          ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
         ok = bar_and(1, 256, ok1);
         if (!ok) break;
         tc_fence_after();
@@ -976,7 +1203,10 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         }
         fs[F_ALPHA + h] = alpha;
       }
-      if (stid == 0) ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
+      if (F8 && Q8)
+        ok1 = promote(t, par);
+      else if (stid == 0)
+        ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
       ok = bar_and(1, 256, ok1);
       if (!ok) break;
       if (stid == 0) TRACE(3, t);
@@ -1331,9 +1561,9 @@ __device__ __forceinline__ bool end_of_pass(int mode, uint8_t* sm) {
 
 // The same pass as an out-of-line function (the FP8 cache's passes run through it: measured
 // faster there than the pass inlined into the kernel).
-template <bool F8>
+template <bool F8, bool Q8 = false>
 __device__ __noinline__ void decode_pass_ool(const Maps& maps, const Params& prm, uint8_t* sm, int mode) {
-  decode_pass<F8>(maps, prm, sm, mode);
+  decode_pass<F8, Q8>(maps, prm, sm, mode);
 }
 
 // The two extra passes of a unit whose first pass clamped a weight, out of line so that the
@@ -1400,7 +1630,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   // weight is at most 1 and none is clamped).
   if constexpr (F8) {
     for (int mode = 0; mode < 3; ++mode) {
-      decode_pass_ool<F8>(maps, prm, sm, mode);
+      if (prm.q8)
+        decode_pass_ool<F8, true>(maps, prm, sm, mode);
+      else
+        decode_pass_ool<F8, false>(maps, prm, sm, mode);
       if (!end_of_pass<F8>(mode, sm)) break;
     }
   } else {
@@ -1447,7 +1680,7 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
 
 // 2-D byte map over the FP8 pool, rows of `entry` bytes, box_bytes x box_rows boxes, no swizzle.
 static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t entry,
-                        uint32_t box_bytes, uint32_t box_rows) {
+                        uint32_t box_bytes, uint32_t box_rows, bool swizzle128 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)entry, rows};
@@ -1455,7 +1688,7 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_
   cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1515,7 +1748,8 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
         !tc::make_map_u8(&maps.cv, pool, prow, eb, 64, 32) ||
         !tc::make_map_u8(&maps.ss, pool, prow, eb, 16, 64) ||
         !tc::make_map_u8(&maps.sv, pool, prow, eb, 16, 32) ||
-        !tc::make_map_u8(&maps.kr, pool, prow, eb, 128, 64))
+        !tc::make_map_u8(&maps.kr, pool, prow, eb, 128, 64) ||
+        (d.fp8_scores && !tc::make_map_u8(&maps.c8, pool, prow, eb, 128, 64, true)))
       return cudaErrorInvalidValue;
   } else {
     if (!tc::make_map(&maps.k, pool, prow, 64)) return cudaErrorInvalidValue;
@@ -1535,6 +1769,8 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.wait_limit = lim > 0 ? lim : tc::kTimeout;
   prm.withhold = tc::g_withhold.load();
   prm.bt = bt;
+  prm.pool = static_cast<const uint8_t*>(pool);
+  prm.q8 = d.fp8_scores ? 1 : 0;
   prm.maxp = maxp;
   prm.num_pages = num_pages;
   prm.seq_lens = seq_lens;

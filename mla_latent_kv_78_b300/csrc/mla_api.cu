@@ -30,7 +30,7 @@ int make_dims(const mla_config* c, Dims* d) {
   if (c->act_dtype != MLA_F32 && c->act_dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
   if (c->cache_dtype != MLA_F32 && c->cache_dtype != MLA_BF16 && c->cache_dtype != MLA_FP8_E4M3)
     return MLA_ERR_INVALID_ARG;
-  if (c->kernel < MLA_KERNEL_AUTO || c->kernel > MLA_KERNEL_TC) return MLA_ERR_INVALID_ARG;
+  if (c->kernel < MLA_KERNEL_AUTO || c->kernel > MLA_KERNEL_TC_FP8_SCORES) return MLA_ERR_INVALID_ARG;
   if (c->d_latent > 512) return MLA_ERR_UNSUPPORTED;   // SIMT register tile bound
   // the cache input type follows the cache: fp32 cache <- fp32 latents, else bf16
   if (c->cache_dtype == MLA_FP8_E4M3) {
@@ -47,6 +47,7 @@ int make_dims(const mla_config* c, Dims* d) {
   d->scale = c->softmax_scale > 0.f ? c->softmax_scale : 1.0f / sqrtf((float)(c->d_head + c->d_rope));
   d->rope_base = c->rope_base > 0.f ? c->rope_base : 10000.0f;
   d->entry_bytes = (int)entry_bytes(c);
+  d->fp8_scores = false;
   // YaRN (「一文通透DeepSeek-V2」 §3.1.3): defaults are the page's values
   d->yarn_s = c->rope_scaling > 1.f ? c->rope_scaling : 1.f;
   d->yarn_orig = c->rope_orig_context > 0 ? c->rope_orig_context : 4096;
@@ -81,6 +82,8 @@ int pick_kernel(const mla_config* c, const Dims& d, int n_q) {
   const bool tc_ok = mla::tc_supported(d, n_q);
   if (c->kernel == MLA_KERNEL_SIMT) return MLA_KERNEL_SIMT;
   if (c->kernel == MLA_KERNEL_TC) return tc_ok ? MLA_KERNEL_TC : MLA_ERR_UNSUPPORTED;
+  if (c->kernel == MLA_KERNEL_TC_FP8_SCORES)
+    return tc_ok && d.cache_dtype == MLA_FP8_E4M3 ? MLA_KERNEL_TC_FP8_SCORES : MLA_ERR_UNSUPPORTED;
   return tc_ok ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
 }
 
@@ -148,7 +151,8 @@ size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n
   if (make_dims(cfg, &d) != MLA_OK || batch < 1 || n_q < 1 || max_seq_len < 1 || num_splits < 0)
     return 0;
   const int k = pick_kernel(cfg, d, n_q);
-  if (k == MLA_KERNEL_TC) return mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
+  if (k == MLA_KERNEL_TC || k == MLA_KERNEL_TC_FP8_SCORES)
+    return mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
   if (k != MLA_KERNEL_SIMT) return 0;
   const int S = mla::simt_pick_splits(d, batch, n_q, max_seq_len, num_splits, num_sms());
   return mla::simt_workspace_bytes(d, batch, n_q, S);
@@ -180,7 +184,8 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
   if ((long)max_pages_per_seq * d.P < (long)max_seq_len) return MLA_ERR_INVALID_ARG;
   const int k = pick_kernel(cfg, d, n_q);
   if (k < 0) return k;
-  if (k == MLA_KERNEL_TC) {
+  if (k == MLA_KERNEL_TC || k == MLA_KERNEL_TC_FP8_SCORES) {
+    d.fp8_scores = k == MLA_KERNEL_TC_FP8_SCORES;
     const size_t need = mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
     if (workspace_bytes < need || (need && !workspace)) return MLA_ERR_WORKSPACE;
     if (!aligned16(q_lat) || !aligned16(kv_pool) || !aligned16(o_lat) || !aligned16(workspace))

@@ -22,6 +22,8 @@ struct Dims {
   // YaRN on the decoupled RoPE (yarn_s <= 1: plain RoPE)
   float yarn_s, yarn_alpha, yarn_beta;
   int yarn_orig;
+  // FP8 cache: scores on FP8 tensor cores (q_lat's latent part quantised per 1x128 group)
+  bool fp8_scores;
 };
 
 // RoPE frequency of pair k, computed on the host in fp64: base^(-2k/R), or with YaRN

@@ -71,6 +71,20 @@ def test_kernel_selection():
     assert k in (M.MLA_KERNEL_SIMT, M.MLA_KERNEL_TC)
 
 
+def test_fp8_scores_kernel_selection():
+    """MLA_KERNEL_TC_FP8_SCORES runs only over an FP8 cache with the tensor-core shapes."""
+    fp8 = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=M.MLA_KERNEL_TC_FP8_SCORES)
+    assert M.mla_decode_kernel(fp8, 64, 1) == M.MLA_KERNEL_TC_FP8_SCORES
+    assert M.mla_decode_kernel(fp8, 64, 2) == M.MLA_KERNEL_TC_FP8_SCORES
+    bf16 = M.make_config(128, 128, 512, 64, 64, cache="bf16", kernel=M.MLA_KERNEL_TC_FP8_SCORES)
+    assert M.mla_decode_kernel(bf16, 64, 1) == L.MLA_ERR_UNSUPPORTED
+    small = M.make_config(4, 32, 128, 16, 16, cache="fp8", kernel=M.MLA_KERNEL_TC_FP8_SCORES)
+    assert M.mla_decode_kernel(small, 2, 1) == L.MLA_ERR_UNSUPPORTED
+    assert M.mla_decode_workspace_size(fp8, 8, 1, 4096, 3) == 8 * 1 * 128 * 3 * (512 + 1) * 4
+    bad = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=4)
+    assert M.mla_decode_kernel(bad, 1, 1) == L.MLA_ERR_INVALID_ARG
+
+
 def test_workspace_size_grows_with_splits():
     cfg = M.make_config(128, 128, 512, 64, 64, kernel=M.MLA_KERNEL_SIMT)
     assert M.mla_decode_workspace_size(cfg, 2, 1, 4096, 1) == 0
