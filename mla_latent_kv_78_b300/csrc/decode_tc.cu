@@ -1084,20 +1084,21 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
 #pragma unroll 1
       for (int p = 0; p < 5; ++p) {
         const int n = 5 * t + p, bb = n & 1, u = n >> 1;
+        // each warp reads only its own TMEM lanes: one lane polls for the warp
         bool okp = true;
-        if (stid == 0) okp = wait_bar(&bars->s_full[bb], (uint32_t)(u & 1), cx);
-        if (!bar_and(1, 256, okp)) return false;
+        if (lane == 0) okp = wait_bar(&bars->s_full[bb], (uint32_t)(u & 1), cx);
+        if (!__shfl_sync(0xffffffffu, okp, 0)) return false;
         tc_fence_after();
         const float f = p == 0 ? skv[0] : p == 1 ? skv[1] : p == 2 ? skv[2] : p == 3 ? skv[3] : 1.f;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float x[32];
-          tmem_ld32(lane_addr + (uint32_t)bb * 128u + 64 * g + 32 * h2, x);
+        for (int h4 = 0; h4 < 4; ++h4) {
+          float x[16];
+          tmem_ld16(lane_addr + (uint32_t)bb * 128u + 64 * g + 16 * h4, x);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float qs = p < 4 ? fs[F_SQ + (64 * g + 32 * h2 + c) * 4 + p] : 1.f;
-            acc[32 * h2 + c] = fmaf(f * qs, x[c], acc[32 * h2 + c]);
+          for (int c = 0; c < 16; ++c) {
+            const float qs = p < 4 ? fs[F_SQ + (64 * g + 16 * h4 + c) * 4 + p] : 1.f;
+            acc[16 * h4 + c] = fmaf(f * qs, x[c], acc[16 * h4 + c]);
           }
         }
         if (p < 4) {
@@ -1577,7 +1578,7 @@ __device__ __noinline__ void replay_passes(const Maps& maps, const Params& prm, 
   }
 }
 
-template <bool F8>
+template <bool F8, bool Q8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
     decode_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Params prm) {
   using Ly = Lay<F8>;
@@ -1630,10 +1631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   // weight is at most 1 and none is clamped).
   if constexpr (F8) {
     for (int mode = 0; mode < 3; ++mode) {
-      if (prm.q8)
-        decode_pass_ool<F8, true>(maps, prm, sm, mode);
-      else
-        decode_pass_ool<F8, false>(maps, prm, sm, mode);
+      decode_pass_ool<F8, Q8>(maps, prm, sm, mode);
       if (!end_of_pass<F8>(mode, sm)) break;
     }
   } else {
@@ -1755,10 +1753,11 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
     if (!tc::make_map(&maps.k, pool, prow, 64)) return cudaErrorInvalidValue;
     if (!tc::make_map(&maps.v, pool, prow, 32)) return cudaErrorInvalidValue;
   }
-  static std::atomic<bool> attr_bf16[kMaxDevices], attr_f8[kMaxDevices];
+  static std::atomic<bool> attr_bf16[kMaxDevices], attr_f8[kMaxDevices], attr_q8[kMaxDevices];
   {
-    cudaError_t e = f8 ? set_smem_limit_once(tc::decode_kernel<true>, tc::kSmemBytes<true>, attr_f8)
-                       : set_smem_limit_once(tc::decode_kernel<false>, tc::kSmemBytes<false>, attr_bf16);
+    cudaError_t e = !f8 ? set_smem_limit_once(tc::decode_kernel<false>, tc::kSmemBytes<false>, attr_bf16)
+                    : d.fp8_scores ? set_smem_limit_once(tc::decode_kernel<true, true>, tc::kSmemBytes<true>, attr_q8)
+                                   : set_smem_limit_once(tc::decode_kernel<true>, tc::kSmemBytes<true>, attr_f8);
     if (e != cudaSuccess) return e;
   }
   const size_t rows = (size_t)B * n_q * d.H;
@@ -1788,10 +1787,13 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);
 #endif
   const unsigned grid = 2u * (unsigned)(B * n_q * S);
-  cudaError_t e = f8 ? launch_programmatic(tc::decode_kernel<true>, dim3(grid), dim3(tc::Lay<true>::THREADS),
+  cudaError_t e =
+      !f8 ? launch_programmatic(tc::decode_kernel<false>, dim3(grid), dim3(tc::Lay<false>::THREADS),
+                                tc::kSmemBytes<false>, stream, maps, prm)
+      : d.fp8_scores ? launch_programmatic(tc::decode_kernel<true, true>, dim3(grid), dim3(tc::Lay<true>::THREADS),
                                            tc::kSmemBytes<true>, stream, maps, prm)
-                     : launch_programmatic(tc::decode_kernel<false>, dim3(grid), dim3(tc::Lay<false>::THREADS),
-                                           tc::kSmemBytes<false>, stream, maps, prm);
+                     : launch_programmatic(tc::decode_kernel<true>, dim3(grid), dim3(tc::Lay<true>::THREADS),
+                                           tc::kSmemBytes<true>, stream, maps, prm);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return e;
   return launch_combine(d.C, S, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, rows, stream);
