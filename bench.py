@@ -248,16 +248,17 @@ def run_reference(args, world, rank):
 
 
 def _other_workloads(M, W, torch, dev, flush, peaks, steps: int = 5):
-    """mla_decode alone on the ragged, long-context and FP8 two-token workloads, device
-    resident, over a pool filled with seeded random latents (their values do not change the
-    work; parity on these workloads is checked by the full-size tests). L2 flushed before
-    each timed call."""
+    """mla_decode alone on the ragged, long-context and FP8 two-token workloads (the last
+    also with its scores on FP8 tensor cores, MLA_KERNEL_TC_FP8_SCORES), device resident, over
+    a pool filled with seeded random latents (their values do not change the work; parity on
+    these workloads is checked by the full-size tests). L2 flushed before each timed call."""
     out = {}
     g = torch.Generator(device=dev)
-    for n in (3, 4, 5):
+    for n, kern in ((3, M.MLA_KERNEL_AUTO), (4, M.MLA_KERNEL_AUTO), (5, M.MLA_KERNEL_AUTO),
+                    (5, M.MLA_KERNEL_TC_FP8_SCORES)):
         wl = W.config(n)
         g.manual_seed(7800 + n)
-        cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act)
+        cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act, kernel=kern)
         eb = M.mla_cache_entry_bytes(cfg)
         if wl.cache == "fp8":
             pool = torch.randint(0, 0x76, (wl.num_pages, wl.P, eb), dtype=torch.uint8, device=dev,
@@ -298,10 +299,10 @@ def _other_workloads(M, W, torch, dev, flush, peaks, steps: int = 5):
         cache_bytes, qo_bytes, flops = _workload_sizes(wl)
         gbs = (cache_bytes + qo_bytes) / (ms * 1e-3) / 1e9
         tfl = flops / (ms * 1e-3) / 1e12
-        out[wl.name] = {
+        out[wl.name + ("-fp8-scores" if kern == M.MLA_KERNEL_TC_FP8_SCORES else "")] = {
             "decode_us": ms * 1e3, "gbs": gbs, "tflops": tfl,
             "hbm_frac": gbs / peaks["hbm_gbs"], "tensor_frac": tfl / peaks["bf16_tflops"],
-            "kernel": {1: "simt", 2: "tcgen05"}.get(M.mla_decode_kernel(cfg, wl.B, wl.n_q)),
+            "kernel": {1: "simt", 2: "tcgen05", 3: "tcgen05 (FP8 scores)"}.get(M.mla_decode_kernel(cfg, wl.B, wl.n_q)),
             "status": int(st.item()),
         }
         del pool, q, o, lse, ws

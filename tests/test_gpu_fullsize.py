@@ -60,3 +60,24 @@ def test_full_size_decode_step(n):
             assert_close(wl, gpu_rows(case.step.o, wl, b)[:, HEADS], o, f"cfg{n} o[b={b}]")
             assert_close(wl, gpu_rows(case.step.o_lat, wl, b)[:, HEADS], o_lat, f"cfg{n} naive o_lat[b={b}]")
             assert_close(wl, gpu_rows(case.step.lse, wl, b)[:, HEADS], lse, f"cfg{n} naive lse[b={b}]")
+
+
+@needs_cuda
+def test_full_size_two_token_decode_with_fp8_scores():
+    """Workload 5 (two-token decode, 128 x 8192, FP8 cache) through MLA_KERNEL_TC_FP8_SCORES:
+    every head of four sampled sequences against the oracle's FP8-scores reading (q_lat's
+    latent part quantised per 1x128 group, then the ordinary latent attention)."""
+    import mla_latent_kv_78_b300 as M
+    wl = W.config(5)
+    case = Case(wl, kernel=M.MLA_KERNEL_TC_FP8_SCORES)
+    case.run_step()
+    assert case.step.status() == 0
+    tau = tau_of(wl)
+    for b in _sampled_sequences(wl):
+        pos = wl.positions(b)
+        ce = case.cache_of(b)
+        q_lat = O.round_bf16(O.absorb_q(case.q_c_np[b], case.q_r_np[b], pos, case.w_uk_np, wl.rope_base, theta_of(wl)))
+        q8 = O.quantize_q_latent(q_lat, wl.C)[0]
+        ref_lat, ref_lse = O.latent_attention(q8, ce["c"], ce["k_r"], pos, tau)
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_lat, f"fp8-scores o_lat[b={b}] (all heads)")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"fp8-scores lse[b={b}] (all heads)")
