@@ -155,6 +155,7 @@ struct Params {
   long long wait_limit;   // clock cycles a bounded wait gives up after
   int withhold;           // test hook: latent chunk the even CTA never loads (-1: none)
   const int32_t* bt;
+  const int32_t* order;    // rows by decreasing visible length (nullptr: launch order)
   const uint8_t* pool;     // FP8 scores: the key scales are read from the entries
   int q8;                  // FP8 scores (MLA_KERNEL_TC_FP8_SCORES)
   int maxp, num_pages;
@@ -344,7 +345,8 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
   // ---- which (sequence, query row, split) this pair owns
   const int unit = blockIdx.x >> 1;
   const int split = unit % prm.S;
-  const int row = unit / prm.S;           // b * n_q + j
+  // b * n_q + j; with more rows than CTA pairs the longest rows go first (see plan_order_kernel)
+  const int row = prm.order ? __ldg(prm.order + unit / prm.S) : unit / prm.S;
   const int b = row / prm.n_q, j = row % prm.n_q;
   Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status, prm.wait_limit};
   const uint32_t tmem = bars->tmem_base;
@@ -1602,11 +1604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
 
-  // ---- which (sequence, query row, split) this pair owns
   const int unit = blockIdx.x >> 1;
-  const int split = unit % prm.S;
-  const int row = unit / prm.S;           // b * n_q + j
-  const int b = row / prm.n_q, j = row % prm.n_q;
   // ---- set-up
   if (tid == 0) TRACE(11, 0);
   if (tid == 0) init_barriers<F8>(bars);
@@ -1690,6 +1688,45 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The plan: query rows sorted by decreasing visible length (a counting sort on the number of
+// 256-token tiles, rows past kPlanBins - 1 tiles sharing the top bin), so that the longest rows
+// start first. Rows of equal length land in any order: every row's result is independent of
+// the pair that computes it. The decode that follows reads q_lat from the kernel before this
+// one, so this kernel waits for that kernel before it completes.
+constexpr int kPlanBins = 1024;
+__global__ void __launch_bounds__(1024) plan_order_kernel(const int32_t* __restrict__ seq_lens, int B, int n_q,
+                                                          int max_seq_len, int32_t* __restrict__ order) {
+  __shared__ int hist[kPlanBins];
+  griddep_launch_dependents();
+  const int rows = B * n_q, tid = threadIdx.x;
+  auto key_of = [&](int r) {
+    const int L = seq_lens[r / n_q];
+    const int vis = (L < n_q || L > max_seq_len) ? 0 : L - n_q + r % n_q + 1;
+    return min((vis + kTile - 1) / kTile, kPlanBins - 1);
+  };
+  hist[tid] = 0;
+  __syncthreads();
+  for (int r = tid; r < rows; r += blockDim.x) atomicAdd(&hist[key_of(r)], 1);
+  __syncthreads();
+  // start of bin k = rows in bins above k: an inclusive scan from the top bin down, shifted
+  const int mine = hist[kPlanBins - 1 - tid];
+  __syncthreads();
+  hist[tid] = mine;   // hist[i] = count of bin kPlanBins - 1 - i
+  __syncthreads();
+  for (int off = 1; off < kPlanBins; off <<= 1) {
+    const int add = tid >= off ? hist[tid - off] : 0;
+    __syncthreads();
+    hist[tid] += add;
+    __syncthreads();
+  }
+  const int incl = hist[tid];
+  __syncthreads();
+  hist[kPlanBins - 1 - tid] = incl - mine;   // exclusive start of bin kPlanBins - 1 - tid
+  __syncthreads();
+  for (int r = tid; r < rows; r += blockDim.x) order[atomicAdd(&hist[key_of(r)], 1)] = r;
+  griddep_wait();
+}
+
 // Test hook state (mla_debug_decode_fault): the limit of every bounded wait and a latent
 // chunk the bf16 kernel withholds.
 static std::atomic<long long> g_wait_limit{0};
@@ -1714,6 +1751,14 @@ bool tc_supported(const Dims& d, int n_q) {
          n_q >= 1 && n_q <= 2;
 }
 
+// With more query rows than CTA pairs the pairs take rows in the order of a plan (a
+// permutation of the rows by decreasing visible length, the longest-first rule for
+// scheduling unequal jobs on identical machines), kept in the workspace after the partials.
+static bool use_plan(int B, int n_q, int num_sms) { return B * n_q > num_sms / 2; }
+static size_t plan_bytes(int B, int n_q, int num_sms) {
+  return use_plan(B, n_q, num_sms) ? ((size_t)B * n_q * sizeof(int32_t) + 255) / 256 * 256 : 0;
+}
+
 static size_t partial_bytes(const Dims& d, int B, int n_q, int S) {
   if (S <= 1) return 0;
   const size_t rows = (size_t)B * n_q * d.H;
@@ -1724,7 +1769,7 @@ size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int nu
                           int num_sms) {
   const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, num_sms);
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
-  return part;
+  return part + plan_bytes(B, n_q, num_sms);
 }
 
 cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool, const int32_t* bt,
@@ -1762,12 +1807,14 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   }
   const size_t rows = (size_t)B * n_q * d.H;
   const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
-  if (ws_bytes < part) return cudaErrorInvalidValue;
+  if (ws_bytes < part + plan_bytes(B, n_q, sms)) return cudaErrorInvalidValue;
+  int32_t* order = use_plan(B, n_q, sms) ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + part) : nullptr;
   tc::Params prm;
   const long long lim = tc::g_wait_limit.load();
   prm.wait_limit = lim > 0 ? lim : tc::kTimeout;
   prm.withhold = tc::g_withhold.load();
   prm.bt = bt;
+  prm.order = order;
   prm.pool = static_cast<const uint8_t*>(pool);
   prm.q8 = d.fp8_scores ? 1 : 0;
   prm.maxp = maxp;
@@ -1787,6 +1834,11 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);
 #endif
   const unsigned grid = 2u * (unsigned)(B * n_q * S);
+  if (order) {
+    cudaError_t e = launch_programmatic(tc::plan_order_kernel, dim3(1), dim3(1024), 0, stream, seq_lens, B,
+                                        n_q, max_seq_len, order);
+    if (e != cudaSuccess) return e;
+  }
   cudaError_t e =
       !f8 ? launch_programmatic(tc::decode_kernel<false>, dim3(grid), dim3(tc::Lay<false>::THREADS),
                                 tc::kSmemBytes<false>, stream, maps, prm)

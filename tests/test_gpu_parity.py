@@ -166,6 +166,19 @@ def test_decode_splits_agree(splits, kernel, wl):
                                rtol=0, atol=2.0 ** -9)
 
 
+# more query rows than the 74 CTA pairs, lengths spread from 1 to 900 tokens: the tensor-core
+# decode takes its rows longest first (a device-side plan); every row must still be exact
+_lens = [int(x) for x in np.random.default_rng(51).integers(1, 900, size=96)]
+MANY_RAGGED = W.small_v2(96, _lens, n_q=1, cache="bf16", seed=52)
+MANY_RAGGED_FP8_MTP = W.small_v2(45, [max(2, x // 2) for x in _lens[:45]], n_q=2, cache="fp8", seed=53)
+
+
+@needs_cuda
+@pytest.mark.parametrize("wl", [MANY_RAGGED, MANY_RAGGED_FP8_MTP], ids=["bf16", "fp8-mtp"])
+def test_decode_many_ragged_rows(wl):
+    _decode_only(wl, M.MLA_KERNEL_AUTO)
+
+
 @needs_cuda
 def test_tensor_core_kernel_is_selected_for_v2_shapes():
     for wl in (SMALL_BF16, SMALL_BF16_MTP, SMALL_FP8, SMALL_FP8_LONG):
