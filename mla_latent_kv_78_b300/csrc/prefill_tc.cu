@@ -7,13 +7,14 @@
 // For a prompt the decompression is cheaper than attending in the 576-d latent space, so this
 // path forms K^C, V^C with the projection GEMM (bf16, [L][H d_h]), assembles Q = [q^C; RoPE(q^R)]
 // ([L][H][d_h + d_h^R]) and runs causal attention per head:
-//   one CTA per (head, 128 queries); 64-key blocks; S = Q K^T (M = 128 queries, N = 64 keys,
-//   K = 192) into one of two TMEM buffers; a softmax thread per query row (a reference maximum
-//   that moves when a block's maximum exceeds it by more than 2^8, O rescaled in TMEM then);
-//   P (bf16) through shared memory;
-//   O += P V (M = 128, N = 128, K = 64) in TMEM; TMA loads of Q once, of K^C, k^R and V^C in
-//   3-stage rings. Warp 0 loads, warp 1 issues the MMAs, warps 2-5 run the softmax
-//   (TMEM lane quadrant = warp % 4). Every wait is bounded.
+//   one CTA per (head, 256 queries) as two 128-query tiles that share every key and value
+//   block; 64-key blocks; per tile S = Q K^T (M = 128 queries, N = 64 keys, K = 192) into one of
+//   two TMEM buffers; a softmax thread per query row (a reference maximum that moves when a
+//   block's maximum exceeds it by more than 2^8, O rescaled in TMEM then); P (bf16) through
+//   shared memory; O += P V (M = 128, N = 128, K = 64) in TMEM; TMA loads of both tiles' Q
+//   once, of K^C, k^R and V^C in 2-stage rings. Warp 0 loads, warp 1 issues the MMAs, warps 2-5
+//   and 6-9 run the two tiles' softmax (TMEM lane quadrant = warp % 4), so each scheduler
+//   interleaves two softmax warps. Every wait is bounded.
 #include <math_constants.h>
 
 #include "mla_internal.cuh"
@@ -26,24 +27,25 @@ namespace pf {
 using namespace ptx;
 
 constexpr int kD = 128, kR = 64, kDQ = kD + kR;   // per-head qk width 192, v width 128
-constexpr int kBQ = 128, kBK = 64;               // queries per CTA, keys per block
-constexpr int kNK = 3, kNV = 3;                  // ring stages
-constexpr int kThreads = 192;
+constexpr int kBQ = 128, kBK = 64;               // queries per tile, keys per block
+constexpr int kTiles = 2;                        // query tiles per CTA, each with its softmax group
+constexpr int kNK = 2, kNV = 2;                  // ring stages
+constexpr int kThreads = 64 + 128 * kTiles;      // loader warp, MMA warp, 4 softmax warps per tile
 constexpr long long kTimeout = 4000000000LL;
 
 // shared-memory layout (bytes from the 1024-aligned base)
-constexpr int Q_OFF = 0;                            // 3 boxes [128 q x 64] = 48 KB
-constexpr int K_OFF = Q_OFF + 3 * 16384;            // kNK stages of 3 boxes [64 keys x 64] = 24 KB
-constexpr int V_OFF = K_OFF + kNK * 3 * 8192;       // kNV stages of 2 boxes [64 keys x 64 dv] = 16 KB
-constexpr int P_OFF = V_OFF + kNV * 2 * 8192;       // 2 buffers [128 q x 64 keys] = 16 KB each
-constexpr int BAR_OFF = P_OFF + 2 * 16384;
+constexpr int Q_OFF = 0;                             // per tile 3 boxes [128 q x 64] = 48 KB
+constexpr int K_OFF = Q_OFF + kTiles * 3 * 16384;    // kNK stages of 3 boxes [64 keys x 64] = 24 KB
+constexpr int V_OFF = K_OFF + kNK * 3 * 8192;        // kNV stages of 2 boxes [64 keys x 64 dv] = 16 KB
+constexpr int P_OFF = V_OFF + kNV * 2 * 8192;        // per tile [128 q x 64 keys] = 16 KB
+constexpr int BAR_OFF = P_OFF + kTiles * 16384;
 constexpr int kSmem = BAR_OFF + 256 + 1024;
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kNK], k_empty[kNK];
   uint64_t v_full[kNV], v_empty[kNV];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t s_full[kTiles][2], s_empty[kTiles][2], p_full[kTiles], pv_done[kTiles];
   uint32_t tmem;
 };
 static_assert(sizeof(Bars) <= 256, "barriers");
@@ -67,7 +69,9 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int
   return true;
 }
 
-// grid (H, ceil(L / 128)), 192 threads.
+// grid (H, ceil(L / 256)), 320 threads. Two query tiles share every key and value block: the
+// MMA warp issues S(j) of both tiles from one K stage and P.V(j - 1) of both from one V stage,
+// and while one tile's softmax group works the tensor core serves the other.
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmKR, const __grid_constant__ CUtensorMap tmV,
@@ -76,9 +80,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(sm + BAR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, q0 = blockIdx.y * kBQ;
-  // key blocks up to the last query of this block (causal)
-  const int nkb = min((p.L + kBK - 1) / kBK, (min(q0 + kBQ, p.L) - 1) / kBK + 1);
+  // the query blocks in decreasing order: the last ones attend to the most keys and start first
+  const int h = blockIdx.x, q0 = (gridDim.y - 1 - blockIdx.y) * (kTiles * kBQ);
+  // key blocks each tile needs (causal: up to its last query); 0 for a tile past the prompt
+  const int nkb_all = (p.L + kBK - 1) / kBK;
+  auto nkb_of = [&](int t) -> int {
+    const int qs = q0 + t * kBQ;
+    return qs < p.L ? min(nkb_all, (min(qs + kBQ, p.L) - 1) / kBK + 1) : 0;
+  };
+  const int nkb0 = nkb_of(0), nkb1 = nkb_of(1);
+  const int nkb = max(nkb0, nkb1);
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kNK; ++s) {
@@ -89,16 +100,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_empty[s], 4);   // the 4 softmax warps
-      mbar_init(&bars->p_full[s], 4);
-      mbar_init(&bars->pv_done[s], 1);
+    for (int t = 0; t < kTiles; ++t) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&bars->s_full[t][s], 1);
+        mbar_init(&bars->s_empty[t][s], 4);   // the tile's 4 softmax warps
+      }
+      mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->pv_done[t], 1);
     }
     fence_mbarrier_init_cluster();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem, 256);   // S buffers at columns 0 and 64, O at 128..255
+    tmem_alloc(&bars->tmem, 512);   // tile t: S buffers at 256t and 256t + 64, O at 256t + 128
     tmem_relinquish();
   }
   __syncthreads();
@@ -110,10 +123,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- loads (one box per lane)
     const uint64_t pol = policy_evict_normal();
-    if (lane < 3) {
-      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, 3 * 16384);
-      __syncwarp(0x7u);
-      tma_load_3d(sm + Q_OFF + lane * 16384, &tmQ, lane * 64, h, q0, &bars->q_full, pol);
+    if (lane < 3 * kTiles) {   // both tiles' Q (rows past the prompt read as zeros)
+      if (lane == 0) mbar_arrive_expect_tx(&bars->q_full, 3 * kTiles * 16384);
+      __syncwarp((1u << (3 * kTiles)) - 1u);
+      const int t = lane / 3, c = lane % 3;
+      tma_load_3d(sm + Q_OFF + t * 3 * 16384 + c * 16384, &tmQ, c * 64, h, q0 + t * kBQ, &bars->q_full, pol);
     }
     bool ok = true;
     for (int j = 0; j < nkb && ok; ++j) {
@@ -149,54 +163,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(kBQ, kBK, 0, 0);
       const uint32_t idPV = idesc_bf16_f32(kBQ, kD, 0, 1);   // P K-major, V MN-major
-      const uint32_t qa = smem_u32(sm + Q_OFF);
       bool ok = wait_bounded(&bars->q_full, 0, p.status);
-      auto issue_pv = [&](int j) -> bool {
-        const int b = j & 1, st = j % kNV;
-        if (!wait_bounded(&bars->p_full[b], (j >> 1) & 1, p.status)) return false;
-        if (!wait_bounded(&bars->v_full[st], (j / kNV) & 1, p.status)) return false;
-        tc_fence_after();
-        const uint32_t pa = smem_u32(sm + P_OFF + b * 16384);
+      auto issue_pv = [&](int jj) -> bool {
+        const int st = jj % kNV;
+        if (!wait_bounded(&bars->v_full[st], (jj / kNV) & 1, p.status)) return false;
         const uint32_t va = smem_u32(sm + V_OFF + st * 2 * 8192);
+        for (int t = 0; t < kTiles; ++t) {
+          if (jj >= (t ? nkb1 : nkb0)) continue;
+          if (!wait_bounded(&bars->p_full[t], jj & 1, p.status)) return false;
+          tc_fence_after();
+          const uint32_t pa = smem_u32(sm + P_OFF + t * 16384);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          mma_bf16(tmem + 128, smem_desc(pa + k * 32, 16, 1024, kSw128),
-                   smem_desc(va + k * 2048, 8192, 1024, kSw128), idPV, (j | k) != 0);
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(tmem + (uint32_t)t * 256 + 128, smem_desc(pa + k * 32, 16, 1024, kSw128),
+                     smem_desc(va + k * 2048, 8192, 1024, kSw128), idPV, (jj | k) != 0);
+          mma_commit(&bars->pv_done[t]);
+        }
         mma_commit(&bars->v_empty[st]);
-        mma_commit(&bars->pv_done[b]);
         return true;
       };
       for (int j = 0; j < nkb && ok; ++j) {
-        const int b = j & 1, st = j % kNK;
-        if (j >= 2) ok = wait_bounded(&bars->s_empty[b], ((j >> 1) - 1) & 1, p.status);
-        if (ok) ok = wait_bounded(&bars->k_full[st], (j / kNK) & 1, p.status);
+        const int st = j % kNK, b = j & 1;
+        ok = wait_bounded(&bars->k_full[st], (j / kNK) & 1, p.status);
         if (!ok) break;
-        tc_fence_after();
         const uint32_t ka = smem_u32(sm + K_OFF + st * 3 * 8192);
+        for (int t = 0; t < kTiles && ok; ++t) {
+          if (j >= (t ? nkb1 : nkb0)) continue;
+          if (j >= 2) ok = wait_bounded(&bars->s_empty[t][b], ((j >> 1) - 1) & 1, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm + Q_OFF + t * 3 * 16384);
 #pragma unroll
-        for (int c = 0; c < 3; ++c)
+          for (int c = 0; c < 3; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + (uint32_t)b * 64, smem_desc(qa + c * 16384 + k * 32, 16, 1024, kSw128),
-                     smem_desc(ka + c * 8192 + k * 32, 16, 1024, kSw128), idS, (c | k) != 0);
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tmem + (uint32_t)t * 256 + (uint32_t)b * 64, smem_desc(qa + c * 16384 + k * 32, 16, 1024, kSw128),
+                       smem_desc(ka + c * 8192 + k * 32, 16, 1024, kSw128), idS, (c | k) != 0);
+          mma_commit(&bars->s_full[t][b]);
+        }
         mma_commit(&bars->k_empty[st]);
-        mma_commit(&bars->s_full[b]);
-        if (j >= 1) ok = issue_pv(j - 1);
+        if (ok && j >= 1) ok = issue_pv(j - 1);
       }
       if (ok && nkb > 0) issue_pv(nkb - 1);
     }
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax (query rows)
+    const int t = (warp - 2) >> 2;          // query tile of this softmax group
+    const int nkbt = t ? nkb1 : nkb0;
     const int qd = warp & 3;
-    const int r = qd * 32 + lane;           // query row of this CTA = TMEM lane
-    const int qi = q0 + r;                   // query position
-    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const int r = qd * 32 + lane;           // query row of the tile = TMEM lane
+    const int qt = q0 + t * kBQ;            // the tile's first query
+    const int qi = qt + r;                  // query position
+    const uint32_t lane_addr = tmem + (uint32_t)t * 256 + ((uint32_t)(qd * 32) << 16);
     float m = -CUDART_INF_F, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkb && ok; ++j) {
+    for (int j = 0; j < nkbt && ok; ++j) {
       const int b = j & 1;
-      ok = wait_bounded(&bars->s_full[b], (j >> 1) & 1, p.status);
+      ok = wait_bounded(&bars->s_full[t][b], (j >> 1) & 1, p.status);
       if (!ok) break;
       tc_fence_after();
       float s[64];
@@ -205,19 +229,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty[b]);
+      if (lane == 0) mbar_arrive(&bars->s_empty[t][b]);
       const int k0 = j * kBK;
       float mx = -CUDART_INF_F;
+      if (k0 + kBK - 1 > qt || k0 + kBK > p.L) {
+        // a block on the tile's diagonal or at the prompt's end: mask keys past the query
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool valid = k0 + c <= qi && k0 + c < p.L;
-        s[c] = valid ? s[c] * p.scale_log2 : -CUDART_INF_F;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < 64; ++c) {
+          const bool valid = k0 + c <= qi && k0 + c < p.L;
+          s[c] = valid ? s[c] * p.scale_log2 : -CUDART_INF_F;
+          mx = fmaxf(mx, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          s[c] *= p.scale_log2;
+          mx = fmaxf(mx, s[c]);
+        }
       }
       // Lazy reference: the row keeps m while this block's maximum exceeds it by at most 8
       // (log2 units; weights up to 2^8 are exact in bf16 and fp32), so most blocks need no
-      // rescale of O and need not wait for the previous P.V. A larger maximum moves m here,
-      // before any weight is formed, so no weight is ever clamped.
+      // rescale of O. A larger maximum moves m here, before any weight is formed, so no weight
+      // is ever clamped.
       const bool move = mx > m + 8.f;
       const float m_new = move ? mx : m;
       const float alpha = move ? (m == -CUDART_INF_F ? 0.f : ex2(m - m_new)) : 1.f;
@@ -232,15 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
       }
       l = l * alpha + sum;
-      // The P buffer of this block is free once P.V of block j - 2 is done; O may be rescaled
-      // only once P.V of block j - 1 is.
-      const bool rescale = j >= 1 && __any_sync(0xffffffffu, alpha != 1.f);
-      const int wj = rescale ? j - 1 : j - 2;
-      if (wj >= 0) ok = wait_bounded(&bars->pv_done[wj & 1], (wj >> 1) & 1, p.status);
+      // the tile's P buffer is free, and O stable to rescale, once P.V of block j - 1 is done
+      if (j >= 1) ok = wait_bounded(&bars->pv_done[t], (j - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      if (rescale) {
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < kD; c += 32) {
           float o[32];
@@ -253,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       // P row r, 128-byte swizzle (16-byte unit u goes to u ^ (r & 7))
-      uint8_t* prow = sm + P_OFF + b * 16384 + r * 128;
+      uint8_t* prow = sm + P_OFF + t * 16384 + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
@@ -261,11 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
-    if (ok && nkb > 0) ok = wait_bounded(&bars->pv_done[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, p.status);
+    if (ok && nkbt > 0) ok = wait_bounded(&bars->pv_done[t], (nkbt - 1) & 1, p.status);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    if (ok && nkbt > 0) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -284,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // Q[t][i] = [q^C[t][i] ; RoPE_t(q^R[t][i])] (bf16), one block per token: the token's cos/sin
@@ -379,7 +409,7 @@ cudaError_t launch_prefill(const Dims& d, const void* c_kv, const void* k_r, int
   static std::atomic<bool> attr[kMaxDevices];
   e = set_smem_limit_once(pf::prefill_attn_kernel, pf::kSmem, attr);
   if (e != cudaSuccess) return e;
-  dim3 grid(d.H, (L + pf::kBQ - 1) / pf::kBQ);
+  dim3 grid(d.H, (L + pf::kTiles * pf::kBQ - 1) / (pf::kTiles * pf::kBQ));
   e = launch_programmatic(pf::prefill_attn_kernel, grid, dim3(pf::kThreads), pf::kSmem, stream, tmQ, tmK,
                           tmKR, tmV, p);
   return e == cudaSuccess ? cudaGetLastError() : e;
