@@ -15,7 +15,9 @@ import mla_latent_kv_78_b300 as M
 import workloads as W
 from mla_latent_kv_78_b300 import _lib as L
 
-from _support import ACT, Case, assert_close, dev
+from oracle import mla_oracle as O
+
+from _support import ACT, Case, assert_close, dev, gpu_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +56,15 @@ def test_noalloc_matches_decode_on_consecutive_calls(kernel):
         ref_o, ref_lse, o, lse = _both(wl, kernel, splits)
         assert_close(wl, o.float().cpu().numpy(), ref_o.float().cpu().numpy(), "o_lat noalloc")
         assert_close(wl, lse.cpu().numpy(), ref_lse.cpu().numpy(), "lse noalloc")
+        # and against the oracle directly
+        q_lat = wl.latent_queries()
+        tau = O.softmax_scale(wl.D, wl.R)
+        for b in range(wl.B):
+            c, r = wl.latents(b)
+            ce = O.cache_entries(c, r, np.arange(wl.seq_lens[b]), wl.cache, wl.rope_base)
+            ref_ob, ref_lb = O.latent_attention(q_lat[b], ce["c"], ce["k_r"], wl.positions(b), tau)
+            assert_close(wl, gpu_rows(o, wl, b), ref_ob, f"o_lat noalloc vs oracle [b={b}]")
+            assert_close(wl, gpu_rows(lse, wl, b), ref_lb, f"lse noalloc vs oracle [b={b}]")
 
 
 @needs_cuda
