@@ -164,6 +164,153 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 1) tmem_dealloc(tmem, BN < 32 ? 32 : BN);
 }
 
+// ---------------------------------------------------------------- persistent, prompt-sized
+// Y [T][N] in bf16 for large T (the prefill's k^C = W^{UK} c, v^C = W^{UV} c): one CTA per SM
+// loops over 128 x 128 output tiles (row tile fastest, so neighbouring CTAs share an X tile in
+// L2). The K stages stream through one ring across tiles; the MMA warp accumulates tile i into
+// TMEM buffer i % 2 while the epilogue warps drain buffer (i - 1) % 2: thread = output feature,
+// bf16 values staged in shared memory (128-byte swizzle, two staging tiles) and stored with TMA.
+constexpr int kPStages = 4;
+constexpr int kPBN = 128;
+constexpr int kPStage = kBM * kBK * 2 + kPBN * kBK * 2;   // 32 KB
+constexpr int kPStageOut = kPBN * kBM * 2;                // 32 KB: [128 tokens][128 features]
+constexpr int kPBars = kPStages * kPStage + 2 * kPStageOut;
+constexpr int kPSmem = kPBars + (2 * kPStages + 4) * 8 + 16 + 1024;
+
+__global__ void __launch_bounds__(192, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                           const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPBars);
+  uint64_t* freeb = full + kPStages;
+  uint64_t* acc_full = freeb + kPStages;   // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint32_t* slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = (p.N + kBM - 1) / kBM, t_tiles = (p.T + kPBN - 1) / kPBN;
+  const int tiles = n_tiles * t_tiles;
+  const int nk = (p.K + kBK - 1) / kBK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&freeb[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);   // the 4 epilogue warps
+    }
+    fence_mbarrier_init_cluster();
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, 2 * kPBN);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  griddep_launch_dependents();
+  griddep_wait();
+  if (warp == 0) {
+    // ---- producer: W rows and X tokens of each K step, the two boxes from two lanes
+    const uint64_t pol_w = policy_evict_normal();   // W is re-read by every token tile
+    const uint64_t pol_x = policy_evict_normal();
+    int it = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < tiles && ok; i += gridDim.x) {
+      const int n0 = (i % n_tiles) * kBM, t0 = (i / n_tiles) * kPBN;
+      for (int ks = 0; ks < nk && ok; ++ks, ++it) {
+        const int st = it % kPStages;
+        bool r = true;
+        if (lane == 0 && it >= kPStages) r = wait_bounded(&freeb[st], ((it / kPStages) - 1) & 1, p.status);
+        ok = __shfl_sync(0xffffffffu, r, 0);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], kPStage);
+        __syncwarp();
+        if (lane < 2) {
+          uint8_t* dst = sm + st * kPStage + lane * (kBM * kBK * 2);
+          tma_load_2d(dst, lane ? &tmX : &tmW, ks * kBK, lane ? t0 : n0, &full[st], lane ? pol_x : pol_w);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: D[feature][token] of tile i in TMEM buffer i % 2
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16_f32(kBM, kPBN, 0, 0);
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < tiles && ok; i += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        if (lt >= 2) ok = wait_bounded(&acc_empty[b], ((lt >> 1) - 1) & 1, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        for (int ks = 0; ks < nk && ok; ++ks, ++it) {
+          const int st = it % kPStages;
+          ok = wait_bounded(&full[st], (it / kPStages) & 1, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a = smem_u32(sm + st * kPStage), bb = a + kBM * kBK * 2;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(tmem + (uint32_t)b * kPBN, smem_desc(a + k * 32, 16, 1024, kSw128),
+                     smem_desc(bb + k * 32, 16, 1024, kSw128), id, (ks | k) != 0);
+          mma_commit(&freeb[st]);
+        }
+        if (ok) mma_commit(&acc_full[b]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: thread = feature row r of the tile (TMEM lane quadrant = warp % 4)
+    const int qd = warp & 3, r = qd * 32 + lane, et = threadIdx.x - 64;   // et: 0..127
+    const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+    int lt = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < tiles && ok; i += gridDim.x, ++lt) {
+      const int n0 = (i % n_tiles) * kBM, t0 = (i / n_tiles) * kPBN;
+      const int b = lt & 1;
+      if (lane == 0) ok = wait_bounded(&acc_full[b], (lt >> 1) & 1, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      // the staging tile of tile lt - 2 has been read by its TMA stores
+      if (et == 0) bulk_wait_read_1();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      uint8_t* stg = sm + kPStages * kPStage + b * kPStageOut;
+      // staging: two boxes [128 tokens][64 features] (128-byte rows, 16-byte unit u of token t at
+      // u ^ (t & 7)); feature r goes to box r / 64, unit (r % 64) / 8, element r % 8
+      uint8_t* col = stg + (r >> 6) * (kPBN * 128) + ((r & 63) & 7) * 2;
+      const uint32_t u = (uint32_t)((r & 63) >> 3);
+#pragma unroll 1
+      for (int c = 0; c < kPBN; c += 32) {
+        float v[32];
+        tmem_ld32(lane_base + (uint32_t)b * kPBN + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int t = c + x;
+          *reinterpret_cast<__nv_bfloat16*>(col + t * 128 + ((u ^ (uint32_t)(t & 7)) << 4)) = __float2bfloat16_rn(v[x]);
+        }
+      }
+      // TMEM buffer b may take the next tile
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (et == 0) {
+        tma_store_2d(&tmY, stg, n0, t0);
+        tma_store_2d(&tmY, stg + kPBN * 128, n0 + 64, t0);
+        bulk_commit_group();
+      }
+    }
+    if (et == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 2 * kPBN);
+}
+
 // Y[t][n] = sum over the splits, in split order; fp32 or bf16 out (with a row stride).
 template <typename Out>
 __global__ void __launch_bounds__(256) gemm_reduce_kernel(const float* __restrict__ part, int splits,
@@ -226,6 +373,26 @@ cudaError_t launch_gemm(const void* x, const void* w, int T, int N, int K, int s
   p.out = direct && out_dtype == MLA_F32 ? static_cast<float*>(y) : part;
   p.out_bf16 = direct && out_dtype == MLA_BF16 ? static_cast<__nv_bfloat16*>(y) : nullptr;
   const bool reduce = !direct && out_dtype != kGemmPartials;
+  if (direct && p.out_bf16 && T > 128) {
+    // prompt-sized bf16 output: the persistent kernel, one CTA per SM
+    CUtensorMap tmY;
+    {
+      const uint64_t dims[2] = {(uint64_t)N, (uint64_t)T};
+      const uint64_t st[1] = {(uint64_t)N * 2};
+      const uint32_t box[2] = {64, gemm::kPBN};
+      if (!encode_bf16_map(&tmY, y, 2, dims, st, box)) return cudaErrorInvalidValue;
+    }
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int tiles = ((N + gemm::kBM - 1) / gemm::kBM) * ((T + gemm::kPBN - 1) / gemm::kPBN);
+    static std::atomic<bool> attr[kMaxDevices];
+    cudaError_t e = set_smem_limit_once(gemm::gemm_persistent_kernel, gemm::kPSmem, attr);
+    if (e == cudaSuccess)
+      e = launch_programmatic(gemm::gemm_persistent_kernel, dim3(tiles < sms ? tiles : sms), dim3(192),
+                              gemm::kPSmem, stream, tmW, tmX, tmY, p);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+  }
   dim3 grid((N + gemm::kBM - 1) / gemm::kBM, (T + bn - 1) / bn, splits);
   cudaError_t e;
   if (bn == 64) {
