@@ -29,7 +29,7 @@ using namespace ptx;
 constexpr int kD = 128, kR = 64, kDQ = kD + kR;   // per-head qk width 192, v width 128
 constexpr int kBQ = 128, kBK = 64;               // queries per tile, keys per block
 constexpr int kTiles = 2;                        // query tiles per CTA, each with its softmax group
-constexpr int kNK = 2, kNV = 2;                  // ring stages
+constexpr int kNK = 3, kNV = 3;                  // ring stages
 constexpr int kThreads = 64 + 128 * kTiles;      // loader warp, MMA warp, 4 softmax warps per tile
 constexpr long long kTimeout = 4000000000LL;
 
@@ -37,15 +37,14 @@ constexpr long long kTimeout = 4000000000LL;
 constexpr int Q_OFF = 0;                             // per tile 3 boxes [128 q x 64] = 48 KB
 constexpr int K_OFF = Q_OFF + kTiles * 3 * 16384;    // kNK stages of 3 boxes [64 keys x 64] = 24 KB
 constexpr int V_OFF = K_OFF + kNK * 3 * 8192;        // kNV stages of 2 boxes [64 keys x 64 dv] = 16 KB
-constexpr int P_OFF = V_OFF + kNV * 2 * 8192;        // per tile [128 q x 64 keys] = 16 KB
-constexpr int BAR_OFF = P_OFF + kTiles * 16384;
+constexpr int BAR_OFF = V_OFF + kNV * 2 * 8192;      // (P lives in tensor memory)
 constexpr int kSmem = BAR_OFF + 256 + 1024;
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kNK], k_empty[kNK];
   uint64_t v_full[kNV], v_empty[kNV];
-  uint64_t s_full[kTiles][2], s_empty[kTiles][2], p_full[kTiles], pv_done[kTiles];
+  uint64_t s_full[kTiles][2], p_full[kTiles][2], pv_done[kTiles][2];   // by S / P buffer
   uint32_t tmem;
 };
 static_assert(sizeof(Bars) <= 256, "barriers");
@@ -103,15 +102,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < kTiles; ++t) {
       for (int s = 0; s < 2; ++s) {
         mbar_init(&bars->s_full[t][s], 1);
-        mbar_init(&bars->s_empty[t][s], 4);   // the tile's 4 softmax warps
+        mbar_init(&bars->p_full[t][s], 4);   // the tile's 4 softmax warps
+        mbar_init(&bars->pv_done[t][s], 1);
       }
-      mbar_init(&bars->p_full[t], 4);
-      mbar_init(&bars->pv_done[t], 1);
     }
     fence_mbarrier_init_cluster();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem, 512);   // tile t: S buffers at 256t and 256t + 64, O at 256t + 128
+    tmem_alloc(&bars->tmem, 512);   // tile t: S / P buffers at 256t and 256t + 64, O at 256t + 128
     tmem_relinquish();
   }
   __syncthreads();
@@ -168,16 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = jj % kNV;
         if (!wait_bounded(&bars->v_full[st], (jj / kNV) & 1, p.status)) return false;
         const uint32_t va = smem_u32(sm + V_OFF + st * 2 * 8192);
+        const int bb = jj & 1;
         for (int t = 0; t < kTiles; ++t) {
           if (jj >= (t ? nkb1 : nkb0)) continue;
-          if (!wait_bounded(&bars->p_full[t], jj & 1, p.status)) return false;
+          if (!wait_bounded(&bars->p_full[t][bb], (jj >> 1) & 1, p.status)) return false;
           tc_fence_after();
-          const uint32_t pa = smem_u32(sm + P_OFF + t * 16384);
+          // A = P in tensor memory: the bf16 weights the softmax wrote over S buffer bb
+          const uint32_t pa = tmem + (uint32_t)t * 256 + (uint32_t)bb * 64;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16(tmem + (uint32_t)t * 256 + 128, smem_desc(pa + k * 32, 16, 1024, kSw128),
-                     smem_desc(va + k * 2048, 8192, 1024, kSw128), idPV, (jj | k) != 0);
-          mma_commit(&bars->pv_done[t]);
+            mma_bf16_ta(tmem + (uint32_t)t * 256 + 128, pa + (uint32_t)k * 8,
+                        smem_desc(va + k * 2048, 8192, 1024, kSw128), idPV, (jj | k) != 0);
+          mma_commit(&bars->pv_done[t][bb]);
         }
         mma_commit(&bars->v_empty[st]);
         return true;
@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ka = smem_u32(sm + K_OFF + st * 3 * 8192);
         for (int t = 0; t < kTiles && ok; ++t) {
           if (j >= (t ? nkb1 : nkb0)) continue;
-          if (j >= 2) ok = wait_bounded(&bars->s_empty[t][b], ((j >> 1) - 1) & 1, p.status);
+          // S / P buffer b is free once P.V of block j - 2 has read its weights
+          if (j >= 2) ok = wait_bounded(&bars->pv_done[t][b], ((j >> 1) - 1) & 1, p.status);
           if (!ok) break;
           tc_fence_after();
           const uint32_t qa = smem_u32(sm + Q_OFF + t * 3 * 16384);
@@ -227,9 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_addr + b * 64, s);
       tmem_ld32(lane_addr + b * 64 + 32, s + 32);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_empty[t][b]);
       const int k0 = j * kBK;
       float mx = -CUDART_INF_F;
       if (k0 + kBK - 1 > qt || k0 + kBK > p.L) {
@@ -265,12 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
       }
       l = l * alpha + sum;
-      // the tile's P buffer is free, and O stable to rescale, once P.V of block j - 1 is done
-      if (j >= 1) ok = wait_bounded(&bars->pv_done[t], (j - 1) & 1, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
+      // O is stable to rescale once P.V of block j - 1 is done (only then is it waited for)
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        ok = wait_bounded(&bars->pv_done[t][(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < kD; c += 32) {
           float o[32];
@@ -282,18 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // P row r, 128-byte swizzle (16-byte unit u goes to u ^ (r & 7))
-      uint8_t* prow = sm + P_OFF + t * 16384 + r * 128;
+      // P row r over the S columns just read (bf16 pairs, one 32-bit column per two keys)
+      {
+        float pf[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();
+        for (int c = 0; c < 32; ++c) pf[c] = __uint_as_float(pk[c]);
+        tmem_st32(lane_addr + b * 64, pf);
+        tmem_st_wait();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[t]);
+      if (lane == 0) mbar_arrive(&bars->p_full[t][b]);
     }
-    if (ok && nkbt > 0) ok = wait_bounded(&bars->pv_done[t], (nkbt - 1) & 1, p.status);
+    if (ok && nkbt > 0) ok = wait_bounded(&bars->pv_done[t][(nkbt - 1) & 1], ((nkbt - 1) >> 1) & 1, p.status);
     ok = __all_sync(0xffffffffu, ok);
     if (ok && nkbt > 0) {
       tc_fence_after();
