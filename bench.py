@@ -249,13 +249,16 @@ def run_reference(args, world, rank):
 
 def _other_workloads(M, W, torch, dev, flush, peaks, steps: int = 5):
     """mla_decode alone on the ragged, long-context and FP8 two-token workloads (the last
-    also with its scores on FP8 tensor cores, MLA_KERNEL_TC_FP8_SCORES), device resident, over
+    also with its scores on FP8 tensor cores, MLA_KERNEL_TC_FP8_SCORES, and with the cache
+    staged to bf16 first, MLA_KERNEL_TC_FP8_STAGED), device resident, over
     a pool filled with seeded random latents (their values do not change the work; parity on
     these workloads is checked by the full-size tests). L2 flushed before each timed call."""
     out = {}
     g = torch.Generator(device=dev)
+    suffix = {M.MLA_KERNEL_AUTO: "", M.MLA_KERNEL_TC_FP8_SCORES: "-fp8-scores",
+              M.MLA_KERNEL_TC_FP8_STAGED: "-fp8-staged"}
     for n, kern in ((3, M.MLA_KERNEL_AUTO), (4, M.MLA_KERNEL_AUTO), (5, M.MLA_KERNEL_AUTO),
-                    (5, M.MLA_KERNEL_TC_FP8_SCORES)):
+                    (5, M.MLA_KERNEL_TC_FP8_SCORES), (5, M.MLA_KERNEL_TC_FP8_STAGED)):
         wl = W.config(n)
         g.manual_seed(7800 + n)
         cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act, kernel=kern)
@@ -299,10 +302,11 @@ def _other_workloads(M, W, torch, dev, flush, peaks, steps: int = 5):
         cache_bytes, qo_bytes, flops = _workload_sizes(wl)
         gbs = (cache_bytes + qo_bytes) / (ms * 1e-3) / 1e9
         tfl = flops / (ms * 1e-3) / 1e12
-        out[wl.name + ("-fp8-scores" if kern == M.MLA_KERNEL_TC_FP8_SCORES else "")] = {
+        out[wl.name + suffix[kern]] = {
             "decode_us": ms * 1e3, "gbs": gbs, "tflops": tfl,
             "hbm_frac": gbs / peaks["hbm_gbs"], "tensor_frac": tfl / peaks["bf16_tflops"],
-            "kernel": {1: "simt", 2: "tcgen05", 3: "tcgen05 (FP8 scores)"}.get(M.mla_decode_kernel(cfg, wl.B, wl.n_q)),
+            "kernel": {1: "simt", 2: "tcgen05", 3: "tcgen05 (FP8 scores)",
+                       4: "FP8 staged to bf16 + tcgen05"}.get(M.mla_decode_kernel(cfg, wl.B, wl.n_q)),
             "status": int(st.item()),
         }
         del pool, q, o, lse, ws

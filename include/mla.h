@@ -90,6 +90,18 @@ extern "C" {
                                bf16 RoPE part is added. Softmax and P.V as MLA_KERNEL_TC.
                                FP8 cache, same shapes as MLA_KERNEL_TC; else
                                MLA_ERR_UNSUPPORTED. */
+#define MLA_KERNEL_TC_FP8_STAGED 4  /* FP8 cache, same shapes as MLA_KERNEL_TC (else
+                               MLA_ERR_UNSUPPORTED): one streaming kernel converts every
+                               visible token of the batch once into a bf16 pool in the
+                               workspace (code * group scale in fp32, rounded once to bf16,
+                               the same operand values MLA_KERNEL_TC builds inside the
+                               decode; RoPE keys copied), then the bf16 tensor-core decode
+                               runs over that pool. Trades workspace for speed: the
+                               workspace grows by batch * ceil(max_seq_len/64) * 64 * 1152
+                               bytes (plus the staged block table), and each visible token
+                               costs 1152 more bytes written and read back; in exchange no
+                               token is converted more than once (MLA_KERNEL_TC converts it
+                               once per query row) and the conversion runs on every SM. */
 
 typedef struct mla_config {
   int32_t n_heads;      /* H  = n_h                                               */
@@ -164,15 +176,16 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
 /*
  * Workspace bytes mla_decode needs for these sizes: the fp32 split partials (one [C] output
  * and one log-sum-exp per query row, head and split) when the rows are split over several
- * ranges (num_splits, or the automatic choice, above 1); 0 otherwise.
+ * ranges (num_splits, or the automatic choice, above 1); 0 otherwise. With
+ * MLA_KERNEL_TC_FP8_STAGED also the staged bf16 pool and its block table, which come first.
  * num_splits as for mla_decode; max_seq_len bounds every seq_lens[b].
  */
 size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n_q,
                                  int32_t max_seq_len, int32_t num_splits);
 
 /*
- * Which decode kernel mla_decode would launch for these sizes:
- * MLA_KERNEL_SIMT or MLA_KERNEL_TC, or a negative MLA_ERR_* code.
+ * Which decode kernel mla_decode would launch for these sizes: one of the MLA_KERNEL_*
+ * values other than MLA_KERNEL_AUTO, or a negative MLA_ERR_* code.
  */
 int mla_decode_kernel(const mla_config* cfg, int32_t batch, int32_t n_q);
 

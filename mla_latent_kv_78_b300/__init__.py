@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     MLA_KERNEL_SIMT,
     MLA_KERNEL_TC,
     MLA_KERNEL_TC_FP8_SCORES,
+    MLA_KERNEL_TC_FP8_STAGED,
     MlaError,
     lib,
     make_config,

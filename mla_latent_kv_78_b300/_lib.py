@@ -32,6 +32,7 @@ MLA_DEV_TIMEOUT = 4
 
 MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
 MLA_KERNEL_AUTO, MLA_KERNEL_SIMT, MLA_KERNEL_TC, MLA_KERNEL_TC_FP8_SCORES = 0, 1, 2, 3
+MLA_KERNEL_TC_FP8_STAGED = 4
 
 _DTYPES = {"f32": MLA_F32, "bf16": MLA_BF16, "fp8": MLA_FP8_E4M3}
 TORCH_ACT = {MLA_F32: torch.float32, MLA_BF16: torch.bfloat16}

@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmla_b300.so")
 SOURCES = ["mla_api.cu", "append.cu", "absorb.cu", "absorb_tc.cu", "decode_simt.cu", "decode_tc.cu",
-           "decode_noalloc.cu", "gemm_tc.cu", "prefill_tc.cu"]
+           "decode_noalloc.cu", "gemm_tc.cu", "prefill_tc.cu", "stage_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

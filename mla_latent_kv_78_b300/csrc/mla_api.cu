@@ -30,7 +30,7 @@ int make_dims(const mla_config* c, Dims* d) {
   if (c->act_dtype != MLA_F32 && c->act_dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
   if (c->cache_dtype != MLA_F32 && c->cache_dtype != MLA_BF16 && c->cache_dtype != MLA_FP8_E4M3)
     return MLA_ERR_INVALID_ARG;
-  if (c->kernel < MLA_KERNEL_AUTO || c->kernel > MLA_KERNEL_TC_FP8_SCORES) return MLA_ERR_INVALID_ARG;
+  if (c->kernel < MLA_KERNEL_AUTO || c->kernel > MLA_KERNEL_TC_FP8_STAGED) return MLA_ERR_INVALID_ARG;
   if (c->d_latent > 512) return MLA_ERR_UNSUPPORTED;   // SIMT register tile bound
   // the cache input type follows the cache: fp32 cache <- fp32 latents, else bf16
   if (c->cache_dtype == MLA_FP8_E4M3) {
@@ -84,6 +84,8 @@ int pick_kernel(const mla_config* c, const Dims& d, int n_q) {
   if (c->kernel == MLA_KERNEL_TC) return tc_ok ? MLA_KERNEL_TC : MLA_ERR_UNSUPPORTED;
   if (c->kernel == MLA_KERNEL_TC_FP8_SCORES)
     return tc_ok && d.cache_dtype == MLA_FP8_E4M3 ? MLA_KERNEL_TC_FP8_SCORES : MLA_ERR_UNSUPPORTED;
+  if (c->kernel == MLA_KERNEL_TC_FP8_STAGED)
+    return tc_ok && d.cache_dtype == MLA_FP8_E4M3 ? MLA_KERNEL_TC_FP8_STAGED : MLA_ERR_UNSUPPORTED;
   return tc_ok ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
 }
 
@@ -153,6 +155,9 @@ size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n
   const int k = pick_kernel(cfg, d, n_q);
   if (k == MLA_KERNEL_TC || k == MLA_KERNEL_TC_FP8_SCORES)
     return mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
+  if (k == MLA_KERNEL_TC_FP8_STAGED)
+    return mla::fp8_staged_bytes(batch, max_seq_len) +
+           mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
   if (k != MLA_KERNEL_SIMT) return 0;
   const int S = mla::simt_pick_splits(d, batch, n_q, max_seq_len, num_splits, num_sms());
   return mla::simt_workspace_bytes(d, batch, n_q, S);
@@ -194,6 +199,17 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
                                          num_pages, seq_lens, batch, n_q, max_seq_len, num_splits,
                                          workspace, workspace_bytes, o_lat, lse, dev_status,
                                          (cudaStream_t)stream));
+  }
+  if (k == MLA_KERNEL_TC_FP8_STAGED) {
+    const size_t need = mla::fp8_staged_bytes(batch, max_seq_len) +
+                        mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
+    if (workspace_bytes < need || !workspace) return MLA_ERR_WORKSPACE;
+    if (!aligned16(q_lat) || !aligned16(kv_pool) || !aligned16(o_lat) || !aligned16(workspace))
+      return MLA_ERR_ALIGNMENT;
+    return cuda_rc(mla::launch_decode_tc_fp8_staged(d, q_lat, kv_pool, block_table, max_pages_per_seq,
+                                                    num_pages, seq_lens, batch, n_q, max_seq_len,
+                                                    num_splits, workspace, workspace_bytes, o_lat, lse,
+                                                    dev_status, (cudaStream_t)stream));
   }
   const int S = mla::simt_pick_splits(d, batch, n_q, max_seq_len, num_splits, num_sms());
   const size_t need = mla::simt_workspace_bytes(d, batch, n_q, S);

@@ -103,4 +103,14 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
                              int max_seq_len, int num_splits, void* ws, size_t ws_bytes,
                              void* o_lat, float* lse, int32_t* status, cudaStream_t stream);
 
+// FP8 cache staged to bf16 (every visible token converted once into the workspace), then the
+// bf16 tensor-core decode over the staged pool. The workspace holds fp8_staged_bytes() first,
+// then the bf16 decode's own workspace.
+size_t fp8_staged_bytes(int B, int max_seq_len);
+cudaError_t launch_decode_tc_fp8_staged(const Dims& d, const void* q_lat, const void* pool,
+                                        const int32_t* bt, int maxp, int num_pages,
+                                        const int32_t* seq_lens, int B, int n_q, int max_seq_len,
+                                        int num_splits, void* ws, size_t ws_bytes, void* o_lat,
+                                        float* lse, int32_t* status, cudaStream_t stream);
+
 }  // namespace mla

@@ -81,8 +81,28 @@ def test_fp8_scores_kernel_selection():
     small = M.make_config(4, 32, 128, 16, 16, cache="fp8", kernel=M.MLA_KERNEL_TC_FP8_SCORES)
     assert M.mla_decode_kernel(small, 2, 1) == L.MLA_ERR_UNSUPPORTED
     assert M.mla_decode_workspace_size(fp8, 8, 1, 4096, 3) == 8 * 1 * 128 * 3 * (512 + 1) * 4
-    bad = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=4)
+    bad = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=5)
     assert M.mla_decode_kernel(bad, 1, 1) == L.MLA_ERR_INVALID_ARG
+
+
+def test_fp8_staged_kernel_selection_and_workspace():
+    """MLA_KERNEL_TC_FP8_STAGED runs only over an FP8 cache with the tensor-core shapes; its
+    workspace is the staged bf16 pool (ceil(max_seq_len / 64) pages of 64 x 1152 bytes per
+    sequence), the staged block table (rounded up to 256 bytes), then the tensor-core kernel's
+    own workspace."""
+    st = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=M.MLA_KERNEL_TC_FP8_STAGED)
+    assert M.mla_decode_kernel(st, 64, 1) == M.MLA_KERNEL_TC_FP8_STAGED
+    assert M.mla_decode_kernel(st, 64, 2) == M.MLA_KERNEL_TC_FP8_STAGED
+    bf16 = M.make_config(128, 128, 512, 64, 64, cache="bf16", kernel=M.MLA_KERNEL_TC_FP8_STAGED)
+    assert M.mla_decode_kernel(bf16, 64, 1) == L.MLA_ERR_UNSUPPORTED
+    small = M.make_config(4, 32, 128, 16, 16, cache="fp8", kernel=M.MLA_KERNEL_TC_FP8_STAGED)
+    assert M.mla_decode_kernel(small, 2, 1) == L.MLA_ERR_UNSUPPORTED
+    tc = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=M.MLA_KERNEL_TC)
+    for B, n_q, L_max, splits in ((8, 1, 4096, 3), (5, 2, 1000, 1), (128, 2, 8192, 0)):
+        ppr = -(-L_max // 64)
+        staged = B * ppr * 64 * 1152 + -(-(B * ppr * 4) // 256) * 256
+        assert (M.mla_decode_workspace_size(st, B, n_q, L_max, splits)
+                == staged + M.mla_decode_workspace_size(tc, B, n_q, L_max, splits))
 
 
 def test_workspace_size_grows_with_splits():

@@ -81,3 +81,23 @@ def test_full_size_two_token_decode_with_fp8_scores():
         ref_lat, ref_lse = O.latent_attention(q8, ce["c"], ce["k_r"], pos, tau)
         assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_lat, f"fp8-scores o_lat[b={b}] (all heads)")
         assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"fp8-scores lse[b={b}] (all heads)")
+
+
+@needs_cuda
+def test_full_size_two_token_decode_staged():
+    """Workload 5 (two-token decode, 128 x 8192, FP8 cache) through MLA_KERNEL_TC_FP8_STAGED
+    (the cache converted once to bf16 in the workspace, then the bf16 tensor-core decode):
+    every head of four sampled sequences against the oracle."""
+    import mla_latent_kv_78_b300 as M
+    wl = W.config(5)
+    case = Case(wl, kernel=M.MLA_KERNEL_TC_FP8_STAGED)
+    case.run_step()
+    assert case.step.status() == 0
+    tau = tau_of(wl)
+    for b in _sampled_sequences(wl):
+        pos = wl.positions(b)
+        ce = case.cache_of(b)
+        q_lat = O.round_bf16(O.absorb_q(case.q_c_np[b], case.q_r_np[b], pos, case.w_uk_np, wl.rope_base, theta_of(wl)))
+        ref_lat, ref_lse = O.latent_attention(q_lat, ce["c"], ce["k_r"], pos, tau)
+        assert_close(wl, gpu_rows(case.step.o_lat, wl, b), ref_lat, f"staged o_lat[b={b}] (all heads)")
+        assert_close(wl, gpu_rows(case.step.lse, wl, b), ref_lse, f"staged lse[b={b}] (all heads)")

@@ -68,6 +68,21 @@ def test_noalloc_matches_decode_on_consecutive_calls(kernel):
 
 
 @needs_cuda
+def test_noalloc_staged_fp8_decode():
+    """MLA_KERNEL_TC_FP8_STAGED keeps its bf16 copy of the cache in the scratch: a small batch
+    fits and matches mla_decode bit for bit; the two-token 128 x 8192 batch (1.2 GB staged)
+    is refused before anything is launched."""
+    wl = W.small_v2(3, [300, 129, 700], n_q=2, cache="fp8", seed=24)
+    ref_o, ref_lse, o, lse = _both(wl, M.MLA_KERNEL_TC_FP8_STAGED, 0)
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    cfg = M.make_config(128, 128, 512, 64, 64, cache="fp8", kernel=M.MLA_KERNEL_TC_FP8_STAGED)
+    assert M.mla_decode_workspace_size(cfg, 128, 2, 8192, 0) > L.NOALLOC_SCRATCH_BYTES
+    rc = M.lib().mla_decode_noalloc(ctypes.byref(cfg), 16, 16, 16, 128, 16384, 16, 128, 2, 8192, 0,
+                                    16, None, None, None)
+    assert rc == L.MLA_ERR_SCRATCH_LIMIT
+
+
+@needs_cuda
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     wl = W.small_v2(2, [64, 64], n_q=1, cache="bf16", seed=23)
     cfg = M.make_config(wl.H, wl.D, wl.C, wl.R, wl.P, cache=wl.cache, act=wl.act)
