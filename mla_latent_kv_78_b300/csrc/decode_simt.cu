@@ -140,8 +140,12 @@ template <typename Act>
 __global__ void __launch_bounds__(128) combine_kernel(int C, int S, const float* __restrict__ ws_o,
                                                       const float* __restrict__ ws_lse,
                                                       Act* __restrict__ o_lat,
-                                                      float* __restrict__ lse_out) {
+                                                      float* __restrict__ lse_out,
+                                                      const int32_t* __restrict__ row_of, int H) {
   const size_t r = blockIdx.x;
+  // output row: r itself, or (partials of some query rows only) head r % H of query row
+  // row_of[r / H]
+  const size_t out = row_of ? (size_t)__ldg(row_of + r / H) * H + r % H : r;
   float M = -CUDART_INF_F;
   for (int s = 0; s < S; ++s) M = fmaxf(M, ws_lse[r * S + s]);
   float z = 0.f;
@@ -156,9 +160,9 @@ __global__ void __launch_bounds__(128) combine_kernel(int C, int S, const float*
       const float ls = ws_lse[r * S + s];
       if (ls != -CUDART_INF_F) v = fmaf(__expf(ls - M), ws_o[(r * S + s) * C + k], v);
     }
-    st_act(o_lat, r * C + k, v * inv);
+    st_act(o_lat, out * C + k, v * inv);
   }
-  if (threadIdx.x == 0 && lse_out) lse_out[r] = z > 0.f ? M + logf(z) : -CUDART_INF_F;
+  if (threadIdx.x == 0 && lse_out) lse_out[out] = z > 0.f ? M + logf(z) : -CUDART_INF_F;
 }
 
 size_t simt_workspace_bytes(const Dims& d, int B, int n_q, int S) {
@@ -196,17 +200,21 @@ static cudaError_t launch_t(const Dims& d, const void* q_lat, const void* pool, 
                                             ws_lse, (Act*)o_lat, lse, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || S == 1) return e;
-  combine_kernel<Act><<<(unsigned)rows, 128, 0, stream>>>(d.C, S, ws_o, ws_lse, (Act*)o_lat, lse);
+  combine_kernel<Act><<<(unsigned)rows, 128, 0, stream>>>(d.C, S, ws_o, ws_lse, (Act*)o_lat, lse,
+                                                           nullptr, 1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(int C, int S, const float* ws_o, const float* ws_lse, void* o_lat,
-                           int act_dtype, float* lse, size_t rows, cudaStream_t stream) {
+                           int act_dtype, float* lse, size_t rows, cudaStream_t stream,
+                           const int32_t* row_of, int H) {
   if (act_dtype == MLA_F32)
-    combine_kernel<float><<<(unsigned)rows, 128, 0, stream>>>(C, S, ws_o, ws_lse, (float*)o_lat, lse);
+    combine_kernel<float><<<(unsigned)rows, 128, 0, stream>>>(C, S, ws_o, ws_lse, (float*)o_lat, lse,
+                                                              row_of, H);
   else
     combine_kernel<__nv_bfloat16><<<(unsigned)rows, 128, 0, stream>>>(C, S, ws_o, ws_lse,
-                                                                      (__nv_bfloat16*)o_lat, lse);
+                                                                      (__nv_bfloat16*)o_lat, lse,
+                                                                      row_of, H);
   return cudaGetLastError();
 }
 

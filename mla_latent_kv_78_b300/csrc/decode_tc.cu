@@ -161,6 +161,7 @@ struct Params {
   int maxp, num_pages;
   const int32_t* seq_lens;
   int B, n_q, max_seq_len, S;
+  int tail;                // rows of the plan's tail run as two half-range units each (S == 1)
   float scale_log2;
   __nv_bfloat16* o_lat;
   float* lse;
@@ -344,16 +345,36 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
 
   // ---- which (sequence, query row, split) this pair owns
   const int unit = blockIdx.x >> 1;
-  const int split = unit % prm.S;
-  // b * n_q + j; with more rows than CTA pairs the longest rows go first (see plan_order_kernel)
-  const int row = prm.order ? __ldg(prm.order + unit / prm.S) : unit / prm.S;
+  // row = b * n_q + j; with more rows than CTA pairs the longest rows go first (see
+  // plan_order_kernel), and the last `tail` rows of the plan each run as two units (split 0 and
+  // 1 of 2) whose partials sit at the row's place in the tail. Head h's result goes to entry
+  // obase + h * ostride of o_lat / lse rows (ostride 1) or of the partials (ostride = splits).
+  int row, split, nsplit, obase, ostride;
+  {
+    const int rows = prm.B * prm.n_q;
+    int prow;
+    if (prm.tail > 0 && unit >= rows - prm.tail) {
+      const int k = unit - (rows - prm.tail);
+      prow = k >> 1;
+      split = k & 1;
+      nsplit = 2;
+      row = __ldg(prm.order + rows - prm.tail + prow);
+    } else {
+      split = unit % prm.S;
+      nsplit = prm.S;
+      row = prm.order ? __ldg(prm.order + unit / prm.S) : unit / prm.S;
+      prow = row;
+    }
+    obase = nsplit == 1 ? row * kH : prow * kH * nsplit + split;
+    ostride = nsplit;
+  }
   const int b = row / prm.n_q, j = row % prm.n_q;
   Ctx cx{reinterpret_cast<volatile int*>(&flags[FL_ABORT]), prm.status, prm.wait_limit};
   const uint32_t tmem = bars->tmem_base;
   const int L = prm.seq_lens[b];
   const bool bad_len = (L < prm.n_q || L > prm.max_seq_len);
   const int visible = bad_len ? 0 : L - prm.n_q + j + 1;
-  int chunk = (visible + prm.S - 1) / prm.S;
+  int chunk = (visible + nsplit - 1) / nsplit;
   chunk = (chunk + kTile - 1) / kTile * kTile;
   const int lo = min(visible, split * chunk);
   const int hi = min(visible, lo + chunk);
@@ -392,18 +413,18 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
     for (int idx = tid; idx < kH * 256; idx += kThreads) {
       const int h = idx >> 8, q = idx & 255;
       const int dc = (q >> 7) * 256 + rank * 128 + (q & 127);
-      const size_t o = (size_t)row * kH + h;
-      if (prm.S == 1)
+      const size_t o = (size_t)obase + (size_t)h * ostride;
+      if (ostride == 1)
         prm.o_lat[o * kC + dc] = __float2bfloat16_rn(0.f);
       else
-        prm.ws_o[(o * prm.S + split) * kC + dc] = 0.f;
+        prm.ws_o[o * kC + dc] = 0.f;
     }
     if (rank == 0 && tid < kH) {
-      const size_t o = (size_t)row * kH + tid;
-      if (prm.S == 1) {
+      const size_t o = (size_t)obase + (size_t)tid * ostride;
+      if (ostride == 1) {
         if (prm.lse) prm.lse[o] = -CUDART_INF_F;
       } else {
-        prm.ws_lse[o * prm.S + split] = -CUDART_INF_F;
+        prm.ws_lse[o] = -CUDART_INF_F;
       }
     }
   } else if (warp == 0) {
@@ -1491,11 +1512,11 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
           if (rank == 0) {
             const float lse = Lsum > 0.f ? (fs[F_M + h] + log2f(Lsum)) * 0.6931471805599453f
                                          : -CUDART_INF_F;
-            const size_t o = (size_t)row * kH + h;
-            if (prm.S == 1) {
+            const size_t o = (size_t)obase + (size_t)h * ostride;
+            if (ostride == 1) {
               if (prm.lse) prm.lse[o] = lse;
             } else {
-              prm.ws_lse[o * prm.S + split] = lse;
+              prm.ws_lse[o] = lse;
             }
           }
         }
@@ -1513,11 +1534,11 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
               for (int x = 0; x < 32; ++x) {
                 const int h = 64 * g + hh * 32 + x;
                 const float val = o[x] * fs[F_INV + h];
-                const size_t orow = (size_t)row * kH + h;
-                if (prm.S == 1)
-                  prm.o_lat[orow * kC + dc] = __float2bfloat16_rn(val);
+                const size_t o = (size_t)obase + (size_t)h * ostride;
+                if (ostride == 1)
+                  prm.o_lat[o * kC + dc] = __float2bfloat16_rn(val);
                 else
-                  prm.ws_o[(orow * prm.S + split) * kC + dc] = val;
+                  prm.ws_o[o * kC + dc] = val;
               }
             }
           }
@@ -1688,10 +1709,11 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The plan: query rows sorted by decreasing visible length (a counting sort on the number of
-// 256-token tiles, rows past kPlanBins - 1 tiles sharing the top bin), so that the longest rows
-// start first. Rows of equal length land in any order: every row's result is independent of
-// the pair that computes it. The decode that follows reads q_lat from the kernel before this
+// The plan: query rows sorted by decreasing visible length (a stable counting sort on the
+// number of 256-token tiles, rows past kPlanBins - 1 tiles sharing the top bin), so that the
+// longest rows start first. The order is a function of the lengths alone (equal keys keep
+// their row order), so the rows that end up in the split tail, and with them every result,
+// are the same on every call. The decode that follows reads q_lat from the kernel before this
 // one, so this kernel waits for that kernel before it completes.
 constexpr int kPlanBins = 1024;
 __global__ void __launch_bounds__(1024) plan_order_kernel(const int32_t* __restrict__ seq_lens, int B, int n_q,
@@ -1723,7 +1745,24 @@ __global__ void __launch_bounds__(1024) plan_order_kernel(const int32_t* __restr
   __syncthreads();
   hist[kPlanBins - 1 - tid] = incl - mine;   // exclusive start of bin kPlanBins - 1 - tid
   __syncthreads();
-  for (int r = tid; r < rows; r += blockDim.x) order[atomicAdd(&hist[key_of(r)], 1)] = r;
+  // scatter in row order by one warp, 32 rows per step: lanes with equal keys take
+  // consecutive places in lane order, and one of them advances the bin's next place
+  if (tid < 32) {
+    for (int base = 0; base < rows; base += 32) {
+      const int r = base + tid;
+      const int k = r < rows ? key_of(r) : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, k);
+      const int first = __ffs(same) - 1;
+      const int rank = __popc(same & ((1u << tid) - 1u));
+      int at = 0;
+      if (tid == first && k >= 0) at = hist[k];
+      at = __shfl_sync(0xffffffffu, at, first);
+      if (k >= 0) order[at + rank] = r;
+      __syncwarp();
+      if (tid == first && k >= 0) hist[k] = at + __popc(same);
+      __syncwarp();
+    }
+  }
   griddep_wait();
 }
 
@@ -1759,16 +1798,29 @@ static size_t plan_bytes(int B, int n_q, int num_sms) {
   return use_plan(B, n_q, num_sms) ? ((size_t)B * n_q * sizeof(int32_t) + 255) / 256 * 256 : 0;
 }
 
-static size_t partial_bytes(const Dims& d, int B, int n_q, int S) {
-  if (S <= 1) return 0;
-  const size_t rows = (size_t)B * n_q * d.H;
-  return rows * S * ((size_t)d.C + 1) * sizeof(float);
+// With one split and more rows than CTA pairs, the rows of the last, partly filled round of
+// pairs (in the plan's order the shortest) are each split in two when that round would keep
+// at most half of the pairs busy: their halves then take that round in half the time.
+static int pick_tail(int B, int n_q, int num_splits, int S, int num_sms) {
+  const int rows = B * n_q, pairs = num_sms / 2;
+  if (num_splits > 0 || S != 1 || !use_plan(B, n_q, num_sms) || rows <= pairs) return 0;
+  const int r = rows % pairs;
+  return 2 * r <= pairs ? r : 0;
+}
+
+// fp32 partial outputs and log-sum-exps: every row's S ranges, or the tail rows' two halves
+static size_t partial_bytes(const Dims& d, int B, int n_q, int S, int tail) {
+  const size_t rows = S > 1 ? (size_t)B * n_q : (size_t)tail;
+  const int n = S > 1 ? S : 2;
+  if (rows == 0) return 0;
+  return rows * d.H * n * ((size_t)d.C + 1) * sizeof(float);
 }
 
 size_t tc_workspace_bytes(const Dims& d, int B, int n_q, int max_seq_len, int num_splits,
                           int num_sms) {
   const int S = tc::pick_splits(B, n_q, max_seq_len, num_splits, num_sms);
-  const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
+  const int tail = pick_tail(B, n_q, num_splits, S, num_sms);
+  const size_t part = (partial_bytes(d, B, n_q, S, tail) + 255) / 256 * 256;
   return part + plan_bytes(B, n_q, num_sms);
 }
 
@@ -1805,8 +1857,10 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
                                    : set_smem_limit_once(tc::decode_kernel<true>, tc::kSmemBytes<true>, attr_f8);
     if (e != cudaSuccess) return e;
   }
-  const size_t rows = (size_t)B * n_q * d.H;
-  const size_t part = (partial_bytes(d, B, n_q, S) + 255) / 256 * 256;
+  const int tail = pick_tail(B, n_q, num_splits, S, sms);
+  const size_t prows = (S > 1 ? (size_t)B * n_q : (size_t)tail) * d.H;   // partial rows
+  const int pn = S > 1 ? S : 2;                                         // partials per row
+  const size_t part = (partial_bytes(d, B, n_q, S, tail) + 255) / 256 * 256;
   if (ws_bytes < part + plan_bytes(B, n_q, sms)) return cudaErrorInvalidValue;
   int32_t* order = use_plan(B, n_q, sms) ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + part) : nullptr;
   tc::Params prm;
@@ -1824,16 +1878,17 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
   prm.n_q = n_q;
   prm.max_seq_len = max_seq_len;
   prm.S = S;
+  prm.tail = tail;
   prm.scale_log2 = d.scale * 1.4426950408889634f;
   prm.o_lat = static_cast<__nv_bfloat16*>(o_lat);
   prm.lse = lse;
-  prm.ws_o = S > 1 ? static_cast<float*>(ws) : nullptr;
-  prm.ws_lse = S > 1 ? static_cast<float*>(ws) + rows * S * d.C : nullptr;
+  prm.ws_o = part ? static_cast<float*>(ws) : nullptr;
+  prm.ws_lse = part ? static_cast<float*>(ws) + prows * pn * d.C : nullptr;
   prm.status = status;
 #ifdef MLA_TC_TRACE
   prm.trace = static_cast<unsigned long long*>(tc::g_tc_trace_host);
 #endif
-  const unsigned grid = 2u * (unsigned)(B * n_q * S);
+  const unsigned grid = 2u * (unsigned)(B * n_q * S + tail);
   if (order) {
     cudaError_t e = launch_programmatic(tc::plan_order_kernel, dim3(1), dim3(1024), 0, stream, seq_lens, B,
                                         n_q, max_seq_len, order);
@@ -1847,8 +1902,10 @@ cudaError_t launch_decode_tc(const Dims& d, const void* q_lat, const void* pool,
                      : launch_programmatic(tc::decode_kernel<true>, dim3(grid), dim3(tc::Lay<true>::THREADS),
                                            tc::kSmemBytes<true>, stream, maps, prm);
   if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess || S == 1) return e;
-  return launch_combine(d.C, S, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, rows, stream);
+  if (e != cudaSuccess || (S == 1 && tail == 0)) return e;
+  // the tail's partial row p belongs to query row order[rows - tail + p]
+  return launch_combine(d.C, pn, prm.ws_o, prm.ws_lse, o_lat, MLA_BF16, lse, prows, stream,
+                        S > 1 ? nullptr : order + (B * n_q - tail), d.H);
 }
 
 }  // namespace mla

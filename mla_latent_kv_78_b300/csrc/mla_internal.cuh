@@ -68,8 +68,10 @@ cudaError_t launch_decode_simt(const Dims& d, const void* q_lat, const void* poo
                                float* lse, int32_t* status, cudaStream_t stream);
 
 // Log-sum-exp merge of split partials ws_o [rows][S][C], ws_lse [rows][S] into o_lat, lse.
+// Partial row r goes to output row r, or with row_of to head r % H of query row row_of[r / H].
 cudaError_t launch_combine(int C, int S, const float* ws_o, const float* ws_lse, void* o_lat,
-                           int act_dtype, float* lse, size_t rows, cudaStream_t stream);
+                           int act_dtype, float* lse, size_t rows, cudaStream_t stream,
+                           const int32_t* row_of = nullptr, int H = 1);
 
 // Tensor-core projection Y = X . W^T (X [T][K], W [N][K] bf16; K a multiple of 8). Y is fp32 or
 // bf16 (out_dtype); kGemmPartials leaves the fp32 split partials [splits][T][N] in `part`.

@@ -179,6 +179,27 @@ def test_decode_many_ragged_rows(wl):
     _decode_only(wl, M.MLA_KERNEL_AUTO)
 
 
+# 90 query rows of one length: two full rounds of the 74 CTA pairs would leave 16 rows for a
+# third; those (the plan's last 16) run instead as two half-range units each, merged after
+EQUAL_MTP = W.small_v2(45, [700] * 45, n_q=2, cache="bf16", seed=54)
+
+
+@needs_cuda
+def test_tail_rows_split_in_two_are_exact_and_deterministic():
+    """Every row, split or not, against the oracle; then the same decode three more times
+    with bit-identical results (which rows form the split tail depends on the lengths only)."""
+    wl = EQUAL_MTP
+    case = _decode_only(wl, M.MLA_KERNEL_AUTO)
+    # the 16 tail rows' two fp32 partials per head (148 SMs: 74 pairs)
+    assert M.mla_decode_workspace_size(case.cfg, wl.B, wl.n_q, wl.max_seq_len, 0) >= 16 * 128 * 2 * 513 * 4
+    q = dev(wl.latent_queries().reshape(-1, wl.H, wl.C + wl.R), ACT[wl.act])
+    first_o, first_lse = case.step.o_lat.clone(), case.step.lse.clone()
+    for _ in range(3):
+        case.step.decode(q)
+        torch.cuda.synchronize()
+        assert torch.equal(case.step.o_lat, first_o) and torch.equal(case.step.lse, first_lse)
+
+
 @needs_cuda
 def test_tensor_core_kernel_is_selected_for_v2_shapes():
     for wl in (SMALL_BF16, SMALL_BF16_MTP, SMALL_FP8, SMALL_FP8_LONG):
