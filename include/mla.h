@@ -176,7 +176,10 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
 /*
  * Workspace bytes mla_decode needs for these sizes: the fp32 split partials (one [C] output
  * and one log-sum-exp per query row, head and split) when the rows are split over several
- * ranges (num_splits, or the automatic choice, above 1); 0 otherwise. With
+ * ranges (num_splits, or the automatic choice, above 1). The tensor-core kernels also keep
+ * there, with more query rows than CTA pairs, the order in which the pairs take the rows
+ * (longest first), and with the automatic choice the two partials of each row in a last,
+ * partly filled round of pairs that it splits in two. 0 when none of this applies. With
  * MLA_KERNEL_TC_FP8_STAGED also the staged bf16 pool and its block table, which come first.
  * num_splits as for mla_decode; max_seq_len bounds every seq_lens[b].
  */

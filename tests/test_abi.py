@@ -105,6 +105,25 @@ def test_fp8_staged_kernel_selection_and_workspace():
                 == staged + M.mla_decode_workspace_size(tc, B, n_q, L_max, splits))
 
 
+def test_tensor_core_workspace_holds_the_plan_and_the_split_tail():
+    """Automatic schedule of the tensor-core decode on 148 SMs (74 CTA pairs; the CPU build
+    assumes that count): more query rows than pairs need the plan (one int32 per row, rounded
+    up to 256 bytes); when the rows left for the last round fill at most half the pairs, those
+    rows are split in two and their fp32 partials (2 x (512 + 1) floats per head) come first."""
+    cfg = M.make_config(128, 128, 512, 64, 64)
+
+    def up(x):
+        return -(-x // 256) * 256
+
+    part = 128 * 2 * (512 + 1) * 4   # one split row's partials, all heads
+    assert M.mla_decode_workspace_size(cfg, 64, 1, 4096, 0) == 0                      # 64 rows: one round
+    assert M.mla_decode_workspace_size(cfg, 128, 1, 32768, 0) == up(128 * 4)          # 54 left > 37: no split
+    assert M.mla_decode_workspace_size(cfg, 45, 2, 700, 0) == up(16 * part) + up(90 * 4)
+    assert M.mla_decode_workspace_size(cfg, 128, 2, 8192, 0) == up(34 * part) + up(256 * 4)
+    # an explicit split count turns the tail off
+    assert M.mla_decode_workspace_size(cfg, 128, 2, 8192, 1) == up(256 * 4)
+
+
 def test_workspace_size_grows_with_splits():
     cfg = M.make_config(128, 128, 512, 64, 64, kernel=M.MLA_KERNEL_SIMT)
     assert M.mla_decode_workspace_size(cfg, 2, 1, 4096, 1) == 0
