@@ -101,7 +101,9 @@ extern "C" {
                                bytes (plus the staged block table), and each visible token
                                costs 1152 more bytes written and read back; in exchange no
                                token is converted more than once (MLA_KERNEL_TC converts it
-                               once per query row) and the conversion runs on every SM. */
+                               once per query row) and the conversion runs on every SM.
+                               mla_decode returns MLA_ERR_UNSUPPORTED for batch > 65535 or
+                               batch * ceil(max_seq_len/64) * 64 >= 2^31 staged rows. */
 
 typedef struct mla_config {
   int32_t n_heads;      /* H  = n_h                                               */

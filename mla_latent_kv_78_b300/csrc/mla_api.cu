@@ -201,6 +201,9 @@ int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
                                          (cudaStream_t)stream));
   }
   if (k == MLA_KERNEL_TC_FP8_STAGED) {
+    // the staging grid is (pages per row, batch); the staged pool's rows must fit an int
+    if (batch > 65535 || (long)batch * ((max_seq_len + d.P - 1) / d.P) * d.P > 0x7fffffffL)
+      return MLA_ERR_UNSUPPORTED;
     const size_t need = mla::fp8_staged_bytes(batch, max_seq_len) +
                         mla::tc_workspace_bytes(d, batch, n_q, max_seq_len, num_splits, num_sms());
     if (workspace_bytes < need || !workspace) return MLA_ERR_WORKSPACE;
