@@ -75,8 +75,7 @@ constexpr int F_LLOC = F_ALPHA + 128;  // [128]
 constexpr int F_LRCV = F_LLOC + 128;   // [128]
 constexpr int F_INV = F_LRCV + 128;    // [128]
 constexpr int F_X0 = F_INV + 128;     // [128] the peer's tile-0 per-head maxima
-constexpr int F_SQ = F_X0 + 128;     // [128 heads][4] FP8 scores: query group scales (both CTAs')
-constexpr int F_FLAG = F_SQ + 4 * kH;    // ints, see FL_*
+constexpr int F_FLAG = F_X0 + 128;    // ints, see FL_*
 constexpr int FL_RESCALE = 0;  // [2] by tile parity: the reference moved for this tile
 constexpr int FL_ABORT = 2;    // a bounded wait gave up
 constexpr int FL_PUB = 3;      // [2] by tile parity: this CTA published the tile's maxima
@@ -85,18 +84,26 @@ constexpr int FL_CLAMP = 6;    // this pass clamped a weight of this CTA's token
 constexpr int FL_REPLAY = 7;   // the unit runs again exactly (set in both CTAs alike)
 constexpr int FL_PEER_CLAMP = 8;   // the peer's FL_CLAMP, received with its epilogue sums
 constexpr int FL_PEER_ABORT = 9;   // the peer's FL_ABORT at the end of a pass
-constexpr int F_END = F_FLAG + 10;   // (even: the barriers that follow need 8-byte alignment)
+constexpr int F_FLAGS_END = F_FLAG + 10;
+constexpr int F_SQ = F_FLAGS_END;    // [128 heads][4] FP8 scores: query group scales (both CTAs')
+// end of the fp32 scratch (even: the barriers that follow need 8-byte alignment); only the FP8
+// instantiations keep the query group scales
+template <bool F8>
+constexpr int F_END = F8 ? F_SQ + 4 * kH : F_FLAGS_END;
 // Shared-memory layout. bf16 cache: keys and latents arrive by TMA in their MMA layout.
 // FP8 cache: raw codes and scales arrive by TMA in staging rings (RS, RV slots) and the
 // converter warps write bf16 operand tiles into the S and V rings.
 template <bool F8>
 struct Lay {
-  // bf16: Q travels with every key chunk (a [64 heads x 64 dims] box read from L2 next to the
-  // [128 tokens x 64 dims] key box), which frees 72 KB for deeper rings and two P^T buffers.
-  // FP8: Q stays resident.
+  // bf16: Q is streamed, chunk by chunk, next to the key chunks (a [64 heads x 64 dims] box
+  // read from L2 per [128 tokens x 64 dims] key box), which frees 72 KB for deeper rings and
+  // two P^T buffers; its own NQ-slot ring trails the key ring by NQ chunks, so with
+  // 2 NQ >= NS a Q slot is always free once the key slot of the same step is. FP8: Q stays
+  // resident.
   static constexpr bool QRES = F8;
-  static constexpr int SSTAGE = QRES ? 16384 : 16384 + 8192;   // S-phase stage bytes
-  static constexpr int NS = F8 ? 2 : 3;     // S-phase ring
+  static constexpr int SSTAGE = 16384;      // S-phase stage bytes (key chunk)
+  static constexpr int NS = F8 ? 2 : 4;     // S-phase ring
+  static constexpr int NQ = F8 ? 0 : 2;     // streamed Q chunks (bf16) [64 heads x 64 dims]
   static constexpr int NV = F8 ? 2 : 4;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
   static constexpr int PB = F8 ? 1 : 2;     // P^T buffers [256 tok x 64 heads] = 32 KB each
   static constexpr int RS = F8 ? 3 : 0;     // raw key-chunk slots (kRawS bytes)
@@ -104,12 +111,13 @@ struct Lay {
   static constexpr int THREADS = F8 ? 512 : 416;
   static constexpr int OFF_Q = 0;                        // 9 x [64 heads x 64 dims] (8 KB each)
   static constexpr int OFF_S = OFF_Q + (QRES ? kKCh * 8192 : 0);
-  static constexpr int OFF_V = OFF_S + NS * SSTAGE;
+  static constexpr int OFF_QS = OFF_S + NS * SSTAGE;
+  static constexpr int OFF_V = OFF_QS + NQ * 8192;
   static constexpr int OFF_P = OFF_V + NV * 16384;
   static constexpr int OFF_RS = OFF_P + PB * 32768;
   static constexpr int OFF_RV = OFF_RS + RS * kRawS;
   static constexpr int OFF_F = OFF_RV + RV * kRawV;      // fp32 scratch
-  static constexpr int OFF_BAR = OFF_F + F_END * 4;
+  static constexpr int OFF_BAR = OFF_F + F_END<F8> * 4;
 };
 
 template <bool F8>
@@ -120,6 +128,7 @@ struct BarsT {
   uint64_t q_ready;
   uint64_t q_conv;       // FP8: both CTAs' resident Q halves have landed (even CTA, 2 arrivals)
   uint64_t s_ready[NS], s_free[NS];
+  uint64_t qs_ready[Lay<F8>::NQ > 0 ? Lay<F8>::NQ : 1];  // bf16: streamed Q chunks (even CTA)
   uint64_t v_landed[NV], v_ready[NV], v_free[NV];
   uint64_t rs_ready[RS], rs_free[RS], rv_ready[RV], rv_free[RV];
   uint64_t s_full[2], s_empty[2];
@@ -287,6 +296,7 @@ __device__ __forceinline__ void init_barriers(BarsT<F8>* bars) {
       mbar_init(&bars->s_ready[s], F8 ? 2 : 1);
       mbar_init(&bars->s_free[s], 1);
     }
+    for (int s = 0; s < Ly::NQ; ++s) mbar_init(&bars->qs_ready[s], 1);
     for (int s = 0; s < kNV; ++s) {
       mbar_init(&bars->v_landed[s], 1);
       mbar_init(&bars->v_ready[s], F8 ? 2 : 1);
@@ -465,6 +475,17 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
     const long long prof_start = clock64();
 #endif
     const uint64_t pol_q = policy_evict_last();   // Q chunks are read again every tile
+    // Q chunk of S-phase step m into slot m % NQ. Issued after the key chunk of step m + NQ,
+    // whose slot was free only once the MMAs of step m + NQ - NS <= m - NQ completed, the
+    // last of them reading the slot's previous Q.
+    constexpr int kNQ = Ly::NQ;
+    static_assert(F8 || (kNQ >= 1 && 2 * kNQ >= kNS), "Q ring too shallow for the key ring");
+    auto load_q_chunk = [&](int m) {
+      const int qs = m % (kNQ > 0 ? kNQ : 1);
+      if (even) mbar_arrive_expect_tx(&bars->qs_ready[qs], 2 * 8192);
+      tma_load_2d_pair(sm + Ly::OFF_QS + qs * 8192, &tmQ, (m % kKCh) * 64, row * kH + (int)rank * 64,
+                       at_even(&bars->qs_ready[qs]), pol_q);
+    };
     auto load_s_chunk = [&](int c, int y0, int y1) -> bool {
       const int st = s_cnt % kNS;
       bool r = true;
@@ -475,7 +496,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       uint8_t* dst = sm + OFF_S + st * kSStage;
       tma_load_2d_pair(dst, &tmK, c * 64, y0, bar, pol_s);
       tma_load_2d_pair(dst + 8192, &tmK, c * 64, y1, bar, pol_s);
-      tma_load_2d_pair(dst + 16384, &tmQ, c * 64, row * kH + (int)rank * 64, bar, pol_q);
+      if (s_cnt >= kNQ) load_q_chunk(s_cnt - kNQ);
       TRACE(16, s_cnt);
       ++s_cnt;
       return true;
@@ -549,6 +570,18 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         }
       }
     }
+    // the Q chunks of the last NQ steps, each once the MMAs of step m - NQ (the previous
+    // user of its slot) have completed
+    if constexpr (!F8) {
+      if (ok && leader) {
+        for (int m = max(s_cnt - kNQ, 0); m < s_cnt && ok; ++m) {
+          const int x = m - kNQ;
+          if (x >= 0) ok = wait_bar(&bars->s_free[x % kNS], (uint32_t)(x / kNS) & 1u, cx);
+          if (ok) load_q_chunk(m);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
 #ifdef MLA_TC_TRACE
     prof[7] = clock64() - prof_start;
     if (leader) PROF_STORE(520);
@@ -569,9 +602,9 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       const uint32_t idS = idesc_bf16_f32(256, 128, 0, 0);
       // operand descriptors; an operand's start moves by adding (byte offset >> 4)
       const uint64_t dS = smem_desc(smem_u32(sm + OFF_S), 16, 1024, kSw128);
-      // bf16: each stage holds its Q chunk after the key chunk; FP8: Q is resident
+      // bf16: the streamed Q chunk of each step in its own 2-slot ring; FP8: Q is resident
       const uint64_t dQ = F8 ? smem_desc(smem_u32(sm + OFF_Q), 16, 1024, kSw128)
-                             : smem_desc(smem_u32(sm + OFF_S + 16384), 16, 1024, kSw128);
+                             : smem_desc(smem_u32(sm + Ly::OFF_QS), 16, 1024, kSw128);
       uint32_t s_st = 0, s_ph = 0;
 #ifdef MLA_TC_TRACE
       int s_cnt = 0;
@@ -637,12 +670,17 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         for (int c = 0; c < kKCh && ok; ++c) {
           TRACE(17, s_cnt);
           PROF(0, ok = wait_bar<F8>(&bars->s_ready[s_st], s_ph, cx));
+          // bf16: step m's Q chunk, slot m % NQ, the (m / NQ)-th use of that slot
+          const int m = t * kKCh + c;
+          constexpr int kNQ = Ly::NQ > 0 ? Ly::NQ : 1;
+          const uint32_t qslot = (uint32_t)(m % kNQ);
+          if (!F8 && ok) PROF(0, ok = wait_bar(&bars->qs_ready[qslot], (uint32_t)(m / kNQ) & 1u, cx));
           if (!ok) break;
           TRACE(18, s_cnt);
           PROF(2, tc_fence_after());
           // K chunk c (128 tokens x 64 dims per CTA) . Q chunk c^T, four K=16 steps
           const uint64_t a0 = dS + s_st * (uint32_t)(kSStage >> 4);
-          const uint64_t b0 = F8 ? dQ + (uint32_t)c * 512u : dQ + s_st * (uint32_t)(kSStage >> 4);
+          const uint64_t b0 = F8 ? dQ + (uint32_t)c * 512u : dQ + qslot * (8192u >> 4);
           PROF(1, {
             mma_bf16_pair(d, a0, b0, idS, c != 0);
             mma_bf16_pair(d, a0 + 2, b0 + 2, idS, 1);
@@ -1576,7 +1614,7 @@ __device__ __forceinline__ bool end_of_pass(int mode, uint8_t* sm) {
     }
     init_barriers<F8>(bars);
   }
-  if (tid < F_END - F_FLAG) flags[tid] = 0;
+  if (tid < F_FLAGS_END - F_FLAG) flags[tid] = 0;
   __syncthreads();
   cluster_sync();
   tc_fence_after();
@@ -1630,7 +1668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<F8>::THREADS, 1)
   if (tid == 0) TRACE(11, 0);
   if (tid == 0) init_barriers<F8>(bars);
   if (tid < kH) fs[F_M + tid] = -CUDART_INF_F;
-  if (tid < F_END - F_FLAG) flags[tid] = 0;
+  if (tid < F_FLAGS_END - F_FLAG) flags[tid] = 0;
   if (warp == 1) {
     tmem_alloc_pair(&bars->tmem_base, 512);
     tmem_relinquish_pair();
