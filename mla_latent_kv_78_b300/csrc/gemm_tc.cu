@@ -8,9 +8,9 @@
 //   * the decompression k^C = W^{UK} c, v^C = W^{UV} c of the non-absorbed prefill.
 // For decode-sized T the weights dominate the bytes, so a CTA owns 128 rows of W (the MMA's M,
 // TMEM lane = output feature) for a tile of 64 or 128 tokens (N) and streams its share of K
-// through a 6-stage TMA ring; K is split over CTAs when the (row, token) tiles alone leave SMs
-// idle, and the fp32 partials are summed in a fixed order by gemm_reduce_kernel (the result
-// does not depend on scheduling). Every wait is bounded.
+// through a TMA ring (9 stages for 64 tokens, 6 for 128); K is split over CTAs when the (row,
+// token) tiles alone leave SMs idle, and the fp32 partials are summed in a fixed order by
+// gemm_reduce_kernel (the result does not depend on scheduling). Every wait is bounded.
 #include "mla_internal.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.cuh"
@@ -22,12 +22,12 @@ using namespace ptx;
 
 constexpr int kBM = 128;       // rows of W per CTA
 constexpr int kBK = 64;        // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kStages = 6;
-constexpr int kGroup = 3;   // stages refilled per producer step (kStages is a multiple)
+constexpr int kGroup = 3;   // stages refilled per producer step (every ring depth is a multiple)
 constexpr long long kTimeout = 4000000000LL;
 
 template <int BN>
 struct GLay {
+  static constexpr int kStages = BN <= 64 ? 9 : 6;   // as deep as shared memory allows
   static constexpr int A = kBM * kBK * 2;       // 16 KB
   static constexpr int B = BN * kBK * 2;        // 8 or 16 KB
   static constexpr int STAGE = A + B;
@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(128, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const GemmParams p) {
   using Ly = GLay<BN>;
+  constexpr int kStages = Ly::kStages;
   extern __shared__ __align__(1024) uint8_t raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly::BARS);
