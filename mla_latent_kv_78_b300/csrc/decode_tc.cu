@@ -97,13 +97,13 @@ template <bool F8>
 struct Lay {
   // bf16: Q is streamed, chunk by chunk, next to the key chunks (a [64 heads x 64 dims] box
   // read from L2 per [128 tokens x 64 dims] key box), which frees 72 KB for deeper rings and
-  // two P^T buffers; its own NQ-slot ring trails the key ring by NQ chunks, so with
-  // 2 NQ >= NS a Q slot is always free once the key slot of the same step is. FP8: Q stays
-  // resident.
+  // two P^T buffers; its own NQ-slot ring (NQ <= NS) trails the key ring by NS - NQ chunks,
+  // so a Q slot is always free once the key slot of the same producer step is, and each Q
+  // chunk is requested NQ steps before its MMAs. FP8: Q stays resident.
   static constexpr bool QRES = F8;
   static constexpr int SSTAGE = 16384;      // S-phase stage bytes (key chunk)
   static constexpr int NS = F8 ? 2 : 4;     // S-phase ring
-  static constexpr int NQ = F8 ? 0 : 2;     // streamed Q chunks (bf16) [64 heads x 64 dims]
+  static constexpr int NQ = F8 ? 0 : 3;     // streamed Q chunks (bf16) [64 heads x 64 dims]
   static constexpr int NV = F8 ? 2 : 4;     // V-phase ring: [32 tok x 256 d_c] 16-bit = 16 KB
   static constexpr int PB = F8 ? 1 : 2;     // P^T buffers [256 tok x 64 heads] = 32 KB each
   static constexpr int RS = F8 ? 3 : 0;     // raw key-chunk slots (kRawS bytes)
@@ -475,11 +475,12 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
     const long long prof_start = clock64();
 #endif
     const uint64_t pol_q = policy_evict_last();   // Q chunks are read again every tile
-    // Q chunk of S-phase step m into slot m % NQ. Issued after the key chunk of step m + NQ,
-    // whose slot was free only once the MMAs of step m + NQ - NS <= m - NQ completed, the
-    // last of them reading the slot's previous Q.
+    // Q chunk of S-phase step m into slot m % NQ. Issued after the key chunk of step
+    // m + NS - NQ, whose slot was free only once the MMAs of step m - NQ completed, the last
+    // of them reading the slot's previous Q.
     constexpr int kNQ = Ly::NQ;
-    static_assert(F8 || (kNQ >= 1 && 2 * kNQ >= kNS), "Q ring too shallow for the key ring");
+    static_assert(F8 || (kNQ >= 1 && kNQ <= kNS), "Q ring deeper than the key ring");
+    constexpr int kLag = kNS - kNQ;
     auto load_q_chunk = [&](int m) {
       const int qs = m % (kNQ > 0 ? kNQ : 1);
       if (even) mbar_arrive_expect_tx(&bars->qs_ready[qs], 2 * 8192);
@@ -496,7 +497,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       uint8_t* dst = sm + OFF_S + st * kSStage;
       tma_load_2d_pair(dst, &tmK, c * 64, y0, bar, pol_s);
       tma_load_2d_pair(dst + 8192, &tmK, c * 64, y1, bar, pol_s);
-      if (s_cnt >= kNQ) load_q_chunk(s_cnt - kNQ);
+      if (s_cnt >= kLag) load_q_chunk(s_cnt - kLag);
       TRACE(16, s_cnt);
       ++s_cnt;
       return true;
@@ -570,11 +571,11 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         }
       }
     }
-    // the Q chunks of the last NQ steps, each once the MMAs of step m - NQ (the previous
+    // the Q chunks of the last NS - NQ steps, each once the MMAs of step m - NQ (the previous
     // user of its slot) have completed
     if constexpr (!F8) {
       if (ok && leader) {
-        for (int m = max(s_cnt - kNQ, 0); m < s_cnt && ok; ++m) {
+        for (int m = max(s_cnt - kLag, 0); m < s_cnt && ok; ++m) {
           const int x = m - kNQ;
           if (x >= 0) ok = wait_bar(&bars->s_free[x % kNS], (uint32_t)(x / kNS) & 1u, cx);
           if (ok) load_q_chunk(m);
