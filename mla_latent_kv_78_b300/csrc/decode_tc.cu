@@ -231,6 +231,22 @@ __device__ __forceinline__ float p16_to_f32(uint32_t h) { return __uint_as_float
 // Sum over the warp's 32 lanes of each of 32 values per lane; lane j returns the sum of
 // value j. Halving exchange: at each step a lane keeps one half of its values, sends the
 // other half to its partner and adds what it receives (31 shuffles in all).
+// Lane j gets the maximum over the warp's lanes of v[j] (a transposing butterfly: 31
+// shuffles for the 32 columns instead of 5 per column). Exact: max does not round.
+__device__ __forceinline__ float warp_transpose_max32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int q = 0; q < w; ++q) {
+      const float keep = hi ? v[q + w] : v[q];
+      const float send = hi ? v[q] : v[q + w];
+      v[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+    }
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1) {
@@ -1213,11 +1229,10 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
                 mbar_arrive_remote_relaxed(mapa(smem_u32(&bars->s_empty[par]), 0));
             }
           }
+          float v[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float mx = warp_max_f32(valid ? sv[c] * prm.scale_log2 : -CUDART_INF_F);
-            if (lane == c) run[h2] = fmaxf(run[h2], mx);
-          }
+          for (int c = 0; c < 32; ++c) v[c] = valid ? sv[c] * prm.scale_log2 : -CUDART_INF_F;
+          run[h2] = fmaxf(run[h2], warp_transpose_max32(v, lane));
         }
       }
       if (ok) {
@@ -1286,10 +1301,8 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
           tmem_ld32(s_addr + 32 * h2, s);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float mx = warp_max_f32(valid ? s[c] * prm.scale_log2 : -CUDART_INF_F);
-            if (lane == c) fs[F_COL + sw * 64 + 32 * h2 + c] = mx;
-          }
+          for (int c = 0; c < 32; ++c) s[c] = valid ? s[c] * prm.scale_log2 : -CUDART_INF_F;
+          fs[F_COL + sw * 64 + 32 * h2 + lane] = warp_transpose_max32(s, lane);
         }
         bar_sync(2, 256);
         // this CTA's per-head maxima go straight into the peer's shared memory (st.async,
@@ -1382,11 +1395,14 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         // ---- this tile's per-head maxima, published for the reference two tiles on: the
         // largest weight of each head (all relative to the same M) gives max s = M + log2(p)
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const uint32_t w = pk[c >> 1];
-          const float pv = p16_to_f32((c & 1) ? (w >> 16) : (w & 0xFFFFu));
-          const float mx = warp_max_f32(pv);
-          if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t w = pk[16 * h2 + (c >> 1)];
+            v[c] = p16_to_f32((c & 1) ? (w >> 16) : (w & 0xFFFFu));
+          }
+          fs[F_COL + sw * 64 + 32 * h2 + lane] = warp_transpose_max32(v, lane);
         }
         bar_sync(2, 256);
         if (stid < kH) {
