@@ -1229,10 +1229,20 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
                 mbar_arrive_remote_relaxed(mapa(smem_u32(&bars->s_empty[par]), 0));
             }
           }
-          float v[32];
+          if constexpr (!F8) {
+            float v[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = valid ? sv[c] * prm.scale_log2 : -CUDART_INF_F;
-          run[h2] = fmaxf(run[h2], warp_transpose_max32(v, lane));
+            for (int c = 0; c < 32; ++c) v[c] = valid ? sv[c] * prm.scale_log2 : -CUDART_INF_F;
+            run[h2] = fmaxf(run[h2], warp_transpose_max32(v, lane));
+          } else {
+            // (the FP8 instantiations keep one reduction per column: the transposing form
+            // measured slower there, through their register allocation)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float mx = warp_max_f32(valid ? sv[c] * prm.scale_log2 : -CUDART_INF_F);
+              if (lane == c) run[h2] = fmaxf(run[h2], mx);
+            }
+          }
         }
       }
       if (ok) {
@@ -1300,9 +1310,17 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
           float s[32];
           tmem_ld32(s_addr + 32 * h2, s);
           tmem_ld_wait();
+          if constexpr (!F8) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c] = valid ? s[c] * prm.scale_log2 : -CUDART_INF_F;
-          fs[F_COL + sw * 64 + 32 * h2 + lane] = warp_transpose_max32(s, lane);
+            for (int c = 0; c < 32; ++c) s[c] = valid ? s[c] * prm.scale_log2 : -CUDART_INF_F;
+            fs[F_COL + sw * 64 + 32 * h2 + lane] = warp_transpose_max32(s, lane);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float mx = warp_max_f32(valid ? s[c] * prm.scale_log2 : -CUDART_INF_F);
+              if (lane == c) fs[F_COL + sw * 64 + 32 * h2 + c] = mx;
+            }
+          }
         }
         bar_sync(2, 256);
         // this CTA's per-head maxima go straight into the peer's shared memory (st.async,
@@ -1394,15 +1412,25 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         any_over = true;
         // ---- this tile's per-head maxima, published for the reference two tiles on: the
         // largest weight of each head (all relative to the same M) gives max s = M + log2(p)
+        if constexpr (!F8) {
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float v[32];
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float v[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t w = pk[16 * h2 + (c >> 1)];
-            v[c] = p16_to_f32((c & 1) ? (w >> 16) : (w & 0xFFFFu));
+            for (int c = 0; c < 32; ++c) {
+              const uint32_t w = pk[16 * h2 + (c >> 1)];
+              v[c] = p16_to_f32((c & 1) ? (w >> 16) : (w & 0xFFFFu));
+            }
+            fs[F_COL + sw * 64 + 32 * h2 + lane] = warp_transpose_max32(v, lane);
           }
-          fs[F_COL + sw * 64 + 32 * h2 + lane] = warp_transpose_max32(v, lane);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const uint32_t w = pk[c >> 1];
+            const float pv = p16_to_f32((c & 1) ? (w >> 16) : (w & 0xFFFFu));
+            const float mx = warp_max_f32(pv);
+            if (lane == (c & 31)) fs[F_COL + sw * 64 + c] = mx;
+          }
         }
         bar_sync(2, 256);
         if (stid < kH) {
