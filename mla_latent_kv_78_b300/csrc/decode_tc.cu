@@ -12,9 +12,9 @@
 //    2-SM MMA (cta_group::2, M = 256 tokens, N = 128 heads): each CTA supplies its 128
 //    tokens' 576-d keys and HALF of Q (its 64 heads), and every MMA runs at full rate
 //    (N = 128). With a bf16 cache the Q half is not resident: each [128 tokens x 64 dims]
-//    key chunk is staged together with the matching [64 heads x 64 dims] Q chunk (an L2
-//    hit after the first tile), which leaves shared memory for a 3-deep key ring, a 4-deep
-//    latent ring and two P^T buffers.
+//    key chunk has its matching [64 heads x 64 dims] Q chunk (an L2 hit after the first
+//    tile) streamed through a 3-slot ring that trails the 4-deep key ring by one step, which
+//    leaves shared memory for a 4-deep latent ring and two P^T buffers.
 //  * The output is accumulated transposed, O^T[d_c][head] = V^T . P^T, again 2-SM
 //    (M = 256 latent rows per MMA, two MMAs per K step): each CTA holds half of O^T,
 //    256 TMEM columns, which leaves room for a double-buffered S^T (2 x 128 columns).
