@@ -13,7 +13,9 @@ L2 is flushed (a 2x-L2 buffer write) before every timed step, outside the
 step's events. `e2e` is the same metric through the public API with pinned
 HOST inputs copied in and the output copied back inside the timed region.
 `other_workloads` adds mla_decode timings of the ragged (128 x U[1024, 32768]),
-long-context (8 x 131072) and FP8 two-token (128 x 8192) workloads.
+long-context (8 x 131072) and FP8 two-token (128 x 8192) workloads, the last with
+the default (fused dequantising) kernel, with FP8 scores and with the cache staged
+to bf16 first; `next_rows` the fused upstream append, W^O and a prompt prefill.
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 workload. With N > 1 each rank runs an independent replica (the path has no
 exchange step), so `scaling` is weak.
