@@ -212,7 +212,9 @@ int mla_decode_kernel(const mla_config* cfg, int32_t batch, int32_t n_q);
  *   workspace   device scratch of >= mla_decode_workspace_size() bytes (may be
  *               NULL when that size is 0); contents need no initialisation.
  *   o_lat       [batch][n_q][H][C] act dtype;   lse [batch][n_q][H] fp32 or NULL
- * The result for a fixed num_splits is deterministic (no floating-point atomics).
+ * The result for a fixed num_splits is deterministic (no floating-point atomics). With
+ * num_splits = 0 the split schedule follows the device's SM count, so results are repeatable
+ * on one kind of GPU and may differ by rounding between GPUs with different SM counts.
  */
 int mla_decode(const mla_config* cfg, const void* q_lat, const void* kv_pool,
                const int32_t* block_table, int32_t max_pages_per_seq, int32_t num_pages,
