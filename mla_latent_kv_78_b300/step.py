@@ -94,12 +94,14 @@ class DecodeStep:
 
     # -- the step as one CUDA graph ----------------------------------------
     def capture(self, c_kv_new, k_r_new, q_c, q_r, timing: bool = False,
-                time_decode: bool = False) -> None:
+                time_decode: bool = False, branches: bool = False) -> None:
         """Record append -> absorb -> decode -> unabsorb over these input tensors as one CUDA
-        graph, so a step costs one graph launch instead of four host-side library calls. In the
-        graph the append and the absorption are independent branches that may overlap, and the
+        graph, so a step costs one graph launch instead of four host-side library calls. The
         decode and unabsorb kernels are programmatic launches that set up while their
-        predecessor finishes.
+        predecessor finishes. branches=True records the append and the absorption as parallel
+        branches joined before the decode; in series (the default) the step measured 1.6 us
+        faster (123.9 vs 125.5 us on the V2-shaped benchmark), the join costing more than the
+        overlap gains.
 
         The graph keeps the inputs' device addresses: write each step's inputs into the same
         tensors (copy_) before replay(). One eager step runs first, outside the capture, so
@@ -125,13 +127,17 @@ class DecodeStep:
             main = torch.cuda.current_stream(dev)
             if ev:
                 ev[0].record()
-            # the cache append and the query absorption touch disjoint buffers: they run side
-            # by side, and the decode waits for both
-            fork.wait_stream(main)
-            with torch.cuda.stream(fork):
+            if branches:
+                # the cache append and the query absorption touch disjoint buffers: they run
+                # side by side, and the decode waits for both
+                fork.wait_stream(main)
+                with torch.cuda.stream(fork):
+                    self.append(c_kv_new, k_r_new)
+                self.absorb(q_c, q_r)
+                main.wait_stream(fork)
+            else:
                 self.append(c_kv_new, k_r_new)
-            self.absorb(q_c, q_r)
-            main.wait_stream(fork)
+                self.absorb(q_c, q_r)
             if time_decode:
                 ev[1].record()
             self.decode()

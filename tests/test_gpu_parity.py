@@ -225,6 +225,28 @@ def test_decode_step_end_to_end(wl):
 
 
 @needs_cuda
+@pytest.mark.parametrize("branches", [False, True], ids=["series", "branches"])
+def test_captured_step_matches_the_eager_step(branches):
+    """The step recorded as one CUDA graph (append and absorb in series, or as parallel
+    branches) computes what the four calls do eagerly, bit for bit, replay after replay, and
+    matches the oracle."""
+    wl = SMALL_BF16_LONG
+    case = Case(wl)
+    case.run_step()
+    eager = case.step.o.clone()
+    case.step.capture(case.new_c, case.new_r, case.q_c, case.q_r, branches=branches)
+    for _ in range(3):
+        case.step.o.zero_()
+        case.step.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(case.step.o, eager)
+    assert case.step.status() == 0
+    for b in range(wl.B):
+        o, _, _ = case.oracle(b)
+        assert_close(wl, gpu_rows(case.step.o, wl, b), o, f"o[b={b}]")
+
+
+@needs_cuda
 @pytest.mark.parametrize("splits", [1, 3])
 def test_decode_is_deterministic(splits):
     wl = SMALL_BF16_LONG
