@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(128, 2)
   const uint32_t tmem = *slot;
   const int t = warp * 32 + lane;   // this thread's token (TMEM lane) in the tile
   griddep_launch_dependents();   // the decode may start its set-up while this grid finishes
+  // launched programmatically: the set-up above overlaps the preceding kernel (in a decode
+  // step, the cache append); every input is read after that kernel has completed, so this
+  // grid completes after it too
+  griddep_wait();
   // the six boxes from six lanes of warp 0: a warp's TMA loads issued by separate
   // instructions complete one after another on this part, those of one instruction overlap
   if (warp == 0) {
@@ -289,8 +293,9 @@ cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, co
     if (e != cudaSuccess) return e;
   }
   dim3 grid(d.H, 2, (T + tca::kAbsNT - 1) / tca::kAbsNT);
-  tca::absorb_tc_kernel<<<grid, 128, tca::kAbsSmem, stream>>>(tmW, tmQ, tmL, p);
-  return cudaGetLastError();
+  cudaError_t e = launch_programmatic(tca::absorb_tc_kernel, grid, dim3(128), tca::kAbsSmem, stream,
+                                      tmW, tmQ, tmL, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_unabsorb_tc(const Dims& d, const void* o_lat, int T, const void* w_uv, float* o,

@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, const In* __restric
                                                      int maxp, int num_pages,
                                                      uint8_t* __restrict__ pool,
                                                      int32_t* status, const RopeTable rt) {
+  // a kernel launched programmatically after this one (the query absorption of a decode step)
+  // may start its own set-up now; it reads its inputs only once this grid has completed
+  ptx::griddep_launch_dependents();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
