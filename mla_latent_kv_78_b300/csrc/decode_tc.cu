@@ -1273,7 +1273,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       // waits on each barrier; the others sleep in the named barrier, so no warp spins.
       bool ok1 = true;
       if (t >= 2) {
-        if (stid == 0) ok1 = wait_bar<true>(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx);
+        if (stid == 0) PROF(3, ok1 = wait_bar<true>(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx));
         ok = bar_and(12, 256, ok1);
         if (!ok) break;
       }
@@ -1294,7 +1294,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       if (F8 && Q8)
         ok1 = promote(t, par);
       else if (stid == 0)
-        ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx);
+        PROF(4, ok1 = wait_bar(&bars->s_full[par], (t >> 1) & 1, cx));
       ok = bar_and(1, 256, ok1);
       if (!ok) break;
       if (stid == 0) TRACE(3, t);
@@ -1403,7 +1403,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       bool ok3 = true;
       {
         const int wt = rescale ? t - 1 : t - kPB;   // (a rescale needs t >= 2)
-        if (wt >= 0 && stid == 0) ok3 = wait_bar(&bars->o_done[wt & 1], (wt >> 1) & 1, cx);
+        if (wt >= 0 && stid == 0) PROF(5, ok3 = wait_bar(&bars->o_done[wt & 1], (wt >> 1) & 1, cx));
       }
       bool any_over = false;
       if (bar_or(5, 256, over || !ok3)) {
