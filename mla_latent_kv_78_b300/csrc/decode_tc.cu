@@ -86,10 +86,13 @@ constexpr int FL_PEER_CLAMP = 8;   // the peer's FL_CLAMP, received with its epi
 constexpr int FL_PEER_ABORT = 9;   // the peer's FL_ABORT at the end of a pass
 constexpr int F_FLAGS_END = F_FLAG + 10;
 constexpr int F_SQ = F_FLAGS_END;    // [128 heads][4] FP8 scores: query group scales (both CTAs')
+// bf16: [128] the rescale factors of odd tiles (even tiles' at F_ALPHA): the relay warp folds a
+// tile's column sums of P into the running sums after the softmax has moved on to later tiles
+constexpr int F_ALPHA_ODD = F_FLAGS_END;
 // end of the fp32 scratch (even: the barriers that follow need 8-byte alignment); only the FP8
-// instantiations keep the query group scales
+// instantiations keep the query group scales, only the bf16 one the odd tiles' factors
 template <bool F8>
-constexpr int F_END = F8 ? F_SQ + 4 * kH : F_FLAGS_END;
+constexpr int F_END = F8 ? F_SQ + 4 * kH : F_ALPHA_ODD + kH;
 // Shared-memory layout. bf16 cache: keys and latents arrive by TMA in their MMA layout.
 // FP8 cache: raw codes and scales arrive by TMA in staging rings (RS, RV slots) and the
 // converter warps write bf16 operand tiles into the S and V rings.
@@ -133,6 +136,7 @@ struct BarsT {
   uint64_t rs_ready[RS], rs_free[RS], rv_ready[RV], rv_free[RV];
   uint64_t s_full[2], s_empty[2];
   uint64_t p_landed[2], p_ready[2], o_done[2];
+  uint64_t l_done[2];    // bf16: the relay has folded the tile's column sums of P in
   uint64_t gs_ready[2], gs_free[2];   // FP8 scores: latent code groups (even CTA / both)
   uint64_t q8_done;      // FP8 scores: Q quantised (the group ring may overwrite its bf16 rows)
   uint64_t sq_ready;     // FP8 scores: the peer's query group scales have landed
@@ -331,6 +335,7 @@ __device__ __forceinline__ void init_barriers(BarsT<F8>* bars) {
       mbar_init(&bars->s_empty[s], 16);
       mbar_init(&bars->p_landed[s], 8);
       mbar_init(&bars->p_ready[s], 2);
+      mbar_init(&bars->l_done[s], 1);
       mbar_init(&bars->o_done[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -1023,16 +1028,49 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
     // This CTA's P^T buffer of tile t is complete once its own softmax warps have written their
     // rows and the peer's rows and maxima have landed (p_landed); the relay makes the peer's
     // stores visible to the tensor core and reports the buffer to the even CTA's P.V issuer.
-    if (lane == 0) {
-      bool ok = true;
-      for (int t = 0; t < nt && ok; ++t) {
-        const int par = t & 1;
+    // bf16: then the whole warp sums the buffer's columns (each head of this CTA's half over
+    // the tile's 256 tokens) into running sums of P, scaled by the tile's factor when the
+    // reference moved; the softmax threads then need no cross-thread sum per tile.
+    bool ok = true;
+    float l0 = 0.f, l1 = 0.f;   // bf16: sums of P for heads 64 rank + 2 lane, + 1
+    for (int t = 0; t < nt && ok; ++t) {
+      const int par = t & 1;
+      if (lane == 0) {
         ok = wait_bar<true>(&bars->p_landed[par], (t >> 1) & 1, cx);
         TRACE(7, t);
         if (ok) {
           fence_proxy_async_smem();
           arrive_even(&bars->p_ready[par], rank);
         }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if constexpr (!F8) {
+        if (!ok) break;
+        // row r: 64 bf16 weights in 16-byte chunks, chunk c at (c ^ (r % 8)) * 16; lane j
+        // reads word j % 4 of chunk j / 4, i.e. heads 2j and 2j + 1
+        const uint8_t* buf = sm + OFF_P + (t % kPB) * 32768 + (lane & 3) * 4;
+        const int cc = lane >> 2;
+        float c0 = 0.f, c1 = 0.f;
+#pragma unroll 8
+        for (int r = 0; r < 256; ++r) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(buf + r * 128 + ((cc ^ (r & 7)) << 4));
+          c0 += p16_to_f32(w & 0xFFFFu);
+          c1 += p16_to_f32(w >> 16);
+        }
+        // the reference moves from tile 2 on, with the factor the softmax stored for tile t
+        if (t >= 2) {
+          const float* a = fs + (par ? F_ALPHA_ODD : F_ALPHA) + 64 * (int)rank + 2 * lane;
+          l0 *= a[0];
+          l1 *= a[1];
+        }
+        l0 += c0;
+        l1 += c1;
+        if (t == nt - 1) {
+          fs[F_LLOC + 64 * (int)rank + 2 * lane] = l0;
+          fs[F_LLOC + 64 * (int)rank + 2 * lane + 1] = l1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->l_done[par]);
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -1272,8 +1310,11 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       // ---- reference for tile t, from tile t-2's published maxima (both CTAs). One thread
       // waits on each barrier; the others sleep in the named barrier, so no warp spins.
       bool ok1 = true;
+      // bf16: this tile's rescale factors overwrite tile t - 2's, which the relay must have read
+      const int f_alpha = (!F8 && par) ? F_ALPHA_ODD : F_ALPHA;
       if (t >= 2) {
         if (stid == 0) PROF(3, ok1 = wait_bar<true>(&bars->p_landed[par], ((t - 2) >> 1) & 1, cx));
+        if (!F8 && stid == 0 && ok1) PROF(3, ok1 = wait_bar(&bars->l_done[par], ((t - 2) >> 1) & 1, cx));
         ok = bar_and(12, 256, ok1);
         if (!ok) break;
       }
@@ -1289,7 +1330,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
           fs[F_M + h] = cand;
           flags[FL_RESCALE + par] = 1;
         }
-        fs[F_ALPHA + h] = alpha;
+        fs[f_alpha + h] = alpha;
       }
       if (F8 && Q8)
         ok1 = promote(t, par);
@@ -1386,15 +1427,17 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
           pk[16 * h2 + 2 * c4] = pack_bf16x2(p[0], p[1]);
           pk[16 * h2 + 2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
         }
-        float v[32];
+        if constexpr (F8) {
+          float v[32];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          v[2 * c] = p16_to_f32(pk[16 * h2 + c] & 0xFFFFu);
-          v[2 * c + 1] = p16_to_f32(pk[16 * h2 + c] >> 16);
+          for (int c = 0; c < 16; ++c) {
+            v[2 * c] = p16_to_f32(pk[16 * h2 + c] & 0xFFFFu);
+            v[2 * c + 1] = p16_to_f32(pk[16 * h2 + c] >> 16);
+          }
+          const float lsum = warp_transpose_sum32(v, lane);
+          if (rescale) l_w[h2] *= fs[F_ALPHA + 64 * g + 32 * h2 + lane];
+          l_w[h2] += lsum;
         }
-        const float lsum = warp_transpose_sum32(v, lane);
-        if (rescale) l_w[h2] *= fs[F_ALPHA + 64 * g + 32 * h2 + lane];
-        l_w[h2] += lsum;
       }
       if (extreme) flags[FL_CLAMP] = 1;
       if (stid == 0) TRACE(14, t);
@@ -1464,7 +1507,7 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
             tmem_ld32(ta, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= fs[F_ALPHA + 64 * g + hh * 32 + x];
+            for (int x = 0; x < 32; ++x) o[x] *= fs[f_alpha + 64 * g + hh * 32 + x];
             tmem_st32(ta, o);
           }
         tmem_st_wait();
@@ -1560,26 +1603,38 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
       ok = bar_and(7, 256, ok);
       if (ok) {
         tc_fence_after();
-        // per-head sums of P over this warp's tokens
-        fs[F_COL + sw * 64 + lane] = l_w[0];
-        fs[F_COL + sw * 64 + 32 + lane] = l_w[1];
-        bar_and(8, 256, true);
         const uint32_t peer_l = mapa(smem_u32(fs + F_LRCV), peer);
         const uint32_t peer_l_bar = mapa(smem_u32(&bars->l_landed), peer);
-        if (stid < kH) {
-          const int h = stid, gg = h >> 6, cc = h & 63;
-          float sum = 0.f;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) sum += fs[F_COL + (gg * 4 + q) * 64 + cc];
-          fs[F_LLOC + h] = sum;
-          st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(sum), peer_l_bar);
-        }
         bool ok4 = true;
-        if (stid == 0) {
+        if constexpr (F8) {
+          // per-head sums of P over this warp's tokens, then over this CTA's tokens
+          fs[F_COL + sw * 64 + lane] = l_w[0];
+          fs[F_COL + sw * 64 + 32 + lane] = l_w[1];
+          bar_and(8, 256, true);
+          if (stid < kH) {
+            const int h = stid, gg = h >> 6, cc = h & 63;
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sum += fs[F_COL + (gg * 4 + q) * 64 + cc];
+            fs[F_LLOC + h] = sum;
+            st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(sum), peer_l_bar);
+          }
+        } else {
+          // the relay's sums over both CTAs' tokens for this CTA's 64 heads (after the last
+          // tile), to the peer, which has the other 64
+          bool okl = true;
+          if (stid == 0) okl = wait_bar(&bars->l_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
+          ok4 = bar_and(8, 256, okl);
+          if (ok4 && stid < 64) {
+            const int h = 64 * (int)rank + stid;
+            st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(fs[F_LLOC + h]), peer_l_bar);
+          }
+        }
+        if (stid == 0 && ok4) {
           // with the sums goes this CTA's clamp flag, so that both CTAs take the same decision
           st_async_b32(mapa(smem_u32(&flags[FL_PEER_CLAMP]), peer), (uint32_t)flags[FL_CLAMP],
                        peer_l_bar);
-          mbar_arrive_expect_tx(&bars->l_landed, kH * 4 + 4);
+          mbar_arrive_expect_tx(&bars->l_landed, (F8 ? kH : 64) * 4 + 4);
           ok4 = wait_bar<true>(&bars->l_landed, 0, cx);
         }
         ok4 = bar_and(14, 256, ok4);
@@ -1590,7 +1645,9 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         if (ok4 && !replay && stid < kH) {
           const int h = stid;
           const float mine = fs[F_LLOC + h], other = fs[F_LRCV + h];
-          const float Lsum = rank == 0 ? mine + other : other + mine;
+          // FP8: both CTAs' tokens summed here; bf16: each half's sum is whole in one CTA
+          const float Lsum = F8 ? (rank == 0 ? mine + other : other + mine)
+                                : ((h >> 6) == (int)rank ? mine : other);
           fs[F_INV + h] = Lsum > 0.f ? 1.f / Lsum : 0.f;
           if (rank == 0) {
             const float lse = Lsum > 0.f ? (fs[F_M + h] + log2f(Lsum)) * 0.6931471805599453f
