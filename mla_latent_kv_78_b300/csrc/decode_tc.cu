@@ -1066,8 +1066,20 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         l0 += c0;
         l1 += c1;
         if (t == nt - 1) {
-          fs[F_LLOC + 64 * (int)rank + 2 * lane] = l0;
-          fs[F_LLOC + 64 * (int)rank + 2 * lane + 1] = l1;
+          // the finished sums: kept, and sent to the peer (which holds the other 64 heads) while
+          // the last P.V still runs, together with this CTA's clamp flag (final: the softmax set
+          // it before its last P^T rows landed)
+          const int h = 64 * (int)rank + 2 * lane;
+          fs[F_LLOC + h] = l0;
+          fs[F_LLOC + h + 1] = l1;
+          const uint32_t peer_l = mapa(smem_u32(fs + F_LRCV + h), peer);
+          const uint32_t peer_l_bar = mapa(smem_u32(&bars->l_landed), peer);
+          st_async_b32(peer_l, __float_as_uint(l0), peer_l_bar);
+          st_async_b32(peer_l + 4, __float_as_uint(l1), peer_l_bar);
+          if (lane == 0) {
+            st_async_b32(mapa(smem_u32(&flags[FL_PEER_CLAMP]), peer), (uint32_t)flags[FL_CLAMP], peer_l_bar);
+            mbar_arrive_expect_tx(&bars->l_landed, 64 * 4 + 4);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->l_done[par]);
@@ -1619,23 +1631,19 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
             fs[F_LLOC + h] = sum;
             st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(sum), peer_l_bar);
           }
-        } else {
-          // the relay's sums over both CTAs' tokens for this CTA's 64 heads (after the last
-          // tile), to the peer, which has the other 64
-          bool okl = true;
-          if (stid == 0) okl = wait_bar(&bars->l_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
-          ok4 = bar_and(8, 256, okl);
-          if (ok4 && stid < 64) {
-            const int h = 64 * (int)rank + stid;
-            st_async_b32(peer_l + (uint32_t)(h * 4), __float_as_uint(fs[F_LLOC + h]), peer_l_bar);
-          }
         }
         if (stid == 0 && ok4) {
-          // with the sums goes this CTA's clamp flag, so that both CTAs take the same decision
-          st_async_b32(mapa(smem_u32(&flags[FL_PEER_CLAMP]), peer), (uint32_t)flags[FL_CLAMP],
-                       peer_l_bar);
-          mbar_arrive_expect_tx(&bars->l_landed, (F8 ? kH : 64) * 4 + 4);
-          ok4 = wait_bar<true>(&bars->l_landed, 0, cx);
+          if constexpr (F8) {
+            // with the sums goes this CTA's clamp flag, so that both CTAs take the same decision
+            st_async_b32(mapa(smem_u32(&flags[FL_PEER_CLAMP]), peer), (uint32_t)flags[FL_CLAMP],
+                         peer_l_bar);
+            mbar_arrive_expect_tx(&bars->l_landed, kH * 4 + 4);
+          } else {
+            // bf16: the relay sent this CTA's sums and flag after the last tile; its own
+            // sums are in F_LLOC once that has happened
+            ok4 = wait_bar(&bars->l_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, cx);
+          }
+          if (ok4) ok4 = wait_bar<true>(&bars->l_landed, 0, cx);
         }
         ok4 = bar_and(14, 256, ok4);
         // a clamped weight in either CTA: the outputs of this pass are not written, the unit
