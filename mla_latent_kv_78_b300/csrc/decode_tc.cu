@@ -231,6 +231,12 @@ __device__ __forceinline__ void trace(unsigned long long* buf, int unit, uint32_
 
 // One bf16 weight -> fp32, exactly.
 __device__ __forceinline__ float p16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+// lo += low bf16 of w, hi += high bf16 of w, each an fp32 add of the exact bf16 value
+__device__ __forceinline__ void add_bf16x2_f32(float& lo, float& hi, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(w));
+}
 
 // Sum over the warp's 32 lanes of each of 32 values per lane; lane j returns the sum of
 // value j. Halving exchange: at each step a lane keeps one half of its values, sends the
@@ -1049,14 +1055,18 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
         // row r: 64 bf16 weights in 16-byte chunks, chunk c at (c ^ (r % 8)) * 16; lane j
         // reads word j % 4 of chunk j / 4, i.e. heads 2j and 2j + 1
         const uint8_t* buf = sm + OFF_P + (t % kPB) * 32768 + (lane & 3) * 4;
+        // (even and odd rows in separate chains; each bf16 half enters its fp32 add directly)
         const int cc = lane >> 2;
-        float c0 = 0.f, c1 = 0.f;
+        float c0 = 0.f, c1 = 0.f, d0 = 0.f, d1 = 0.f;
 #pragma unroll 8
-        for (int r = 0; r < 256; ++r) {
+        for (int r = 0; r < 256; r += 2) {
           const uint32_t w = *reinterpret_cast<const uint32_t*>(buf + r * 128 + ((cc ^ (r & 7)) << 4));
-          c0 += p16_to_f32(w & 0xFFFFu);
-          c1 += p16_to_f32(w >> 16);
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(buf + (r + 1) * 128 + ((cc ^ ((r + 1) & 7)) << 4));
+          add_bf16x2_f32(c0, c1, w);
+          add_bf16x2_f32(d0, d1, x);
         }
+        c0 += d0;
+        c1 += d1;
         // the reference moves from tile 2 on, with the factor the softmax stored for tile t
         if (t >= 2) {
           const float* a = fs + (par ? F_ALPHA_ODD : F_ALPHA) + 64 * (int)rank + 2 * lane;
