@@ -2,8 +2,9 @@
 
 A step is one pass of the whole decode hot path over the DeepSeek-V2-shaped
 workload (batch 64, 128 heads, d_h 128, d_c 512, d_h^R 64, 4096 cached tokens
-per sequence, bf16 cache, one query token): mla_append_cache (this step's 64
-tokens) -> mla_absorb_q -> mla_decode (+ combine) -> mla_unabsorb.
+per sequence, bf16 cache, one query token): mla_append_absorb (the cache append
+of this step's 64 tokens and the query absorption, overlapped) -> mla_decode
+(+ combine) -> mla_unabsorb.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 

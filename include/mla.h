@@ -176,6 +176,22 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
                  int32_t num_tokens, const void* w_uk, void* q_lat, void* stream);
 
 /*
+ * mla_append_absorb — the two inputs of a decode step in one call: mla_append_cache of the
+ * step's new tokens, then mla_absorb_q of its queries, with the same pos [T] for both (each
+ * token's position). Arguments, layouts and results exactly as those two calls; every
+ * argument of both is checked before anything is launched, and MLA_OK means both were
+ * queued. The absorption reads none of what the append writes, so it does not wait for the
+ * append to finish before reading its own inputs: the two overlap on the device. A kernel
+ * queued after this call still finds both the cache entries and q_lat complete. The buffers
+ * of the two halves must not overlap.
+ */
+int mla_append_absorb(const mla_config* cfg, const void* c_kv, const void* k_r,
+                      const int32_t* seq_idx, const int32_t* pos, int32_t num_tokens,
+                      const int32_t* block_table, int32_t batch, int32_t max_pages_per_seq,
+                      int32_t num_pages, void* kv_pool, int32_t* dev_status, const void* q_c,
+                      const void* q_r, const void* w_uk, void* q_lat, void* stream);
+
+/*
  * Workspace bytes mla_decode needs for these sizes: the fp32 split partials (one [C] output
  * and one log-sum-exp per query row, head and split) when the rows are split over several
  * ranges (num_splits, or the automatic choice, above 1). The tensor-core kernels also keep

@@ -22,6 +22,7 @@ from ._lib import (  # noqa: F401
     lib,
     make_config,
     mla_absorb_q,
+    mla_append_absorb,
     mla_append_cache,
     mla_cache_entry_bytes,
     mla_config,

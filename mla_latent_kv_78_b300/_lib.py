@@ -84,6 +84,8 @@ _SIGS = {
     "mla_append_cache": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _P, _I, _P, _I, _I,
                                         _I, _P, _P, _P]),
     "mla_absorb_q": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _I, _P, _P, _P]),
+    "mla_append_absorb": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _P, _I, _P, _I, _I,
+                                         _I, _P, _P, _P, _P, _P, _P, _P]),
     "mla_decode_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(mla_config), _I, _I, _I, _I]),
     "mla_decode_kernel": (ctypes.c_int, [ctypes.POINTER(mla_config), _I, _I]),
     "mla_decode": (ctypes.c_int, [ctypes.POINTER(mla_config), _P, _P, _P, _I, _I, _P, _I, _I, _I,
@@ -165,6 +167,21 @@ def mla_absorb_q(cfg: mla_config, q_c, q_r, pos, w_uk, q_lat, stream=None) -> No
     T = q_c.shape[0]
     _check("mla_absorb_q", lib().mla_absorb_q(ctypes.byref(cfg), _ptr(q_c), _ptr(q_r), _ptr(pos),
                                               T, _ptr(w_uk), _ptr(q_lat), _stream(stream)))
+
+
+def mla_append_absorb(cfg: mla_config, c_kv, k_r, seq_idx, pos, block_table, kv_pool, q_c, q_r,
+                      w_uk, q_lat, num_pages: Optional[int] = None, dev_status=None,
+                      stream=None) -> None:
+    T = c_kv.shape[0]
+    if q_c.shape[0] != T:
+        raise ValueError("c_kv and q_c must hold the same tokens")
+    batch, maxp = block_table.shape
+    if num_pages is None:
+        num_pages = kv_pool.shape[0]
+    _check("mla_append_absorb", lib().mla_append_absorb(
+        ctypes.byref(cfg), _ptr(c_kv), _ptr(k_r), _ptr(seq_idx), _ptr(pos), T, _ptr(block_table),
+        batch, maxp, num_pages, _ptr(kv_pool), _ptr(dev_status), _ptr(q_c), _ptr(q_r),
+        _ptr(w_uk), _ptr(q_lat), _stream(stream)))
 
 
 def mla_decode_workspace_size(cfg: mla_config, batch: int, n_q: int, max_seq_len: int,

@@ -30,6 +30,11 @@ struct AbsorbParams {
   const int32_t* pos;
   __nv_bfloat16* q_lat;
   int32_t* status;
+  // 1: launched right behind a cache append, which writes none of this kernel's inputs, so
+  // they are read at once and the append is waited for only before exiting (a kernel that
+  // waits for this grid then also finds the append complete); 0: every input is read after
+  // the preceding kernel has completed
+  int early_inputs;
   float theta_hi[kR / 2], theta_lo[kR / 2];   // RoPE frequencies base^(-2k/R) as hi + lo floats
 };
 
@@ -85,20 +90,21 @@ __global__ void __launch_bounds__(128, 2)
   const uint32_t tmem = *slot;
   const int t = warp * 32 + lane;   // this thread's token (TMEM lane) in the tile
   griddep_launch_dependents();   // the decode may start its set-up while this grid finishes
-  // launched programmatically: the set-up above overlaps the preceding kernel (in a decode
-  // step, the cache append); every input is read after that kernel has completed, so this
-  // grid completes after it too
-  griddep_wait();
-  // the six boxes from six lanes of warp 0: a warp's TMA loads issued by separate
-  // instructions complete one after another on this part, those of one instruction overlap
+  // launched programmatically: the set-up above and the weight loads overlap the preceding
+  // kernel (in a decode step, the cache append), which never writes W^{UK}; q_c, q^R and the
+  // positions are read after that kernel has completed unless early_inputs says they may be
+  // read at once, and this grid completes after that kernel either way.
+  // The six boxes come from six lanes of warp 0: a warp's TMA loads issued by separate
+  // instructions complete one after another on this part, those of one instruction overlap.
+  const uint64_t pol = policy_evict_first();
   if (warp == 0) {
-    const uint64_t pol = policy_evict_first();
     if (lane == 0) mbar_arrive_expect_tx(&bars[0], 6 * 16384);
     __syncwarp();
-    if (lane < 2) tma_load_3d(sA + lane * 16384, &tmQ, lane * 64, i, t0, &bars[0], pol);
-    else if (lane < 6)
+    if (lane >= 2 && lane < 6)
       tma_load_2d(sB + (lane - 2) * 16384, &tmW, (4 * half + lane - 2) * 64, i * kD, &bars[0], pol);
   }
+  if (!p.early_inputs) griddep_wait();
+  if (warp == 0 && lane < 2) tma_load_3d(sA + lane * 16384, &tmQ, lane * 64, i, t0, &bars[0], pol);
   // the first half's CTA also rotates q^R while the operands land: two threads per token,
   // 16 RoPE pairs each, all four 16-byte loads issued before any is used
   const uint32_t rsw = (uint32_t)(t & 7);
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__(128, 2)
   if (threadIdx.x == 0) bulk_wait_read_all();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
+  if (p.early_inputs) griddep_wait();
 }
 
 // ------------------------------------------------------------------ unabsorb
@@ -205,19 +212,17 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
-  // launched programmatically after the decode: the set-up above overlaps its tail, the inputs
-  // are read only once it has completed
-  griddep_wait();
-  // slice j's two boxes from lane j of warp 0 (one instruction per box kind for all slices)
-  if (warp == 0) {
-    const uint64_t pol = policy_evict_first();
-    if (lane < 8) {
-      mbar_arrive_expect_tx(&bars[lane], 16384 + 8192);
-      tma_load_2d(sA + lane * 16384, &tmW, lane * 64, i * kD, &bars[lane], pol);
-      tma_load_3d(sB + lane * 8192, &tmO, lane * 64, i, t0, &bars[lane], pol);
-    }
-    __syncwarp();
+  // launched programmatically after the decode: the set-up above and the loads of W^{UV} (which
+  // the decode never writes) overlap its tail; o_lat is read only once it has completed.
+  // Slice j's two boxes from lane j of warp 0 (one instruction per box kind for all slices).
+  const uint64_t pol = policy_evict_first();
+  if (warp == 0 && lane < 8) {
+    mbar_arrive_expect_tx(&bars[lane], 16384 + 8192);
+    tma_load_2d(sA + lane * 16384, &tmW, lane * 64, i * kD, &bars[lane], pol);
   }
+  griddep_wait();
+  if (warp == 0 && lane < 8) tma_load_3d(sB + lane * 8192, &tmO, lane * 64, i, t0, &bars[lane], pol);
+  __syncwarp();
   if (threadIdx.x == 0) {
     const uint32_t id = idesc_bf16_f32(128, kUnNT, 0, 0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
@@ -255,7 +260,8 @@ bool absorb_tc_supported(const Dims& d) {
 }
 
 cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, const int32_t* pos,
-                             int T, const void* w_uk, void* q_lat, cudaStream_t stream) {
+                             int T, const void* w_uk, void* q_lat, cudaStream_t stream,
+                             bool early_inputs) {
   CUtensorMap tmW, tmQ, tmL;
   {
     const uint64_t dims[2] = {(uint64_t)tca::kC, (uint64_t)d.H * tca::kD};
@@ -282,6 +288,7 @@ cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, co
   p.pos = pos;
   p.q_lat = static_cast<__nv_bfloat16*>(q_lat);
   p.status = nullptr;
+  p.early_inputs = early_inputs ? 1 : 0;
   for (int k = 0; k < tca::kR / 2; ++k) {
     const double th = rope_theta_host(d, k);
     p.theta_hi[k] = (float)th;

@@ -147,6 +147,37 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
   return cuda_rc(mla::launch_absorb(d, q_c, q_r, pos, num_tokens, w_uk, q_lat, (cudaStream_t)stream));
 }
 
+int mla_append_absorb(const mla_config* cfg, const void* c_kv, const void* k_r,
+                      const int32_t* seq_idx, const int32_t* pos, int32_t num_tokens,
+                      const int32_t* block_table, int32_t batch, int32_t max_pages_per_seq,
+                      int32_t num_pages, void* kv_pool, int32_t* dev_status, const void* q_c,
+                      const void* q_r, const void* w_uk, void* q_lat, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc != MLA_OK) return rc;
+  if (num_tokens < 0 || batch < 0 || max_pages_per_seq < 0 || num_pages < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  // every argument of both halves is checked before anything is launched
+  if (!c_kv || !k_r || !seq_idx || !pos || !block_table || !kv_pool || batch < 1 ||
+      max_pages_per_seq < 1 || num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!q_c || (!q_r && d.R > 0) || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
+  if (d.cache_dtype == MLA_FP8_E4M3 && !aligned16(kv_pool)) return MLA_ERR_ALIGNMENT;
+  const bool tc = mla::absorb_tc_supported(d) && cfg->kernel != MLA_KERNEL_SIMT;
+  if (tc && (!aligned16(q_c) || !aligned16(q_r) || !aligned16(w_uk) || !aligned16(q_lat)))
+    return MLA_ERR_ALIGNMENT;
+  const cudaStream_t s = (cudaStream_t)stream;
+  rc = cuda_rc(mla::launch_append(d, c_kv, k_r, seq_idx, pos, num_tokens, block_table, batch,
+                                  max_pages_per_seq, num_pages, kv_pool, dev_status, s));
+  if (rc != MLA_OK) return rc;
+  // the append is an ordinary launch (everything before it on the stream has completed when
+  // it starts) and writes only the cache, so the absorption behind it may read its inputs at
+  // once; it still completes only after the append has
+  if (tc) return cuda_rc(mla::launch_absorb_tc(d, q_c, q_r, pos, num_tokens, w_uk, q_lat, s, true));
+  return cuda_rc(mla::launch_absorb(d, q_c, q_r, pos, num_tokens, w_uk, q_lat, s));
+}
+
 size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t n_q,
                                  int32_t max_seq_len, int32_t num_splits) {
   Dims d;

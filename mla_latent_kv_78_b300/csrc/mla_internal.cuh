@@ -53,8 +53,11 @@ cudaError_t launch_unabsorb(const Dims& d, const void* o_lat, int T, const void*
 
 // Tensor-core absorb / unabsorb (d_h = 128, d_c = 512, d_h^R = 64, bf16).
 bool absorb_tc_supported(const Dims& d);
+// early_inputs: launched right behind launch_append on the same stream (which writes none of
+// q_c, q_r, pos, w_uk); the inputs are then read before the append has completed.
 cudaError_t launch_absorb_tc(const Dims& d, const void* q_c, const void* q_r, const int32_t* pos,
-                             int T, const void* w_uk, void* q_lat, cudaStream_t stream);
+                             int T, const void* w_uk, void* q_lat, cudaStream_t stream,
+                             bool early_inputs = false);
 cudaError_t launch_unabsorb_tc(const Dims& d, const void* o_lat, int T, const void* w_uv, float* o,
                                cudaStream_t stream);
 

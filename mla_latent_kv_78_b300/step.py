@@ -76,6 +76,12 @@ class DecodeStep:
     def absorb(self, q_c, q_r, stream=None) -> None:
         L.mla_absorb_q(self.cfg, q_c, q_r, self.step_pos, self.w_uk, self.q_lat, stream)
 
+    def append_absorb(self, c_kv_new, k_r_new, q_c, q_r, stream=None) -> None:
+        """append() then absorb() as one library call, the absorption overlapping the append."""
+        L.mla_append_absorb(self.cfg, c_kv_new, k_r_new, self.step_seq, self.step_pos,
+                            self.block_table, self.pool, q_c, q_r, self.w_uk, self.q_lat,
+                            self.num_pages, self.dev_status, stream)
+
     def decode(self, q_lat: Optional[torch.Tensor] = None, stream=None) -> None:
         L.mla_decode(self.cfg, self.q_lat if q_lat is None else q_lat, self.pool, self.block_table,
                      self.seq_lens, self.n_q, self.max_seq_len, self.o_lat, self.lse,
@@ -85,9 +91,8 @@ class DecodeStep:
         L.mla_unabsorb(self.cfg, self.o_lat, self.w_uv, self.o, stream)
 
     def step(self, c_kv_new, k_r_new, q_c, q_r, stream=None) -> torch.Tensor:
-        """append -> absorb -> decode (+combine) -> unabsorb; returns o [B*n_q, H, D] fp32."""
-        self.append(c_kv_new, k_r_new, stream)
-        self.absorb(q_c, q_r, stream)
+        """append + absorb -> decode (+combine) -> unabsorb; returns o [B*n_q, H, D] fp32."""
+        self.append_absorb(c_kv_new, k_r_new, q_c, q_r, stream)
         self.decode(None, stream)
         self.unabsorb(stream)
         return self.o
@@ -95,13 +100,14 @@ class DecodeStep:
     # -- the step as one CUDA graph ----------------------------------------
     def capture(self, c_kv_new, k_r_new, q_c, q_r, timing: bool = False,
                 time_decode: bool = False, branches: bool = False) -> None:
-        """Record append -> absorb -> decode -> unabsorb over these input tensors as one CUDA
-        graph, so a step costs one graph launch instead of four host-side library calls. The
-        decode and unabsorb kernels are programmatic launches that set up while their
-        predecessor finishes. branches=True records the append and the absorption as parallel
-        branches joined before the decode; in series (the default) the step measured 1.6 us
-        faster (123.9 vs 125.5 us on the V2-shaped benchmark), the join costing more than the
-        overlap gains.
+        """Record append + absorb (one mla_append_absorb call) -> decode -> unabsorb over these
+        input tensors as one CUDA graph, so a step costs one graph launch instead of several
+        host-side library calls. The absorption, decode and unabsorb kernels are programmatic
+        launches that set up while their predecessor finishes; the absorption also reads its
+        inputs while the append runs. branches=True records separate append and absorb calls as
+        parallel branches joined before the decode instead; that measured 1.6 us slower than
+        the two separate calls in series (125.5 vs 123.9 us on the V2-shaped benchmark), and the
+        single call beats both (116.6 vs 119.8 us in series).
 
         The graph keeps the inputs' device addresses: write each step's inputs into the same
         tensors (copy_) before replay(). One eager step runs first, outside the capture, so
@@ -136,8 +142,7 @@ class DecodeStep:
                 self.absorb(q_c, q_r)
                 main.wait_stream(fork)
             else:
-                self.append(c_kv_new, k_r_new)
-                self.absorb(q_c, q_r)
+                self.append_absorb(c_kv_new, k_r_new, q_c, q_r)
             if time_decode:
                 ev[1].record()
             self.decode()

@@ -49,8 +49,12 @@ def test_host_argument_checks_return_codes():
     assert lib.mla_append_cache(by(cfg), None, None, None, None, 4, None, 1, 1, 1, None, None, None) == L.MLA_ERR_INVALID_ARG
     assert lib.mla_absorb_q(by(cfg), None, None, None, 4, None, None, None) == L.MLA_ERR_INVALID_ARG
     assert lib.mla_unabsorb(by(cfg), None, 4, None, None, None) == L.MLA_ERR_INVALID_ARG
+    assert lib.mla_append_absorb(by(cfg), None, None, None, None, 4, None, 1, 1, 1, None, None, None, None,
+                                 None, None, None) == L.MLA_ERR_INVALID_ARG
     # empty work is a no-op that launches nothing
     assert lib.mla_append_cache(by(cfg), None, None, None, None, 0, None, 1, 1, 1, None, None, None) == L.MLA_OK
+    assert lib.mla_append_absorb(by(cfg), None, None, None, None, 0, None, 1, 1, 1, None, None, None, None,
+                                 None, None, None) == L.MLA_OK
     assert lib.mla_decode(by(cfg), None, None, None, 1, 1, None, 0, 1, 1, 0, None, 0, None, None, None, None) == L.MLA_OK
     # max_seq_len beyond the page table's reach
     assert lib.mla_decode(by(cfg), 16, 16, 16, 2, 4, 16, 1, 1, 129, 0, None, 0, 16, None, None, None) == L.MLA_ERR_INVALID_ARG

@@ -247,6 +247,22 @@ def test_captured_step_matches_the_eager_step(branches):
 
 
 @needs_cuda
+@pytest.mark.parametrize("wl", [TINY, SMALL_BF16, SMALL_FP8, SMALL_BF16_T200], ids=lambda w: w.name + f"-T{w.B * w.n_q}")
+def test_append_absorb_equals_the_two_calls(wl):
+    """mla_append_absorb (the absorption overlapping the append) leaves the pool and q_lat
+    exactly as mla_append_cache followed by mla_absorb_q."""
+    sep = Case(wl)
+    sep.step.append(sep.new_c, sep.new_r)
+    sep.step.absorb(sep.q_c, sep.q_r)
+    fused = Case(wl)
+    fused.step.append_absorb(fused.new_c, fused.new_r, fused.q_c, fused.q_r)
+    torch.cuda.synchronize()
+    assert torch.equal(sep.step.pool, fused.step.pool)
+    assert torch.equal(sep.step.q_lat, fused.step.q_lat)
+    assert fused.step.status() == 0
+
+
+@needs_cuda
 @pytest.mark.parametrize("splits", [1, 3])
 def test_decode_is_deterministic(splits):
     wl = SMALL_BF16_LONG
