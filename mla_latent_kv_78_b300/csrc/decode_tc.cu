@@ -589,33 +589,10 @@ __device__ __forceinline__ void decode_pass(const Maps& maps, const Params& prm,
           ok = c < 8 ? load_raw_s(false, c, ys0, ys1) : load_raw_s(true, 0, c == 8 ? ys0 : ys1, 0);
         }
       } else {
-        // With each key chunk, an L2 prefetch of the chunk kPf steps later (the same two
-        // boxes, no shared memory, nothing to wait for): its ring load, issued once a slot
-        // frees, then finds the bytes on their way, so more HBM bytes are in flight per SM
-        // than the ring holds. Measured (interleaved, 64 x 4096 / ragged / long): kPf = 1
-        // -4.4 % / -4.4 % / -3.9 %; 2, 3 and 4 slightly less; 9 (a tile ahead) nothing.
-        constexpr int kPf = 1;
-        int nys0 = -1, nys1 = -1;
-        if (kPf > 0 && k + 1 < nt) {
-          nys0 = page_y(4 * (k + 1) + 2 * (int)rank);
-          nys1 = page_y(4 * (k + 1) + 2 * (int)rank + 1);
-        }
-        const int ylim = prm.num_pages * kP;
-        auto prefetch_key = [&](int c, int y0, int y1) {
-          if (y0 < ylim) tma_prefetch_2d(&tmK, c * 64, y0, pol_s);
-          if (y1 < ylim) tma_prefetch_2d(&tmK, c * 64, y1, pol_s);
-        };
         for (int c = 0; c < kKCh && ok; ++c) {
           if (leader) {
             if (c == 4) TRACE(15, k);
             ok = load_s_chunk(c, ys0, ys1);
-            if (kPf > 0 && ok) {
-              const int cp = c + kPf;
-              if (cp < kKCh)
-                prefetch_key(cp, ys0, ys1);
-              else if (nys0 >= 0 && cp - kKCh < kKCh)
-                prefetch_key(cp - kKCh, nys0, nys1);
-            }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }

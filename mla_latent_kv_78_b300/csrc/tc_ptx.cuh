@@ -121,14 +121,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// L2 prefetch of one tile of a tensor (no shared-memory destination, no completion signal)
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "l"(policy)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             uint64_t* bar, uint64_t policy) {
   asm volatile(
