@@ -29,7 +29,12 @@ def build(verbose: bool = False, extra=None) -> str:
     newest = max(os.path.getmtime(p) for p in srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC)])
     hdr = os.path.join(os.path.dirname(HERE), "include", "mla.h")
     newest = max(newest, os.path.getmtime(hdr), os.path.getmtime(__file__))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= newest and not extra:
+    # the library is current only if it is newer than every source and was built with the
+    # same extra flags (a stamp beside it records them)
+    flags = " ".join(extra or [])
+    stamp = LIB + ".flags"
+    built_with = open(stamp).read() if os.path.exists(stamp) else None
+    if os.path.exists(LIB) and os.path.getmtime(LIB) >= newest and built_with == flags:
         return LIB
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-Xptxas", "-v" if verbose else "-O3",
@@ -41,6 +46,8 @@ def build(verbose: bool = False, extra=None) -> str:
     if verbose:
         sys.stderr.write(r.stderr)
     os.replace(LIB + ".tmp", LIB)
+    with open(stamp, "w") as f:
+        f.write(flags)
     return LIB
 
 
