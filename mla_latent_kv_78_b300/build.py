@@ -23,18 +23,26 @@ def nvcc() -> str:
     return "nvcc"
 
 
+def is_current(lib: str, newest_source: float, flags: str) -> bool:
+    """The library is current only if it is newer than every source and was built with the
+    same extra flags (a stamp beside it, lib + ".flags", records them)."""
+    stamp = lib + ".flags"
+    if not os.path.exists(lib) or not os.path.exists(stamp):
+        return False
+    with open(stamp) as f:
+        built_with = f.read()
+    return os.path.getmtime(lib) >= newest_source and built_with == flags
+
+
 def build(verbose: bool = False, extra=None) -> str:
     """Compile every .cu under csrc/ into one shared library. Returns its path."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     newest = max(os.path.getmtime(p) for p in srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC)])
     hdr = os.path.join(os.path.dirname(HERE), "include", "mla.h")
     newest = max(newest, os.path.getmtime(hdr), os.path.getmtime(__file__))
-    # the library is current only if it is newer than every source and was built with the
-    # same extra flags (a stamp beside it records them)
     flags = " ".join(extra or [])
     stamp = LIB + ".flags"
-    built_with = open(stamp).read() if os.path.exists(stamp) else None
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= newest and built_with == flags:
+    if is_current(LIB, newest, flags):
         return LIB
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "--expt-relaxed-constexpr", "-Xptxas", "-v" if verbose else "-O3",
