@@ -180,10 +180,10 @@ int mla_absorb_q(const mla_config* cfg, const void* q_c, const void* q_r, const 
  * step's new tokens, then mla_absorb_q of its queries, with the same pos [T] for both (each
  * token's position). Arguments, layouts and results exactly as those two calls; every
  * argument of both is checked before anything is launched, and MLA_OK means both were
- * queued. The absorption reads none of what the append writes, so it does not wait for the
- * append to finish before reading its own inputs: the two overlap on the device. A kernel
- * queued after this call still finds both the cache entries and q_lat complete. The buffers
- * of the two halves must not overlap.
+ * queued. The absorption reads none of what the append writes, so the tensor-core absorption
+ * reads its own inputs without waiting for the append to finish, and the two overlap on the
+ * device. A kernel queued after this call still finds both the cache entries and q_lat
+ * complete. The buffers of the two halves must not overlap.
  */
 int mla_append_absorb(const mla_config* cfg, const void* c_kv, const void* k_r,
                       const int32_t* seq_idx, const int32_t* pos, int32_t num_tokens,
